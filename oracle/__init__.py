@@ -1,0 +1,357 @@
+"""The oracle: a plain, slow, obviously correct CPU statement of the paged decode path.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  It shares no code
+with ``paged_kv_cache_12_gb300`` (neither imports the other); the only module
+both sides use is the seeded input generator, which holds none of the method's
+arithmetic.
+
+Contents, each with the passage it follows:
+
+* ``kv_bytes_per_token`` -- the KV-size formula of "PagedAttention de vLLM :
+  comment la gestion de la VRAM soutient l'inference des grands modeles"
+  (deepsonar.com.cn), section 2.1.
+* ``OracleAllocator`` -- fixed-size blocks, per-sequence block table and
+  allocation on demand (deepsonar page section 2.2 and section VII steps 1-3;
+  "PagedAttention : comment optimiser la memoire GPU lors de l'inference des
+  LLM" (deeplearn.tn), section "Un exemple concret d'allocation"), reference
+  counts with copy-on-write (deepsonar page section 2.3), free queue handing out
+  from the head and taking freed blocks back at the tail (deepsonar page
+  section 2.4).
+* ``kv_write`` / ``block_copy`` -- the new token's K/V go into the free slot of
+  the sequence's current block (deeplearn.tn page, same section); a writer that
+  finds a shared block copies it first (deepsonar page section 2.3).
+* ``paged_decode`` / ``paged_decode_split`` -- fp64 attention over the gathered
+  history, in C (``oracle.c``), see that file's header for the passages.
+
+Readings where the pages are silent are listed with each function.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from collections import deque
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library with the host C compiler."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if force or not os.path.exists(_LIB_PATH) or os.path.getmtime(_LIB_PATH) < os.path.getmtime(_SRC):
+        tmp = _LIB_PATH + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lib_lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i32, i64, dbl, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
+            lib.or_half_to_double.argtypes = [ctypes.c_uint16]
+            lib.or_half_to_double.restype = dbl
+            common = [vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i64, i64, i64, dbl]
+            lib.or_paged_decode.argtypes = common + [i32, i32]
+            lib.or_paged_decode.restype = i32
+            lib.or_paged_decode_split.argtypes = common + [i32, i32, i32]
+            lib.or_paged_decode_split.restype = i32
+            _lib = lib
+    return _lib
+
+
+def half_to_double(bits: int) -> float:
+    """The C oracle's own binary16 -> double conversion, for pinning it."""
+    return _load().or_half_to_double(int(bits) & 0xFFFF)
+
+
+# ---------------------------------------------------------------------------
+# KV-size formula
+# ---------------------------------------------------------------------------
+
+def kv_bytes_per_token(num_layers: int, num_kv_heads: int, head_dim: int, bytes_per_elem: int) -> int:
+    """KV-cache bytes per token = 2 (K and V) x layers x KV heads x head dim x
+    bytes per element (deepsonar page, section 2.1)."""
+    return 2 * num_layers * num_kv_heads * head_dim * bytes_per_elem
+
+
+# ---------------------------------------------------------------------------
+# Block allocator
+# ---------------------------------------------------------------------------
+
+class OracleError(Exception):
+    def __init__(self, code: str):
+        super().__init__(code)
+        self.code = code
+
+
+class OracleAllocator:
+    """Plain Python block allocator.
+
+    * Blocks hold ``block_size`` tokens; a sequence's token t sits in logical
+      block t // block_size at offset t % block_size; its slot number is
+      physical_block * block_size + offset (the block-16 layout of the
+      chester-dev.com page, section "PagedAttention transforme l'historique en
+      blocs reutilisables": A -> blocks 7, 2, 19, 4).
+    * A new block is taken only when the token to write starts a block, i.e.
+      the previous block is full (allocation on demand, left to right).
+    * The free queue hands out from its head and takes released blocks back at
+      its tail.  Reading taken where the pages are silent: a released
+      sequence's blocks are returned in table order, logical block 0 first.
+    * ``fork`` shares every block of the parent with the child (reference count
+      + 1 each).  Writing a token into a block whose count is above one first
+      takes a fresh block, records the pair (shared, fresh) for the caller to
+      copy, and drops the shared block's count by one (copy-on-write).
+    * A call that runs out of blocks raises ``OracleError('OUT_OF_BLOCKS')``
+      and leaves the state as it was.
+    """
+
+    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+        if num_blocks <= 0 or block_size <= 0:
+            raise OracleError("INVALID_ARG")
+        self.num_blocks = int(num_blocks)
+        self.block_size = int(block_size)
+        order = list(range(num_blocks)) if free_order is None else [int(b) for b in free_order]
+        if sorted(order) != list(range(num_blocks)):
+            raise OracleError("INVALID_ARG")
+        self.free = deque(order)
+        self.ref = [0] * num_blocks
+        self.seqs: dict[int, dict] = {}
+
+    # -- sequences --------------------------------------------------------
+    def add_seq(self, seq_id: int):
+        if seq_id in self.seqs:
+            raise OracleError("INVALID_ARG")
+        self.seqs[seq_id] = {"len": 0, "blocks": []}
+
+    def _blocks_needed(self, seq, n):
+        bs = self.block_size
+        length = seq["len"]
+        new_blocks = -(-(length + n) // bs) - (-(-length // bs))
+        cow = 0
+        if n > 0 and length % bs != 0 and self.ref[seq["blocks"][-1]] > 1:
+            cow = 1
+        return new_blocks + cow
+
+    def append_tokens(self, seq_id: int, n: int):
+        """Reserve slots for the next n tokens of a sequence.
+
+        Returns (slots, pairs): slots[k] is the slot of token len+k; pairs is a
+        list of (src_block, dst_block) copies that must run before the K/V of
+        those tokens are written."""
+        return self.append_batch([seq_id], [n])
+
+    def append_batch(self, seq_ids, counts):
+        """Same as append_tokens for several sequences, in the order given.
+        All-or-nothing: if the blocks needed by the whole call exceed the free
+        queue, nothing changes."""
+        if len(seq_ids) != len(counts):
+            raise OracleError("INVALID_ARG")
+        for s, n in zip(seq_ids, counts):
+            if s not in self.seqs or n < 0:
+                raise OracleError("INVALID_ARG")
+        if len(set(seq_ids)) != len(seq_ids):
+            raise OracleError("INVALID_ARG")
+        need = sum(self._blocks_needed(self.seqs[s], n) for s, n in zip(seq_ids, counts))
+        if need > len(self.free):
+            raise OracleError("OUT_OF_BLOCKS")
+        bs = self.block_size
+        slots, pairs = [], []
+        for s, n in zip(seq_ids, counts):
+            seq = self.seqs[s]
+            for _ in range(n):
+                t = seq["len"]
+                off = t % bs
+                if off == 0:
+                    b = self.free.popleft()
+                    self.ref[b] = 1
+                    seq["blocks"].append(b)
+                else:
+                    tail = seq["blocks"][-1]
+                    if self.ref[tail] > 1:
+                        nb = self.free.popleft()
+                        self.ref[nb] = 1
+                        self.ref[tail] -= 1
+                        seq["blocks"][-1] = nb
+                        pairs.append((tail, nb))
+                slots.append(seq["blocks"][t // bs] * bs + off)
+                seq["len"] = t + 1
+        return slots, pairs
+
+    def fork(self, parent: int, child: int):
+        if parent not in self.seqs or child in self.seqs:
+            raise OracleError("INVALID_ARG")
+        p = self.seqs[parent]
+        for b in p["blocks"]:
+            self.ref[b] += 1
+        self.seqs[child] = {"len": p["len"], "blocks": list(p["blocks"])}
+
+    def free_seq(self, seq_id: int):
+        if seq_id not in self.seqs:
+            raise OracleError("INVALID_ARG")
+        seq = self.seqs.pop(seq_id)
+        for b in seq["blocks"]:
+            if self.ref[b] <= 0:
+                raise OracleError("STATE")
+            self.ref[b] -= 1
+            if self.ref[b] == 0:
+                self.free.append(b)
+
+    # -- views --------------------------------------------------------------
+    def block_table(self, seq_id: int):
+        return list(self.seqs[seq_id]["blocks"])
+
+    def seq_len(self, seq_id: int) -> int:
+        return self.seqs[seq_id]["len"]
+
+    def slot_of(self, seq_id: int, t: int) -> int:
+        seq = self.seqs[seq_id]
+        return seq["blocks"][t // self.block_size] * self.block_size + t % self.block_size
+
+    def stats(self):
+        used = sum(1 for r in self.ref if r > 0)
+        shared = sum(1 for r in self.ref if r > 1)
+        return {
+            "num_blocks": self.num_blocks,
+            "free_blocks": len(self.free),
+            "used_blocks": used,
+            "shared_blocks": shared,
+            "num_seqs": len(self.seqs),
+            "logical_tokens": sum(s["len"] for s in self.seqs.values()),
+        }
+
+    def used_slot_mask(self):
+        """Boolean [num_blocks, block_size]: True where some sequence holds a
+        token.  Used by tests to poison every other slot."""
+        mask = np.zeros((self.num_blocks, self.block_size), dtype=bool)
+        for seq in self.seqs.values():
+            for t in range(seq["len"]):
+                mask[seq["blocks"][t // self.block_size], t % self.block_size] = True
+        return mask
+
+    def tables(self, seq_ids, max_blocks: int):
+        """int32 [len(seq_ids)][max_blocks] block tables (unused entries -1)
+        and int32 context lengths."""
+        tab = np.full((len(seq_ids), max_blocks), -1, dtype=np.int32)
+        lens = np.zeros(len(seq_ids), dtype=np.int32)
+        for i, s in enumerate(seq_ids):
+            blocks = self.seqs[s]["blocks"]
+            tab[i, : len(blocks)] = blocks
+            lens[i] = self.seqs[s]["len"]
+        return tab, lens
+
+
+# ---------------------------------------------------------------------------
+# KV write and block copy
+# ---------------------------------------------------------------------------
+
+def kv_write(k_cache, v_cache, key, value, slot_mapping, block_size):
+    """Return copies of the caches with token t's K/V rows stored at slot
+    slot_mapping[t] (block slot // block_size, offset slot % block_size).
+    Caches are indexed [block, kv_head, offset, dim]; key/value are
+    [tokens, kv_heads, dim].  Negative slots are padding and are skipped."""
+    kc, vc = k_cache.copy(), v_cache.copy()
+    for t, slot in enumerate(np.asarray(slot_mapping).tolist()):
+        if slot < 0:
+            continue
+        b, o = divmod(int(slot), block_size)
+        kc[b, :, o, :] = key[t]
+        vc[b, :, o, :] = value[t]
+    return kc, vc
+
+
+def block_copy(k_cache, v_cache, pairs):
+    """Return copies of the caches where each dst block holds what its src
+    block held before the call (all K and V of every kv head and offset)."""
+    kc, vc = k_cache.copy(), v_cache.copy()
+    for src, dst in np.asarray(pairs, dtype=np.int64).reshape(-1, 2).tolist():
+        kc[dst] = k_cache[src]
+        vc[dst] = v_cache[src]
+    return kc, vc
+
+
+# ---------------------------------------------------------------------------
+# Decode attention (fp64, C)
+# ---------------------------------------------------------------------------
+
+def default_threads() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:  # pragma: no cover
+        return os.cpu_count() or 1
+
+
+def _decode_call(split_tokens, query, k_cache, v_cache, block_tables, context_lens,
+                 num_kv_heads, block_size, scale, threads, seq_range):
+    lib = _load()
+    q = np.ascontiguousarray(query).view(np.uint16)
+    if q.ndim != 3:
+        raise ValueError("query must be [num_seqs, num_heads, head_dim]")
+    num_seqs, num_heads, head_dim = q.shape
+    kc = np.asarray(k_cache).view(np.uint16)
+    vc = np.asarray(v_cache).view(np.uint16)
+    if kc.ndim != 4 or kc.strides != vc.strides or kc.shape != vc.shape:
+        raise ValueError("caches must be 4-d [block, kv_head, offset, dim] views with equal strides")
+    if kc.strides[3] != 2:
+        raise ValueError("the dim axis of the caches must be unit-stride")
+    if kc.shape[1] != num_kv_heads or kc.shape[2] != block_size or kc.shape[3] != head_dim:
+        raise ValueError("cache shape does not match the arguments")
+    sb, sh, st = (s // 2 for s in kc.strides[:3])
+    tab = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    max_blocks = tab.shape[1]
+    out = np.zeros((num_seqs, num_heads, head_dim), dtype=np.float64)
+    # pointers to the start of the (possibly strided) cache views
+    kptr = kc.__array_interface__["data"][0]
+    vptr = vc.__array_interface__["data"][0]
+    lo, hi = seq_range if seq_range is not None else (0, num_seqs)
+    threads = max(1, min(threads or default_threads(), hi - lo))
+
+    def run(a, b):
+        args = [out.ctypes.data, q.ctypes.data, kptr, vptr, tab.ctypes.data, lens.ctypes.data,
+                num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks, sb, sh, st,
+                float(scale)]
+        if split_tokens is None:
+            rc = lib.or_paged_decode(*args, a, b)
+        else:
+            rc = lib.or_paged_decode_split(*args, int(split_tokens), a, b)
+        if rc != 0:
+            raise RuntimeError("oracle decode failed")
+
+    bounds = np.linspace(lo, hi, threads + 1).astype(int)
+    if threads == 1:
+        run(lo, hi)
+    else:
+        with ThreadPoolExecutor(max_workers=threads) as ex:
+            list(ex.map(lambda ab: run(*ab), zip(bounds[:-1], bounds[1:])))
+    return out
+
+
+def paged_decode(query, k_cache, v_cache, block_tables, context_lens, num_kv_heads, block_size,
+                 scale, threads=None, seq_range=None):
+    """fp64 decode attention (see oracle.c).  Caches are [block, kv_head,
+    offset, dim] numpy views (fp16 or their uint16 bits); any strides with a
+    unit-stride dim axis.  Returns float64 [num_seqs, num_heads, head_dim];
+    rows outside ``seq_range`` stay zero."""
+    return _decode_call(None, query, k_cache, v_cache, block_tables, context_lens,
+                        num_kv_heads, block_size, scale, threads, seq_range)
+
+
+def paged_decode_split(query, k_cache, v_cache, block_tables, context_lens, num_kv_heads,
+                       block_size, scale, partition_tokens, threads=None, seq_range=None):
+    """fp64 split-context decode with the log-sum-exp merge (see oracle.c)."""
+    return _decode_call(int(partition_tokens), query, k_cache, v_cache, block_tables, context_lens,
+                        num_kv_heads, block_size, scale, threads, seq_range)

@@ -1,0 +1,271 @@
+/*
+ * Paged decode attention: the oracle (CPU, fp64).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the plain, slow, obviously correct
+ * statement of what the paged decode path computes.  Only the test suite, the
+ * smoke check and the CPU-baseline leg of the benchmark load it.  It shares no
+ * code, header, table or helper with the CUDA library, and the CUDA library
+ * never calls it.
+ *
+ * Sources (the pages describe the method; none prints the formula in full):
+ *  - Block table and gather: "PagedAttention de vLLM : comment la gestion de la
+ *    VRAM soutient l'inference des grands modeles" (deepsonar.com.cn), section
+ *    2.2 (fixed-size blocks, a per-request table from logical to physical block
+ *    numbers, the attention kernel gathers the physical blocks through it) and
+ *    section 2.6 (the block table is handed to the decode kernel as a tensor).
+ *  - "PagedAttention : comment optimiser la memoire GPU lors de l'inference des
+ *    LLM" (deeplearn.tn), section "La table de blocs en arriere-plan" (logical
+ *    block i -> physical block #n; the system reads the right tokens through
+ *    the physical addresses).
+ *  - GQA sharing: the deepsonar page, section 2.1 (64 attention heads share 8
+ *    KV heads).  Reading taken: contiguous groups, kv_head = head / (Hq / Hkv).
+ *  - Decode = one new query token that consults the stored history: "vLLM
+ *    transforme la memoire GPU en systeme d'exploitation pour LLM"
+ *    (chester-dev.com), section "Le cache KV est une memoire vivante".
+ *  - The attention itself is softmax(q K^T * scale) V with scale passed in
+ *    (1/sqrt(head_dim) in every workload).  The pages never write it out; this
+ *    is the standard definition of scaled dot-product attention.
+ *
+ * Every function below reads fp16 inputs exactly (IEEE binary16 -> double is
+ * exact) and computes in double.  The physical cache layout is an explicit
+ * index function: element (block b, kv head h, offset o, dim d) of a cache sits
+ * at b*stride_block + h*stride_head + o*stride_token + d (in elements), so the
+ * oracle does not assume any particular layout.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* IEEE 754 binary16 -> double, written from the format's definition:
+ * 1 sign bit, 5 exponent bits (bias 15), 10 fraction bits.
+ *   exponent 0      : subnormal, value = fraction * 2^-24
+ *   exponent 1..30  : normal,    value = (1024 + fraction) * 2^(exponent-25)
+ *   exponent 31     : infinity (fraction 0) or NaN. */
+double or_half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 0x1f;
+    int frac = h & 0x3ff;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)frac, -24);
+    else if (expo == 31)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + frac), expo - 25);
+    return sign ? -v : v;
+}
+
+/* Gather one sequence's history into contiguous double arrays
+ * K[t][kv_head][d] and V[t][kv_head][d] for t in [t0, t1), walking the block
+ * table: token t lives in physical block table[t / block_size] at offset
+ * t % block_size. */
+static void gather_sequence(double *K, double *V,
+                            const uint16_t *k_cache, const uint16_t *v_cache,
+                            const int32_t *table, int t0, int t1,
+                            int num_kv_heads, int head_dim, int block_size,
+                            int64_t stride_block, int64_t stride_head,
+                            int64_t stride_token)
+{
+    for (int t = t0; t < t1; ++t) {
+        int64_t phys = table[t / block_size];
+        int64_t off = t % block_size;
+        for (int h = 0; h < num_kv_heads; ++h) {
+            int64_t base = phys * stride_block + h * stride_head + off * stride_token;
+            double *krow = K + ((int64_t)(t - t0) * num_kv_heads + h) * head_dim;
+            double *vrow = V + ((int64_t)(t - t0) * num_kv_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d) {
+                krow[d] = or_half_to_double(k_cache[base + d]);
+                vrow[d] = or_half_to_double(v_cache[base + d]);
+            }
+        }
+    }
+}
+
+/* Decode attention for sequences [seq_begin, seq_end).
+ *
+ * out      : double [num_seqs][num_heads][head_dim]
+ * query    : fp16   [num_seqs][num_heads][head_dim]
+ * k_cache, v_cache : fp16, addressed through the strides above
+ * block_tables : int32 [num_seqs][max_blocks_per_seq]
+ * context_lens : int32 [num_seqs]; L = 0 gives a zero output row.
+ *
+ * For each sequence i and query head h (kv head g = h / (Hq/Hkv)):
+ *   s_t = scale * sum_d q[i][h][d] * K_i[t][g][d]          for t < L_i
+ *   p_t = exp(s_t - max_u s_u) / sum_u exp(s_u - max_u s_u)
+ *   out[i][h][d] = sum_t p_t * V_i[t][g][d]
+ * Returns 0, or -1 on a bad argument or allocation failure. */
+int or_paged_decode(double *out, const uint16_t *query,
+                    const uint16_t *k_cache, const uint16_t *v_cache,
+                    const int32_t *block_tables, const int32_t *context_lens,
+                    int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                    int block_size, int max_blocks_per_seq,
+                    int64_t stride_block, int64_t stride_head, int64_t stride_token,
+                    double scale, int seq_begin, int seq_end)
+{
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        block_size <= 0 || seq_begin < 0 || seq_end > num_seqs)
+        return -1;
+    int group = num_heads / num_kv_heads;
+    for (int i = seq_begin; i < seq_end; ++i) {
+        int L = context_lens[i];
+        double *orow = out + (int64_t)i * num_heads * head_dim;
+        if (L <= 0) {
+            memset(orow, 0, sizeof(double) * (size_t)num_heads * head_dim);
+            continue;
+        }
+        size_t n = (size_t)L * num_kv_heads * head_dim;
+        double *K = (double *)malloc(n * sizeof(double));
+        double *V = (double *)malloc(n * sizeof(double));
+        double *s = (double *)malloc((size_t)L * sizeof(double));
+        double *q = (double *)malloc((size_t)head_dim * sizeof(double));
+        if (!K || !V || !s || !q) {
+            free(K); free(V); free(s); free(q);
+            return -1;
+        }
+        gather_sequence(K, V, k_cache, v_cache,
+                        block_tables + (int64_t)i * max_blocks_per_seq, 0, L,
+                        num_kv_heads, head_dim, block_size,
+                        stride_block, stride_head, stride_token);
+        for (int h = 0; h < num_heads; ++h) {
+            int g = h / group;
+            const uint16_t *qh = query + ((int64_t)i * num_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d)
+                q[d] = or_half_to_double(qh[d]);
+            double m = -INFINITY;
+            for (int t = 0; t < L; ++t) {
+                const double *k = K + ((int64_t)t * num_kv_heads + g) * head_dim;
+                double dot = 0.0;
+                for (int d = 0; d < head_dim; ++d)
+                    dot += q[d] * k[d];
+                s[t] = scale * dot;
+                if (s[t] > m)
+                    m = s[t];
+            }
+            double z = 0.0;
+            for (int t = 0; t < L; ++t) {
+                s[t] = exp(s[t] - m);
+                z += s[t];
+            }
+            double *o = orow + (int64_t)h * head_dim;
+            for (int d = 0; d < head_dim; ++d)
+                o[d] = 0.0;
+            for (int t = 0; t < L; ++t) {
+                double p = s[t] / z;
+                const double *v = V + ((int64_t)t * num_kv_heads + g) * head_dim;
+                for (int d = 0; d < head_dim; ++d)
+                    o[d] += p * v[d];
+            }
+        }
+        free(K); free(V); free(s); free(q);
+    }
+    return 0;
+}
+
+/* The split-context form of the same attention, in double: the context of
+ * each sequence is cut into partitions of partition_tokens tokens; each
+ * partition p yields its own running maximum m_p, its sum of exponentials
+ * l_p = sum_t exp(s_t - m_p) and its normalised output o_p; the partitions are
+ * then merged by the log-sum-exp rule
+ *   M = max_p m_p,  w_p = l_p * exp(m_p - M),  out = sum_p w_p o_p / sum_p w_p.
+ * This is the algebra the split-context decode and its merge step follow; in
+ * exact arithmetic it equals or_paged_decode for any partition size.  The
+ * incremental softmax this rests on is the one the deeplearn.tn page credits
+ * to FlashAttention (section "PagedAttention vs. FlashAttention": softmax
+ * computed incrementally, tile by tile). */
+int or_paged_decode_split(double *out, const uint16_t *query,
+                          const uint16_t *k_cache, const uint16_t *v_cache,
+                          const int32_t *block_tables, const int32_t *context_lens,
+                          int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                          int block_size, int max_blocks_per_seq,
+                          int64_t stride_block, int64_t stride_head, int64_t stride_token,
+                          double scale, int partition_tokens, int seq_begin, int seq_end)
+{
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        block_size <= 0 || partition_tokens <= 0 || seq_begin < 0 || seq_end > num_seqs)
+        return -1;
+    int group = num_heads / num_kv_heads;
+    for (int i = seq_begin; i < seq_end; ++i) {
+        int L = context_lens[i];
+        double *orow = out + (int64_t)i * num_heads * head_dim;
+        if (L <= 0) {
+            memset(orow, 0, sizeof(double) * (size_t)num_heads * head_dim);
+            continue;
+        }
+        int P = (L + partition_tokens - 1) / partition_tokens;
+        size_t n = (size_t)L * num_kv_heads * head_dim;
+        double *K = (double *)malloc(n * sizeof(double));
+        double *V = (double *)malloc(n * sizeof(double));
+        double *q = (double *)malloc((size_t)head_dim * sizeof(double));
+        double *mp = (double *)malloc((size_t)P * sizeof(double));
+        double *lp = (double *)malloc((size_t)P * sizeof(double));
+        double *op = (double *)malloc((size_t)P * head_dim * sizeof(double));
+        if (!K || !V || !q || !mp || !lp || !op) {
+            free(K); free(V); free(q); free(mp); free(lp); free(op);
+            return -1;
+        }
+        gather_sequence(K, V, k_cache, v_cache,
+                        block_tables + (int64_t)i * max_blocks_per_seq, 0, L,
+                        num_kv_heads, head_dim, block_size,
+                        stride_block, stride_head, stride_token);
+        for (int h = 0; h < num_heads; ++h) {
+            int g = h / group;
+            const uint16_t *qh = query + ((int64_t)i * num_heads + h) * head_dim;
+            for (int d = 0; d < head_dim; ++d)
+                q[d] = or_half_to_double(qh[d]);
+            /* partition pass */
+            for (int p = 0; p < P; ++p) {
+                int t0 = p * partition_tokens;
+                int t1 = t0 + partition_tokens < L ? t0 + partition_tokens : L;
+                double m = -INFINITY;
+                for (int t = t0; t < t1; ++t) {
+                    const double *k = K + ((int64_t)t * num_kv_heads + g) * head_dim;
+                    double dot = 0.0;
+                    for (int d = 0; d < head_dim; ++d)
+                        dot += q[d] * k[d];
+                    if (scale * dot > m)
+                        m = scale * dot;
+                }
+                double l = 0.0;
+                double *o = op + (int64_t)p * head_dim;
+                for (int d = 0; d < head_dim; ++d)
+                    o[d] = 0.0;
+                for (int t = t0; t < t1; ++t) {
+                    const double *k = K + ((int64_t)t * num_kv_heads + g) * head_dim;
+                    const double *v = V + ((int64_t)t * num_kv_heads + g) * head_dim;
+                    double dot = 0.0;
+                    for (int d = 0; d < head_dim; ++d)
+                        dot += q[d] * k[d];
+                    double e = exp(scale * dot - m);
+                    l += e;
+                    for (int d = 0; d < head_dim; ++d)
+                        o[d] += e * v[d];
+                }
+                for (int d = 0; d < head_dim; ++d)
+                    o[d] /= l;
+                mp[p] = m;
+                lp[p] = l;
+            }
+            /* log-sum-exp merge */
+            double M = -INFINITY;
+            for (int p = 0; p < P; ++p)
+                if (mp[p] > M)
+                    M = mp[p];
+            double wsum = 0.0;
+            double *out_h = orow + (int64_t)h * head_dim;
+            for (int d = 0; d < head_dim; ++d)
+                out_h[d] = 0.0;
+            for (int p = 0; p < P; ++p) {
+                double w = lp[p] * exp(mp[p] - M);
+                wsum += w;
+                for (int d = 0; d < head_dim; ++d)
+                    out_h[d] += w * op[(int64_t)p * head_dim + d];
+            }
+            for (int d = 0; d < head_dim; ++d)
+                out_h[d] /= wsum;
+        }
+        free(K); free(V); free(q); free(mp); free(lp); free(op);
+    }
+    return 0;
+}
