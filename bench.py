@@ -1,0 +1,392 @@
+"""Benchmark: paged decode attention on the 8k-context GQA workload.
+
+One step = one decode iteration of an 80-layer model for 100 sequences of
+8192 tokens (64 query / 8 KV heads, head_dim 128, block 16): per layer the
+step's new K/V rows are scattered into the paged cache (pa_kv_write) and the
+decode attention runs over the whole cache (pa_decode).  The 80 layers share
+one layer's cache (3.36 GB, far larger than the 129 MB L2, so nothing is
+served from L2 across layers; no flush is needed).  The step has no
+copy-on-write pairs (no sharing in this workload), so pa_block_copy is not
+launched.  The allocation of the step's slots is done by the host allocator
+before the timed region.
+
+value  = decode tokens/s = sequences x steps / timed seconds (device-resident inputs)
+e2e    = the same through the public API with pinned host buffers: every step
+         copies its block tables, lengths and slot mapping, and every layer its
+         query and new K/V rows, host -> device, and every layer's output back.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Multi-GPU (torchrun): each rank runs its own replica of the workload (weak
+scaling); the time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "gqa72b"
+LAYERS = 80
+METRIC = "paged decode attention tokens/s and KV GB/s vs GB300 HBM roofline"
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--layers", type=int, default=LAYERS)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def decode_bytes(w) -> int:
+    """Algorithmic bytes of one decode over the workload: every context token's
+    K and V rows, the query, the output, the block-table entries the contexts
+    need and the lengths."""
+    L = w.context_lens.astype(np.int64)
+    kv = int((L * 2 * w.num_kv_heads * w.head_dim * 2).sum())
+    qo = 2 * w.num_seqs * w.num_heads * w.head_dim * 2
+    tables = int((-(-L // w.block_size)).sum()) * 4
+    return kv + qo + tables + 4 * w.num_seqs
+
+
+def kv_write_bytes(w) -> int:
+    T = w.num_new_tokens
+    return 2 * (2 * T * w.num_kv_heads * w.head_dim * 2) + 8 * T
+
+
+def measured_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for l in getattr(self, "lines", []):
+            parts = [x.strip() for x in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------- oracle timing
+
+def oracle_sample_rate(w, target_s=10.0):
+    """Time the oracle (as it stands) on a bounded sample of the workload:
+    n sequences of the same shape and length, one layer, on all host cores.
+    Returns (tokens/s for the 80-layer step, seconds, n, threads)."""
+    import oracle
+    from paged_kv_cache_12_gb300 import workloads as W
+
+    threads = oracle.default_threads()
+
+    def run(n):
+        s = W.custom(name="oracle-sample", seed=w.seed, num_seqs=n, num_heads=w.num_heads,
+                     num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, block_size=w.block_size,
+                     context_lens=[int(w.context_lens[0])] * n, permute=True)
+        al = oracle.OracleAllocator(s.num_blocks, s.block_size, free_order=s.free_order)
+        ids = list(range(n))
+        for i in ids:
+            al.add_seq(i)
+        al.append_batch(ids, [int(x) for x in s.context_lens])
+        tab, lens = al.tables(ids, s.max_blocks_per_seq)
+        k, v, q = s.k_pool, s.v_pool, s.query
+        t0 = time.perf_counter()
+        oracle.paged_decode(q, k, v, tab, lens, s.num_kv_heads, s.block_size, s.scale, threads=threads)
+        return time.perf_counter() - t0
+
+    n = min(threads, w.num_seqs)
+    t = run(n)
+    if t < target_s / 3 and n < w.num_seqs:
+        n = int(min(w.num_seqs, max(n, n * math.floor(target_s / max(t, 1e-3)))))
+        n = max(threads, (n // threads) * threads) if n >= threads else n
+        t = run(n)
+    return n / (t * LAYERS), t, n, threads
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args):
+    import torch
+
+    import paged_kv_cache_12_gb300 as pa
+    from paged_kv_cache_12_gb300 import workloads
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    w = workloads.make(WORKLOAD)
+    layers = args.layers
+
+    # ---- allocation (host): history, then this step's token for every sequence
+    al = pa.Allocator(w.num_blocks, w.block_size, free_order=w.free_order)
+    ids = list(range(w.num_seqs))
+    for s in ids:
+        al.add_seq(s)
+    al.append(ids, w.history_lens)
+    t_alloc = time.perf_counter()
+    slots, pairs = al.append(ids, w.new_counts)
+    alloc_us = (time.perf_counter() - t_alloc) * 1e6
+    assert len(pairs) == 0
+    tables, lens = al.block_tables(ids, w.max_blocks_per_seq)
+
+    # ---- device-resident inputs
+    k = torch.from_numpy(w.k_pool).to(dev)
+    v = torch.from_numpy(w.v_pool).to(dev)
+    w.drop_arrays()
+    q = torch.from_numpy(w.query).to(dev)
+    nk = torch.from_numpy(w.new_key).to(dev)
+    nv = torch.from_numpy(w.new_value).to(dev)
+    d_slots = torch.from_numpy(slots).to(dev)
+    d_tables = torch.from_numpy(tables).to(dev)
+    d_lens = torch.from_numpy(lens).to(dev)
+    out = torch.empty_like(q)
+    ws = torch.zeros(pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def layer():
+        pa.pa_kv_write(nk, nv, d_slots, k, v, stream)
+        pa.pa_decode(out, q, k, v, d_tables, d_lens, w.scale, w.max_context_len, ws, stream)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    # ---- device-resident timing, with per-decode events for the roofline
+    for _ in range(args.warmup):
+        for _ in range(layers):
+            layer()
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps * layers)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        start.record(stream)
+        i = 0
+        for _ in range(args.steps):
+            for _ in range(layers):
+                pa.pa_kv_write(nk, nv, d_slots, k, v, stream)
+                ev[i][0].record(stream)
+                pa.pa_decode(out, q, k, v, d_tables, d_lens, w.scale, w.max_context_len, ws, stream)
+                ev[i][1].record(stream)
+                i += 1
+        stop.record(stream)
+        barrier()
+    assert pa.pa_workspace_status(ws) == pa.PA_OK
+    total_ms = start.elapsed_time(stop)
+    dec_ms = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- end to end through the public API with pinned host buffers
+    h_tables = torch.from_numpy(tables).pin_memory()
+    h_lens = torch.from_numpy(lens).pin_memory()
+    h_slots = torch.from_numpy(slots).pin_memory()
+    h_q = torch.from_numpy(np.ascontiguousarray(q.cpu().numpy())).pin_memory()
+    h_nk = nk.cpu().pin_memory()
+    h_nv = nv.cpu().pin_memory()
+    h_out = torch.empty((layers,) + tuple(out.shape), dtype=out.dtype).pin_memory()
+
+    def e2e_step():
+        d_tables.copy_(h_tables, non_blocking=True)
+        d_lens.copy_(h_lens, non_blocking=True)
+        d_slots.copy_(h_slots, non_blocking=True)
+        for l in range(layers):
+            q.copy_(h_q, non_blocking=True)
+            nk.copy_(h_nk, non_blocking=True)
+            nv.copy_(h_nv, non_blocking=True)
+            pa.pa_kv_write(nk, nv, d_slots, k, v, stream)
+            pa.pa_decode(out, q, k, v, d_tables, d_lens, w.scale, w.max_context_len, ws, stream)
+            h_out[l].copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = h_tables.numel() * 4 + h_lens.numel() * 4 + h_slots.numel() * 8 + layers * (
+        h_q.numel() * 2 + h_nk.numel() * 2 + h_nv.numel() * 2)
+    d2h = layers * out.numel() * 2
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.barrier()
+            torch.distributed.destroy_process_group()
+        return
+
+    # ---- numbers
+    B = w.num_seqs
+    tok_s = world * B * args.steps / (total_ms / 1e3)
+    dbytes = decode_bytes(w)
+    step_bytes = layers * (dbytes + kv_write_bytes(w))
+    kv_gbs = world * step_bytes * args.steps / (total_ms / 1e3) / 1e9
+    dec_avg_ms = statistics.mean(dec_ms)
+    achieved = dbytes / (dec_avg_ms / 1e3) / 1e9
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    line = {
+        "metric": METRIC,
+        "value": round(tok_s, 2),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{WORKLOAD}: GQA 72B-shaped decode, {B} sequences x 8192-token context, "
+                        f"{w.num_heads} query / {w.num_kv_heads} KV heads, head_dim {w.head_dim}, block {w.block_size}, "
+                        f"{layers} layers per step sharing one layer's cache",
+            "num_seqs": B, "context_len": int(w.context_lens[0]), "num_heads": w.num_heads,
+            "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+            "layers": layers, "parallelism": f"replicas x{world}",
+            "l2": "inputs 3.36 GB per layer >> 129 MB L2; no flush",
+        },
+        "kv_gbs": round(kv_gbs, 1),
+        "decode_ms": {"mean": round(dec_avg_ms, 5), "p10": round(float(np.percentile(dec_ms, 10)), 5),
+                      "p90": round(float(np.percentile(dec_ms, 90)), 5)},
+        "roofline": {
+            "kernel": "pa_decode (prep + partition + log-sum-exp merge launches)",
+            "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "algorithmic_bytes_per_launch": dbytes,
+            "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback 6.8 TB/s (of fallback)",
+        },
+        "e2e": {"value": round(world * B * args.steps / (e2e_ms / 1e3), 2), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": args.steps * layers * (1 + 3),
+        "alloc_us_per_step": round(alloc_us, 1),
+        "clocks": clk.summary(),
+    }
+    if not args.no_cpu_baseline and world == 1:
+        rate, secs, n, threads = oracle_sample_rate(w)
+        line["cpu_baseline"] = {"value": round(rate, 6), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{n} of {B} sequences x 8192 tokens, 1 of {layers} layers "
+                                          f"({secs:.1f} s), scaled to the {layers}-layer step"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.barrier()
+        torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------------------------ reference arm
+
+def run_reference(args):
+    """The oracle, as it stands, on the host cores: same workload, metric and
+    unit; each step is a bounded sample (a few sequences, one layer) scaled to
+    the 80-layer step."""
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    from paged_kv_cache_12_gb300 import workloads
+    w = workloads.make(WORKLOAD)
+    rates, secs_all = [], []
+    n = threads = 0
+    for i in range(args.warmup + args.steps):
+        rate, secs, n, threads = oracle_sample_rate(w, target_s=2.0)
+        if i >= args.warmup:
+            rates.append(rate)
+            secs_all.append(secs)
+    value = statistics.mean(rates)
+    line = {
+        "impl": "reference",
+        "metric": METRIC, "value": round(value, 6), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * w.num_seqs / value, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: GQA 72B-shaped decode, {w.num_seqs} sequences x 8192-token context, "
+                               f"64 query / 8 KV heads, head_dim 128, block 16, {LAYERS} layers per step"},
+        "cpu_baseline": {"value": round(value, 6), "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} sequences x 8192 tokens x 1 layer per step, scaled to {LAYERS} layers"},
+        "e2e": {"value": round(value, 6), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        run_reference(a)
+    else:
+        run_ours(a)

@@ -1,0 +1,227 @@
+/*
+ * pa.h -- C ABI of the paged KV cache decode path (GB300, sm_103a).
+ *
+ * One shared library, libpa.so, exports everything declared here.  Plain C
+ * types only: fp16 tensors are passed as pointers to their IEEE binary16 bit
+ * patterns (uint16_t), CUDA streams as void* (a cudaStream_t; NULL is the
+ * legacy default stream).
+ *
+ * Conventions for every call that touches the GPU
+ *  - All tensor pointers are DEVICE pointers owned by the caller; tensors are
+ *    dense and row-major in the shapes stated.  The library allocates no
+ *    device memory: scratch space is the caller's workspace buffer.
+ *  - Work is enqueued on `stream` and the call returns without waiting for
+ *    it.  Argument checks that need no device data run on the host before any
+ *    launch; a failed check returns PA_ERR_INVALID_ARG (or
+ *    PA_ERR_UNSUPPORTED / PA_ERR_WORKSPACE) and launches nothing.  A launch
+ *    failure returns PA_ERR_CUDA.
+ *  - Values that live on the device (slot numbers, block ids, context
+ *    lengths) are checked by the kernels: an entry out of range is never
+ *    dereferenced.  What happens instead is stated per call.
+ *  - With the environment variable PA_DEBUG_VALIDATE=1 the calls also copy
+ *    their device-side index arguments to the host (synchronising `stream`)
+ *    and return PA_ERR_INVALID_ARG on any out-of-range or conflicting entry.
+ *  - No exception crosses this boundary.
+ *
+ * Cache layout (the pages fix none; this library's choice): k_cache and
+ * v_cache are fp16 [num_blocks][num_kv_heads][block_size][head_dim].  Token
+ * slot s lives in physical block s / block_size at offset s % block_size, so
+ * every (block, kv head) tile is one contiguous block_size x head_dim run.
+ *
+ * Sources: "PagedAttention de vLLM : comment la gestion de la VRAM soutient
+ * l'inference des grands modeles" (deepsonar.com.cn) sections 2.1-2.4, 2.6 and
+ * VII; "PagedAttention : comment optimiser la memoire GPU lors de l'inference
+ * des LLM" (deeplearn.tn), sections "Comment fonctionne PagedAttention", "Un
+ * exemple concret d'allocation", "La table de blocs en arriere-plan";
+ * "vLLM transforme la memoire GPU en systeme d'exploitation pour LLM"
+ * (chester-dev.com), section "PagedAttention transforme l'historique en blocs
+ * reutilisables".
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status */
+
+enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = -1,   /* a bad shape, pointer, id or index */
+    PA_ERR_OUT_OF_BLOCKS = -2, /* the free queue cannot cover the request; nothing changed */
+    PA_ERR_STATE = -3,         /* allocator bookkeeping found an inconsistency */
+    PA_ERR_WORKSPACE = -4,     /* workspace missing, misaligned or too small */
+    PA_ERR_CUDA = -5,          /* a CUDA runtime call or launch failed */
+    PA_ERR_UNSUPPORTED = -6,   /* valid but not built: head_dim, block_size or group size */
+    PA_ERR_TIMEOUT = -7        /* a kernel gave up waiting on its own copies (see pa_workspace_status) */
+};
+
+/* Static text for a status code (never NULL). */
+PA_API const char *pa_status_string(int status);
+
+/* Library ABI version, currently 1. */
+PA_API int pa_version(void);
+
+/* ------------------------------------------------------------- KV write */
+
+/* Scatter the K/V rows of new tokens into their cache slots.
+ *
+ * The new token's K and V go into the free slot the allocator reserved for
+ * it in the sequence's current block (deeplearn.tn page, "Un exemple concret
+ * d'allocation", steps 2-4):
+ *   k_cache[slot / block_size][h][slot % block_size][:] = key[t][h][:]
+ *   v_cache[...same...]                                   = value[t][h][:]
+ * for every token t with slot = slot_mapping[t] and every kv head h.
+ *
+ *   key, value     fp16 [num_tokens][num_kv_heads][head_dim]
+ *   slot_mapping   int64 [num_tokens]; slot < 0 marks padding and is skipped;
+ *                  slot >= num_blocks * block_size is skipped as well
+ *                  (PA_DEBUG_VALIDATE reports it).  Two tokens with the same
+ *                  slot in one call are a caller error (either row may win).
+ *   k_cache, v_cache  fp16 caches in the layout above, num_blocks blocks.
+ *   head_dim       a multiple of 8 (16-byte rows); block_size >= 1.
+ * num_tokens = 0 is valid and launches nothing. */
+PA_API int pa_kv_write(const uint16_t *key, const uint16_t *value, const int64_t *slot_mapping,
+                uint16_t *k_cache, uint16_t *v_cache,
+                int num_tokens, int num_kv_heads, int head_dim, int block_size,
+                int64_t num_blocks, void *stream);
+
+/* -------------------------------------------------------- block copy */
+
+/* Copy whole blocks (all kv heads, all offsets, K and V): the copy half of
+ * copy-on-write (deepsonar page section 2.3: a writer that finds a block
+ * shared copies it first, then writes).
+ *
+ *   pairs      int64 [num_pairs][2] = (src_block, dst_block)
+ * Destinations must be distinct and no destination may also be a source in
+ * the same call; a source may repeat.  Pairs with an id outside
+ * [0, num_blocks) are skipped (PA_DEBUG_VALIDATE reports them and any
+ * conflict).  num_pairs = 0 is valid and launches nothing.
+ * head_dim must be a multiple of 8. */
+PA_API int pa_block_copy(uint16_t *k_cache, uint16_t *v_cache, const int64_t *pairs, int num_pairs,
+                  int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                  void *stream);
+
+/* ------------------------------------------------------------ decode */
+
+/* Bytes of device workspace pa_decode needs for these sizes (a host-side
+ * bound; the same value for any context lengths up to max_context_len). */
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len);
+
+/* Single-token decode attention over the paged cache.
+ *
+ * For each sequence i with L = context_lens[i] tokens (the token written this
+ * step included) and each query head h, with G = num_heads / num_kv_heads and
+ * kv head g = h / G (groups of G consecutive query heads share one kv head,
+ * deepsonar page section 2.1):
+ *   token t (t < L) is gathered from physical block block_tables[i][t / block_size]
+ *   at offset t % block_size (deepsonar page section 2.2; deeplearn.tn page
+ *   "La table de blocs en arriere-plan"),
+ *   s_t = scale * <query[i][h], K_t[g]>,
+ *   out[i][h] = sum_t softmax(s)_t * V_t[g].
+ * The context is processed in partitions of 512 tokens; a sequence longer
+ * than one partition is finished by a log-sum-exp merge of its partitions.
+ * Arithmetic: fp16 inputs, fp32 accumulation, fp16 output.
+ *
+ *   out            fp16 [num_seqs][num_heads][head_dim]
+ *   query          fp16 [num_seqs][num_heads][head_dim]
+ *   k_cache, v_cache  fp16 caches, layout above, num_blocks blocks; 16-byte aligned.
+ *   block_tables   int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens   int32 [num_seqs]
+ *   head_dim in {64, 128}; block_size in {8, 16, 32};
+ *   num_heads % num_kv_heads == 0 and 1 <= G <= 16.
+ *   max_context_len  host-side upper bound on every context_lens[i]; it sizes
+ *                  the workspace and needs no device read.
+ *   workspace      device buffer of at least pa_decode_workspace_size(...)
+ *                  bytes, 256-byte aligned, used only for the duration of
+ *                  the work on `stream`.
+ * Device-side cases: L = 0 gives a zero output row.  L < 0,
+ * L > max_context_len or L > max_blocks_per_seq * block_size gives a NaN
+ * output row.  A block id outside [0, num_blocks) is never read; the
+ * partition that met it writes NaN.  Results are deterministic: the same
+ * inputs give the same bits, whatever the physical placement of the blocks
+ * and whatever the block size. */
+PA_API int pa_decode(uint16_t *out, const uint16_t *query,
+              const uint16_t *k_cache, const uint16_t *v_cache,
+              const int32_t *block_tables, const int32_t *context_lens,
+              int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+              int64_t num_blocks, int max_blocks_per_seq, int max_context_len, float scale,
+              void *workspace, size_t workspace_bytes, void *stream);
+
+/* Read the error word a pa_decode call left in its workspace: PA_OK, or
+ * PA_ERR_TIMEOUT if a kernel gave up waiting for its own copies into shared
+ * memory (the affected outputs are NaN).  Synchronises `stream`. */
+PA_API int pa_workspace_status(const void *workspace, int *status_out, void *stream);
+
+/* ------------------------------------------------------ block allocator */
+
+/* Host-side block allocator with reference counts (no GPU involved).
+ *
+ * Blocks hold block_size tokens.  A sequence takes a new block only when the
+ * token to write starts one (allocation on demand, left to right; deepsonar
+ * page section 2.2 and section VII step 2), so it never holds more than
+ * ceil(len / block_size) blocks.  The free queue hands out from its head and
+ * takes released blocks back at its tail, in table order (deepsonar page
+ * section 2.4 and section VII step 1).  fork() shares every block of the
+ * parent (count + 1).  Writing into a block whose count is above one first
+ * takes a fresh block, reports the (shared, fresh) pair for pa_block_copy and
+ * drops the shared block's count (deepsonar page section 2.3).
+ *
+ * Every call returns a status; on any error the allocator is unchanged. */
+typedef struct pa_allocator pa_allocator;
+
+typedef struct {
+    int64_t num_blocks;
+    int64_t free_blocks;
+    int64_t used_blocks;     /* count > 0 */
+    int64_t shared_blocks;   /* count > 1 */
+    int64_t num_seqs;
+    int64_t logical_tokens;  /* sum of sequence lengths */
+} pa_alloc_stats_t;
+
+/* free_order: optional permutation of [0, num_blocks) giving the initial
+ * order of the free queue (NULL = 0, 1, 2, ...). */
+PA_API int pa_alloc_create(int64_t num_blocks, int block_size, const int32_t *free_order,
+                    pa_allocator **out);
+PA_API int pa_alloc_destroy(pa_allocator *a);
+PA_API int pa_alloc_add_seq(pa_allocator *a, int64_t seq_id);
+
+/* Reserve slots for the next counts[k] tokens of sequence seq_ids[k], k in
+ * order.  slots_out receives sum(counts) slot numbers (sequence by sequence,
+ * token by token); pairs_out receives up to pairs_capacity (src, dst) block
+ * pairs (int64 [n][2]) that pa_block_copy must copy before the K/V of these
+ * tokens are written, and *num_pairs_out their number (at most one per
+ * sequence).  All or nothing: PA_ERR_OUT_OF_BLOCKS if the free queue cannot
+ * cover the whole call; PA_ERR_INVALID_ARG for an unknown or repeated id, a
+ * negative count, or pairs_capacity below the number of pairs needed. */
+PA_API int pa_alloc_append(pa_allocator *a, int num_seqs, const int64_t *seq_ids, const int32_t *counts,
+                    int64_t *slots_out, int64_t *pairs_out, int pairs_capacity,
+                    int *num_pairs_out);
+PA_API int pa_alloc_fork(pa_allocator *a, int64_t parent_id, int64_t child_id);
+PA_API int pa_alloc_free_seq(pa_allocator *a, int64_t seq_id);
+PA_API int pa_alloc_seq_len(const pa_allocator *a, int64_t seq_id, int64_t *len_out);
+
+/* Block tables for num_seqs sequences as int32 [num_seqs][max_blocks] (unused
+ * entries -1) and their lengths as int32 [num_seqs]; PA_ERR_INVALID_ARG if a
+ * sequence holds more than max_blocks blocks. */
+PA_API int pa_alloc_block_tables(const pa_allocator *a, int num_seqs, const int64_t *seq_ids,
+                          int32_t *tables_out, int max_blocks, int32_t *lens_out);
+/* Reference count of one block (0 if free). */
+PA_API int pa_alloc_refcount(const pa_allocator *a, int64_t block, int32_t *count_out);
+PA_API int pa_alloc_stats(const pa_allocator *a, pa_alloc_stats_t *out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

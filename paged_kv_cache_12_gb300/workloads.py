@@ -6,9 +6,10 @@ the method computes (no slots, no block tables, no attention); the tests,
 the benchmark and the oracle all build those from what is drawn here.
 
 Every array comes from NumPy's PCG64 seeded with ``1000 + k`` (k = the
-workload's index below), values N(0, 1) rounded to fp16 (round to nearest
-even).  Each array has its own child stream of that seed, so any one of them
-can be drawn without drawing the others.
+workload's index below), values N(0, 1) (Box-Muller over float32
+uniforms) rounded to fp16 (round to nearest even).  Each array has its own child stream of that seed (and each chunk of
+2^22 values its own grandchild stream), so any one of them can be drawn
+without drawing the others, by any number of threads.
 
 Workloads (shaped like the pages' examples; sizes named by what they are):
 
@@ -32,6 +33,8 @@ Workloads (shaped like the pages' examples; sizes named by what they are):
 from __future__ import annotations
 
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from dataclasses import dataclass, field
 
 import numpy as np
@@ -42,20 +45,47 @@ WORKLOADS = ("tiny", "mha7b", "gqa72b", "mix", "cow16", "cow32")
 _S_LENGTHS, _S_ORDER, _S_QUERY, _S_KPOOL, _S_VPOOL, _S_NEWK, _S_NEWV, _S_EXTRA = range(8)
 
 
-def _rng(seed: int, stream: int) -> np.random.Generator:
-    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(stream,))))
+_CHUNK = 1 << 22     # values per independently seeded chunk
+
+
+def _rng(seed: int, stream: int, chunk: int | None = None) -> np.random.Generator:
+    key = (stream,) if chunk is None else (stream, chunk)
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=key)))
+
+
+def _normal_chunk(rng: np.random.Generator, n: int) -> np.ndarray:
+    """n N(0, 1) float32 values by the Box-Muller transform (Box and Muller,
+    1958): from uniforms u1 in (0, 1] and u2 in [0, 1), r = sqrt(-2 ln u1)
+    gives the pair r cos(2 pi u2), r sin(2 pi u2)."""
+    m = (n + 1) // 2
+    u1 = np.float32(1.0) - rng.random(m, dtype=np.float32)
+    ang = rng.random(m, dtype=np.float32) * np.float32(2.0 * np.pi)
+    r = np.sqrt(np.float32(-2.0) * np.log(u1))
+    out = np.empty(2 * m, dtype=np.float32)
+    np.multiply(r, np.cos(ang), out=out[0::2])
+    np.multiply(r, np.sin(ang), out=out[1::2])
+    return out[:n]
 
 
 def normal_fp16(seed: int, stream: int, shape) -> np.ndarray:
-    """N(0, 1) values rounded to fp16, drawn in float32 from child stream
-    ``stream`` of ``seed``."""
-    rng = _rng(seed, stream)
+    """N(0, 1) values rounded to fp16.  Chunk c of _CHUNK values is drawn from
+    child stream (stream, c) of ``seed``, so the result does not depend on how
+    many threads draw it."""
     n = int(np.prod(shape))
     out = np.empty(n, dtype=np.float16)
-    chunk = 1 << 26
-    for a in range(0, n, chunk):
-        b = min(n, a + chunk)
-        out[a:b] = rng.standard_normal(b - a, dtype=np.float32).astype(np.float16)
+
+    def fill(c):
+        a = c * _CHUNK
+        b = min(n, a + _CHUNK)
+        out[a:b] = _normal_chunk(_rng(seed, stream, c), b - a).astype(np.float16)
+
+    chunks = range(-(-n // _CHUNK))
+    if n <= _CHUNK:
+        for c in chunks:
+            fill(c)
+    else:
+        with ThreadPoolExecutor(max_workers=min(32, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, chunks))
     return out.reshape(shape)
 
 

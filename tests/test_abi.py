@@ -1,0 +1,64 @@
+"""The C-ABI library loads on a machine without a GPU and exports every symbol
+include/*.h declares; host-only calls behave as documented."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import paged_kv_cache_12_gb300 as pa
+from conftest import ROOT
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names |= set(re.findall(r"^PA_API[^;(]*?\b(pa_\w+)\s*\(", text, flags=re.M))
+    return names
+
+
+def test_header_declares_the_binding_exports():
+    assert declared_symbols() == set(pa.EXPORTS)
+
+
+def test_every_declared_symbol_is_exported():
+    lib = ctypes.CDLL(pa.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version():
+    assert pa.pa_version() == 1
+    for code in range(-7, 1):
+        assert pa.pa_status_string(code) and pa.pa_status_string(code) != "unknown status"
+    assert pa.pa_status_string(-99) == "unknown status"
+
+
+def test_workspace_size_is_a_host_bound():
+    small = pa.pa_decode_workspace_size(4, 4, 64, 100)
+    big = pa.pa_decode_workspace_size(100, 64, 128, 8192)
+    # header + offsets + item list; partial results only when a sequence can span partitions
+    assert 0 < small < 8192
+    assert big >= 100 * 16 * 64 * 128 * 4
+    assert pa.pa_decode_workspace_size(100, 64, 128, 512) < 100 * 64 * 128 * 4
+
+
+def test_host_checks_fail_before_any_launch():
+    L = pa.lib()
+    nul = None
+    # unsupported head_dim / block size / group size: rejected on the host
+    assert L.pa_decode(nul, nul, nul, nul, nul, nul, 1, 8, 1, 96, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_ERR_UNSUPPORTED
+    assert L.pa_decode(nul, nul, nul, nul, nul, nul, 1, 8, 1, 128, 64, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_ERR_UNSUPPORTED
+    assert L.pa_decode(nul, nul, nul, nul, nul, nul, 1, 32, 1, 128, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_ERR_UNSUPPORTED
+    assert L.pa_decode(nul, nul, nul, nul, nul, nul, 1, 6, 4, 128, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_ERR_INVALID_ARG
+    # missing pointers
+    assert L.pa_decode(nul, nul, nul, nul, nul, nul, 1, 8, 1, 128, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_kv_write(nul, nul, nul, nul, nul, 3, 8, 128, 16, 10, nul) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_block_copy(nul, nul, nul, 2, 8, 128, 16, 10, nul) == pa.PA_ERR_INVALID_ARG
+    assert L.pa_kv_write(nul, nul, nul, nul, nul, 1, 8, 100, 16, 10, nul) == pa.PA_ERR_INVALID_ARG  # head_dim % 8
+    # empty work is valid and launches nothing
+    assert L.pa_kv_write(nul, nul, nul, nul, nul, 0, 8, 128, 16, 10, nul) == pa.PA_OK
+    assert L.pa_block_copy(nul, nul, nul, 0, 8, 128, 16, 10, nul) == pa.PA_OK
+    assert L.pa_decode(nul, nul, nul, nul, nul, nul, 0, 8, 1, 128, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_OK

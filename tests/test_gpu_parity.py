@@ -1,0 +1,210 @@
+"""GPU parity: the library's kernels against the oracle on the same seeded
+inputs.  KV write and block copy must match bit for bit (whole caches,
+poisoned slots included); decode must be within the path's tolerance
+(max abs error <= 2e-3, normwise relative error per row <= 1e-2)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_cache_12_gb300 as pa
+from paged_kv_cache_12_gb300 import workloads
+from scenario import Step, compare
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+def to_np(t):
+    return t.cpu().numpy()
+
+
+def run_step(w, check_caches=True):
+    st = Step(w)
+    d = st.upload(torch)
+    st.run_library(d)
+    torch.cuda.synchronize()
+    assert pa.pa_workspace_status(d["ws"]) == pa.PA_OK
+    kc, vc = st.oracle_caches()
+    if check_caches:
+        assert np.array_equal(to_np(d["k"]).view(np.uint16), kc.view(np.uint16))
+        assert np.array_equal(to_np(d["v"]).view(np.uint16), vc.view(np.uint16))
+    ref = st.oracle_out(kc, vc)
+    got = to_np(d["out"])
+    return compare(got, ref), st, d
+
+
+# ------------------------------------------------------------------ workloads
+
+@pytest.mark.parametrize("name", ["tiny", "mha7b"])
+def test_small_workloads(name):
+    run_step(workloads.make(name))
+
+
+@pytest.mark.parametrize("name,extra", [("cow16", None), ("cow16", 0), ("cow32", None), ("cow32", 0)])
+def test_parallel_sampling_cow(name, extra):
+    w = workloads.make(name, prompt_extra=extra)
+    (_, _), st, _ = run_step(w)
+    if extra == 0:
+        assert len(st.pairs) == 0          # whole-block prompt: the first private token starts a new block
+    else:
+        assert len(st.pairs) == 7 * w.num_prompts
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["gqa72b", "mix"])
+def test_full_size_workloads(name):
+    w = workloads.make(name)
+    run_step(w, check_caches=False)
+
+
+# ---------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("H,Hkv", [(8, 8), (8, 4), (8, 1), (16, 2), (12, 1), (32, 2)])
+def test_shapes_and_ragged_lengths(D, bs, H, Hkv):
+    lens = [1, 2, bs - 1, bs, bs + 1, 15, 16, 17, 511, 512, 513, 1000, 1024, 1025, 1537]
+    w = workloads.custom(seed=11 + D + bs + H, num_seqs=len(lens), num_heads=H, num_kv_heads=Hkv, head_dim=D,
+                         block_size=bs, context_lens=lens)
+    run_step(w)
+
+
+def test_zero_length_rows_are_zero():
+    w = workloads.custom(seed=3, num_seqs=5, num_heads=8, num_kv_heads=2, head_dim=128, block_size=16,
+                         context_lens=[0, 7, 0, 600, 1])
+    (_, _), st, d = run_step(w)
+    out = to_np(d["out"])
+    assert not out[0].any() and not out[2].any()
+
+
+def test_single_token_gives_its_value_row():
+    w = workloads.custom(seed=4, num_seqs=3, num_heads=8, num_kv_heads=2, head_dim=64, block_size=16,
+                         context_lens=[1, 1, 1])
+    (_, _), st, d = run_step(w)
+    out = to_np(d["out"]).astype(np.float32)
+    for i in range(3):
+        for h in range(8):
+            assert np.array_equal(out[i, h], w.new_value[i, h // 4].astype(np.float32))
+
+
+def relocate(src, dst, lens):
+    """Give step `dst` the history content of step `src`, token by token, in
+    dst's own physical placement and block size; dst also takes src's query
+    and new tokens.  Only the placement differs afterwards."""
+    bs_s, bs_d = src.w.block_size, dst.w.block_size
+    k, v = dst.k0.copy(), dst.v0.copy()
+    for i, L in enumerate(lens):
+        for t in range(L - 1):
+            b0, o0 = divmod(src.ref.slot_of(i, t), bs_s)
+            b1, o1 = divmod(dst.ref.slot_of(i, t), bs_d)
+            k[b1, :, o1] = src.k0[b0, :, o0]
+            v[b1, :, o1] = src.v0[b0, :, o0]
+    dst.k0, dst.v0 = k, v
+    dst.query, dst.new_key, dst.new_value = src.w.query, src.w.new_key, src.w.new_value
+
+
+def run_relocated(st):
+    d = st.upload(torch)
+    d["q"].copy_(torch.from_numpy(st.query))
+    d["nk"].copy_(torch.from_numpy(st.new_key))
+    d["nv"].copy_(torch.from_numpy(st.new_value))
+    st.run_library(d)
+    torch.cuda.synchronize()
+    return to_np(d["out"]).view(np.uint16).copy()
+
+
+def test_deterministic_and_placement_invariant():
+    """Different physical placements of the same logical K/V give identical bits, run after run."""
+    lens = [700, 33, 1500, 2049]
+    shape = dict(num_seqs=4, num_heads=16, num_kv_heads=2, head_dim=128, block_size=16, context_lens=lens)
+    base = Step(workloads.custom(seed=21, **shape))
+    outs = []
+    for seed in (22, 23):
+        st = Step(workloads.custom(seed=seed, **shape))
+        assert not np.array_equal(st.tables, base.tables)
+        relocate(base, st, lens)
+        outs += [run_relocated(st), run_relocated(st)]
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
+    # and they match the oracle
+    st = Step(workloads.custom(seed=21, **shape))
+    d = st.upload(torch)
+    st.run_library(d)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(d["out"]).view(np.uint16), outs[0])
+
+
+def test_block_size_invariant_bits():
+    """The same logical K/V paged at block size 8, 16 and 32 gives identical bits."""
+    lens = [1, 40, 513, 1100]
+    shape = dict(num_seqs=4, num_heads=8, num_kv_heads=1, head_dim=128, context_lens=lens)
+    base = Step(workloads.custom(seed=31, block_size=8, **shape))
+    outs = []
+    for bs in (8, 16, 32):
+        st = Step(workloads.custom(seed=32 + bs, block_size=bs, **shape))
+        relocate(base, st, lens)
+        outs.append(run_relocated(st))
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
+def test_invalid_lengths_give_nan_rows():
+    w = workloads.custom(seed=5, num_seqs=3, num_heads=4, num_kv_heads=2, head_dim=64, block_size=16,
+                         context_lens=[20, 20, 20])
+    st = Step(w)
+    d = st.upload(torch)
+    st.run_library(d)
+    lens = d["lens"].clone()
+    lens[1] = 10_000          # beyond max_context_len and the table
+    lens[2] = -3
+    pa.pa_decode(d["out"], d["q"], d["k"], d["v"], d["tables"], lens, w.scale, w.max_context_len, d["ws"])
+    out = to_np(d["out"]).astype(np.float32)
+    assert np.isfinite(out[0]).all() and np.isnan(out[1]).all() and np.isnan(out[2]).all()
+
+
+def test_kv_write_skips_padding_and_out_of_range_slots():
+    w = workloads.make("tiny")
+    st = Step(w)
+    d = st.upload(torch)
+    slots = d["slots"].clone()
+    slots[0] = -1
+    slots[1] = w.num_blocks * w.block_size + 5
+    k_before = to_np(d["k"]).copy()
+    pa.pa_kv_write(d["nk"], d["nv"], slots, d["k"], d["v"])
+    torch.cuda.synchronize()
+    kc, _ = oracle.kv_write(k_before, k_before, w.new_key, w.new_value,
+                            np.where(np.arange(len(st.slots)) < 2, -1, st.slots), w.block_size)
+    assert np.array_equal(to_np(d["k"]).view(np.uint16), kc.view(np.uint16))
+
+
+def test_block_copy_bit_exact_random_pairs():
+    rng = np.random.default_rng(8)
+    nb, hkv, bs, dd = 300, 4, 16, 128
+    k = rng.standard_normal((nb, hkv, bs, dd)).astype(np.float16)
+    v = rng.standard_normal((nb, hkv, bs, dd)).astype(np.float16)
+    perm = rng.permutation(nb)
+    srcs = rng.choice(perm[:100], size=120)            # sources may repeat
+    dsts = perm[100:220]                               # distinct, never a source
+    pairs = np.stack([srcs, dsts], 1).astype(np.int64)
+    kd, vd = torch.from_numpy(k).cuda(), torch.from_numpy(v).cuda()
+    pa.pa_block_copy(kd, vd, torch.from_numpy(pairs).cuda())
+    torch.cuda.synchronize()
+    ek, ev = oracle.block_copy(k, v, pairs)
+    assert np.array_equal(to_np(kd).view(np.uint16), ek.view(np.uint16))
+    assert np.array_equal(to_np(vd).view(np.uint16), ev.view(np.uint16))
+
+
+def test_streams_are_respected():
+    w = workloads.make("tiny")
+    st = Step(w)
+    d = st.upload(torch)
+    s = torch.cuda.Stream()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        st.run_library(d)
+    s.synchronize()
+    kc, vc = st.oracle_caches()
+    compare(to_np(d["out"]), st.oracle_out(kc, vc))
