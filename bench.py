@@ -44,11 +44,13 @@ METRIC = "paged decode attention tokens/s and KV GB/s vs GB300 HBM roofline"
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=30)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--layers", type=int, default=LAYERS)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--seqs", type=int, default=None,
+                   help="same shape with fewer sequences (small cases for profiling); default: the full 100")
     return p.parse_args()
 
 
@@ -167,6 +169,16 @@ def oracle_sample_rate(w, target_s=10.0):
 
 # ------------------------------------------------------------------ our arm
 
+def workload(args):
+    from paged_kv_cache_12_gb300 import workloads
+    w = workloads.make(WORKLOAD)
+    if args.seqs is None or args.seqs == w.num_seqs:
+        return w
+    return workloads.custom(name=f"{WORKLOAD}-{args.seqs}seqs", seed=w.seed, num_seqs=args.seqs,
+                            num_heads=w.num_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
+                            block_size=w.block_size, context_lens=[int(w.context_lens[0])] * args.seqs)
+
+
 def run_ours(args):
     import torch
 
@@ -179,7 +191,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    w = workloads.make(WORKLOAD)
+    w = workload(args)
     layers = args.layers
 
     # ---- allocation (host): history, then this step's token for every sequence
@@ -316,7 +328,7 @@ def run_ours(args):
         "dtype": "f16",
         "data": "synthetic",
         "config": {
-            "workload": f"{WORKLOAD}: GQA 72B-shaped decode, {B} sequences x 8192-token context, "
+            "workload": f"{w.name}: GQA 72B-shaped decode, {B} sequences x 8192-token context, "
                         f"{w.num_heads} query / {w.num_kv_heads} KV heads, head_dim {w.head_dim}, block {w.block_size}, "
                         f"{layers} layers per step sharing one layer's cache",
             "num_seqs": B, "context_len": int(w.context_lens[0]), "num_heads": w.num_heads,
