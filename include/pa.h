@@ -163,6 +163,45 @@ PA_API int pa_decode(uint16_t *out, const uint16_t *query,
  * memory (the affected outputs are NaN).  Synchronises `stream`. */
 PA_API int pa_workspace_status(const void *workspace, int *status_out, void *stream);
 
+/* -------------------------------------------- decode without allocation */
+
+/* Largest scratch area pa_decode_static_ws can use: 64 MiB. */
+#define PA_DECODE_STATIC_WS_BYTES (64u << 20)
+
+/* pa_decode for callers that cannot allocate device memory at all.
+ *
+ * No counterpart in the pages: this is a packaging choice of this library.
+ * Some callers may not call cudaMalloc -- for example a plugin that runs
+ * inside a host framework which owns every byte of device memory through its
+ * own pool (a raw cudaMalloc there goes around the pool, can fail once the
+ * pool holds the memory, and may synchronise the device), or a serving loop
+ * whose rule is that nothing is allocated after start-up.  Such a caller
+ * cannot provide pa_decode's workspace.  This entry point takes the same
+ * arguments as pa_decode minus the workspace and uses instead a scratch array
+ * of PA_DECODE_STATIC_WS_BYTES that the library declares at file scope in
+ * device memory; every GPU that loads the library holds that array until the
+ * process exits.  It allocates nothing: no cudaMalloc, no cudaFree, no
+ * allocating library routine.
+ *
+ *  - The first call on a device looks the array's device address up (with
+ *    that device current) and keeps it; make that first call before any
+ *    stream capture.
+ *  - If pa_decode_workspace_size(num_seqs, num_heads, head_dim,
+ *    max_context_len) exceeds PA_DECODE_STATIC_WS_BYTES the call returns
+ *    PA_ERR_WORKSPACE and launches nothing.
+ *  - All calls on a device share the one array and it keeps whatever the last
+ *    call left there (each call re-initialises what it needs before use).
+ *    Calls whose work overlaps on the GPU -- on different streams without
+ *    ordering between them -- race on the array and give wrong results:
+ *    order them, or use pa_decode with a workspace per stream.
+ * Results are identical to pa_decode's for the same inputs. */
+PA_API int pa_decode_static_ws(uint16_t *out, const uint16_t *query,
+                               const uint16_t *k_cache, const uint16_t *v_cache,
+                               const int32_t *block_tables, const int32_t *context_lens,
+                               int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                               int block_size, int64_t num_blocks, int max_blocks_per_seq,
+                               int max_context_len, float scale, void *stream);
+
 /* ------------------------------------------------------ block allocator */
 
 /* Host-side block allocator with reference counts (no GPU involved).

@@ -37,8 +37,11 @@ EXPORTS = (
     "pa_status_string", "pa_version", "pa_kv_write", "pa_block_copy", "pa_decode_workspace_size", "pa_decode",
     "pa_workspace_status", "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_add_seq", "pa_alloc_append",
     "pa_alloc_fork", "pa_alloc_free_seq", "pa_alloc_seq_len", "pa_alloc_block_tables", "pa_alloc_refcount",
-    "pa_alloc_stats",
+    "pa_alloc_stats", "pa_decode_static_ws",
 )
+
+# bytes of the library's built-in scratch array used by pa_decode_static_ws
+PA_DECODE_STATIC_WS_BYTES = 64 << 20
 
 _lib = None
 
@@ -81,6 +84,8 @@ def lib():
             "pa_alloc_block_tables": ([vp, i32, vp, vp, i32, vp], i32),
             "pa_alloc_refcount": ([vp, i64, ctypes.POINTER(ctypes.c_int32)], i32),
             "pa_alloc_stats": ([vp, ctypes.POINTER(AllocStats)], i32),
+            "pa_decode_static_ws": ([vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, i32, i32,
+                                     ctypes.c_float, vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -179,6 +184,28 @@ def pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, scale, m
                            block_tables.data_ptr(), context_lens.data_ptr(), B, hq, hkv, d, bs, nb,
                            block_tables.shape[1], int(max_context_len), float(scale), workspace.data_ptr(),
                            workspace.numel(), _stream(stream)), "pa_decode")
+
+
+def pa_decode_static_ws(out, query, k_cache, v_cache, block_tables, context_lens, scale, max_context_len,
+                        stream=None):
+    """pa_decode without a workspace argument, for callers that cannot allocate
+    device memory: the library's own fixed scratch array (64 MiB, shared by all
+    calls on a device) stands in for it.  Calls that overlap on the GPU must not
+    share it; sizes needing more scratch raise PAError(PA_ERR_WORKSPACE)."""
+    import torch
+    for t, dt, nd, nm in ((out, torch.float16, 3, "out"), (query, torch.float16, 3, "query"),
+                          (k_cache, torch.float16, 4, "k_cache"), (v_cache, torch.float16, 4, "v_cache"),
+                          (block_tables, torch.int32, 2, "block_tables"), (context_lens, torch.int32, 1, "context_lens")):
+        _need(t, dt, nd, nm)
+    nb, hkv, bs, d = k_cache.shape
+    B, hq, d2 = query.shape
+    if out.shape != query.shape or d2 != d or v_cache.shape != k_cache.shape or block_tables.shape[0] != B \
+            or context_lens.shape[0] != B:
+        raise ValueError("pa_decode_static_ws: shape mismatch")
+    _check(lib().pa_decode_static_ws(out.data_ptr(), query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                     block_tables.data_ptr(), context_lens.data_ptr(), B, hq, hkv, d, bs, nb,
+                                     block_tables.shape[1], int(max_context_len), float(scale), _stream(stream)),
+           "pa_decode_static_ws")
 
 
 def pa_workspace_status(workspace, stream=None) -> int:

@@ -780,3 +780,52 @@ extern "C" int pa_decode(uint16_t *out, const uint16_t *query, const uint16_t *k
     }
     return PA_OK;
 }
+
+// ------------------------------------------------ decode without allocation
+
+// Scratch for pa_decode_static_ws: a file-scope device array, so that callers
+// that may not allocate device memory still have somewhere for the partition
+// results.  In host code the name g_static_ws is only a stand-in; its device
+// address comes from cudaGetSymbolAddress, once per device.
+static __device__ __align__(256) uint8_t g_static_ws[PA_DECODE_STATIC_WS_BYTES];
+
+namespace pa {
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+
+// Device address of g_static_ws on the current device, looked up on the first
+// call for that device; nullptr if the lookup fails.
+void *static_ws_address(int device) {
+    static std::mutex mu;
+    static void *addr[MAX_DEVICES] = {};
+    if (device < 0 || device >= MAX_DEVICES) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[device]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_static_ws) != cudaSuccess || !p) return nullptr;
+        addr[device] = p;
+    }
+    return addr[device];
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_decode_static_ws(uint16_t *out, const uint16_t *query, const uint16_t *k_cache,
+                                   const uint16_t *v_cache, const int32_t *block_tables,
+                                   const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int64_t num_blocks, int max_blocks_per_seq,
+                                   int max_context_len, float scale, void *stream) {
+    if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0) return PA_ERR_INVALID_ARG;
+    if (ws_layout(num_seqs, num_heads, head_dim, max_context_len).total > (size_t)PA_DECODE_STATIC_WS_BYTES)
+        return PA_ERR_WORKSPACE;
+    if (num_seqs == 0) return PA_OK;
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
+    void *ws = static_ws_address(device);
+    if (!ws) return PA_ERR_CUDA;
+    return pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads, num_kv_heads,
+                     head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len, scale, ws,
+                     (size_t)PA_DECODE_STATIC_WS_BYTES, stream);
+}

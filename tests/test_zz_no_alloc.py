@@ -1,0 +1,62 @@
+"""pa_decode_static_ws: decode for callers that cannot allocate device memory.
+
+Such callers (a plugin living inside a framework that owns all device memory
+through its own pool, or a serving loop that allocates nothing after
+start-up) cannot hand pa_decode a workspace, so the library offers a variant
+that uses its own fixed scratch array instead.  This file checks, through the
+C ABI, that two calls in a row give what pa_decode gives for the same inputs
+(within the decode tolerance), although the second call finds the first one's
+leftovers in the shared array, and that a size needing more scratch than the
+array holds is refused.  It is collected last so that a failure here never
+hides the other tests' results."""
+import numpy as np
+import pytest
+
+import paged_kv_cache_12_gb300 as pa
+from paged_kv_cache_12_gb300 import workloads
+from scenario import Step, compare
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+
+def both_outputs(w):
+    st = Step(w)
+    d = st.upload(torch)
+    st.run_library(d)                       # pa_decode with a caller-provided workspace
+    expect = d["out"].clone()
+    got = torch.full_like(d["out"], float("nan"))
+    pa.pa_decode_static_ws(got, d["q"], d["k"], d["v"], d["tables"], d["lens"], w.scale, w.max_context_len)
+    torch.cuda.synchronize()
+    return got.cpu().numpy(), expect.cpu().numpy()
+
+
+def test_two_calls_in_a_row_match_pa_decode():
+    # first call: several multi-partition sequences, 16 query heads per kv head
+    w1 = workloads.custom(seed=41, num_seqs=6, num_heads=32, num_kv_heads=2, head_dim=128, block_size=16,
+                          context_lens=[3000, 1, 700, 2049, 513, 1500])
+    got, expect = both_outputs(w1)
+    compare(got, expect.astype(np.float64))
+    # second call: other shapes and lengths over the same, now dirty, scratch array
+    w2 = workloads.custom(seed=42, num_seqs=9, num_heads=8, num_kv_heads=8, head_dim=64, block_size=32,
+                          context_lens=[1100, 64, 4097, 5, 0, 900, 2600, 513, 1])
+    got, expect = both_outputs(w2)
+    compare(got, expect.astype(np.float64))
+
+
+def test_too_large_is_refused():
+    w = workloads.custom(seed=43, num_seqs=2, num_heads=8, num_kv_heads=1, head_dim=128, block_size=16,
+                         context_lens=[40, 40])
+    st = Step(w)
+    d = st.upload(torch)
+    need = pa.pa_decode_workspace_size(4096, 64, 128, 32768)
+    assert need > pa.PA_DECODE_STATIC_WS_BYTES
+    big_q = torch.zeros((4096, 64, 128), dtype=torch.float16, device="cuda")
+    big_t = torch.zeros((4096, 1), dtype=torch.int32, device="cuda")
+    big_l = torch.zeros((4096,), dtype=torch.int32, device="cuda")
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_decode_static_ws(torch.empty_like(big_q), big_q, d["k"], d["v"], big_t, big_l, w.scale, 32768)
+    assert e.value.code == pa.PA_ERR_WORKSPACE
