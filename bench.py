@@ -217,7 +217,7 @@ def run_ours(args):
     d_tables = torch.from_numpy(tables).to(dev)
     d_lens = torch.from_numpy(lens).to(dev)
     out = torch.empty_like(q)
-    ws = torch.zeros(pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.head_dim, w.max_context_len),
+    ws = torch.zeros(pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.max_context_len),
                      dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 

@@ -115,8 +115,10 @@ PA_API int pa_block_copy(uint16_t *k_cache, uint16_t *v_cache, const int64_t *pa
 /* ------------------------------------------------------------ decode */
 
 /* Bytes of device workspace pa_decode needs for these sizes (a host-side
- * bound; the same value for any context lengths up to max_context_len). */
-PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len);
+ * bound; the same value for any context lengths up to max_context_len).
+ * Returns 0 for invalid sizes. */
+PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                       int max_context_len);
 
 /* Single-token decode attention over the paged cache.
  *
@@ -129,8 +131,11 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim
  *   "La table de blocs en arriere-plan"),
  *   s_t = scale * <query[i][h], K_t[g]>,
  *   out[i][h] = sum_t softmax(s)_t * V_t[g].
- * The context is processed in partitions of 512 tokens; a sequence longer
- * than one partition is finished by a log-sum-exp merge of its partitions.
+ * The context is processed in partitions of PT tokens, PT the largest of
+ * 1024, 512 and 256 for which num_seqs * num_kv_heads *
+ * ceil(max_context_len / PT) >= 4096 (256 if none); a sequence longer than
+ * one partition is finished by a log-sum-exp merge of its partitions.  PT
+ * depends on these host-side sizes only.
  * Arithmetic: fp16 inputs, fp32 accumulation, fp16 output.
  *
  *   out            fp16 [num_seqs][num_heads][head_dim]
@@ -150,7 +155,7 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim
  * output row.  A block id outside [0, num_blocks) is never read; the
  * partition that met it writes NaN.  Results are deterministic: the same
  * inputs give the same bits, whatever the physical placement of the blocks
- * and whatever the block size. */
+ * and whatever the block size.  scale must be positive and finite. */
 PA_API int pa_decode(uint16_t *out, const uint16_t *query,
               const uint16_t *k_cache, const uint16_t *v_cache,
               const int32_t *block_tables, const int32_t *context_lens,
@@ -186,8 +191,8 @@ PA_API int pa_workspace_status(const void *workspace, int *status_out, void *str
  *  - The first call on a device looks the array's device address up (with
  *    that device current) and keeps it; make that first call before any
  *    stream capture.
- *  - If pa_decode_workspace_size(num_seqs, num_heads, head_dim,
- *    max_context_len) exceeds PA_DECODE_STATIC_WS_BYTES the call returns
+ *  - If pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads,
+ *    head_dim, max_context_len) exceeds PA_DECODE_STATIC_WS_BYTES the call returns
  *    PA_ERR_WORKSPACE and launches nothing.
  *  - All calls on a device share the one array and it keeps whatever the last
  *    call left there (each call re-initialises what it needs before use).

@@ -70,7 +70,7 @@ def lib():
             "pa_version": ([], i32),
             "pa_kv_write": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i64, vp], i32),
             "pa_block_copy": ([vp, vp, vp, i32, i32, i32, i32, i64, vp], i32),
-            "pa_decode_workspace_size": ([i32, i32, i32, i32], sz),
+            "pa_decode_workspace_size": ([i32, i32, i32, i32, i32], sz),
             "pa_decode": ([vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, i32, i32, ctypes.c_float, vp, sz, vp],
                           i32),
             "pa_workspace_status": ([vp, ctypes.POINTER(i32), vp], i32),
@@ -159,8 +159,9 @@ def pa_block_copy(k_cache, v_cache, pairs, stream=None):
                                nb, _stream(stream)), "pa_block_copy")
 
 
-def pa_decode_workspace_size(num_seqs, num_heads, head_dim, max_context_len) -> int:
-    n = lib().pa_decode_workspace_size(int(num_seqs), int(num_heads), int(head_dim), int(max_context_len))
+def pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len) -> int:
+    n = lib().pa_decode_workspace_size(int(num_seqs), int(num_heads), int(num_kv_heads), int(head_dim),
+                                       int(max_context_len))
     if n == 0 and num_seqs >= 0:
         raise PAError(PA_ERR_INVALID_ARG, "pa_decode_workspace_size")
     return n

@@ -109,11 +109,12 @@ __device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t &r0, u
                  : "memory");
 }
 
-// D = A(16x16, row) * B(16x8, col) + C, fp16 inputs, fp32 accumulate.
+// D = A(16x16, row) * B(16x8, col) + C, fp16 inputs, fp32 accumulate.  A pure
+// register operation (not volatile), so the compiler may schedule it freely.
 __device__ __forceinline__ void mma_16816(float &d0, float &d1, float &d2, float &d3, uint32_t a0, uint32_t a1,
                                           uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1, float c0,
                                           float c1, float c2, float c3) {
-    asm volatile(
+    asm(
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
         "{%8, %9}, {%10, %11, %12, %13};"
         : "=f"(d0), "=f"(d1), "=f"(d2), "=f"(d3)
@@ -123,6 +124,29 @@ __device__ __forceinline__ void mma_16816(float &d0, float &d1, float &d2, float
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
     __half2 h = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&h);
+}
+
+}  // namespace pa
+
+namespace pa {
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Transpose an 8x8 matrix of 16-bit elements held one row pair per lane
+// (the mma fragment layout) across the warp.
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t d;
+    asm("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+    return d;
+}
+
+// 2^x, hardware approximation (flushes subnormal results to zero).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 }  // namespace pa

@@ -12,27 +12,29 @@
 // incremental, tile-by-tile softmax is section "PagedAttention vs.
 // FlashAttention" of the deeplearn.tn page.
 //
-// How (three launches on the caller's stream):
+// How (two launches on the caller's stream):
 //  1. decode_prep_kernel (one CTA): splits every sequence into partitions of
-//     PART_TOKENS tokens, writes the compact list of (sequence, partition)
-//     work items into the workspace, zeroes the work counter, and writes the
-//     rows of empty (zero) and invalid (NaN) sequences.
-//  2. decode_kernel (persistent, one warp = one independent pipeline):
-//     each warp takes work items (sequence, partition, kv head) from an atomic
-//     counter.  For an item it streams 16-token chunks of the K and V tiles
-//     through a DEPTH-deep ring of shared-memory stages with TMA (2-D tiled
-//     copies through a tensor map over the cache, 128-byte swizzle), the
-//     gather being the per-chunk TMA y coordinate taken from the block table.
-//     The G query heads of the kv head ride on the M dimension of
-//     m16n8k16 tensor-core MMAs: S = Q K^T (heads x tokens) and O += P V,
-//     with ldmatrix from the swizzled tiles (bank-conflict free) and an
-//     online softmax in fp32 registers.  Each KV tile is read from HBM once
-//     for the whole group.  A single-partition sequence writes its fp16
-//     output directly; otherwise the item writes (m, l, unnormalised o) to
-//     the workspace.
-//  3. decode_merge_kernel: log-sum-exp merge of the partitions of every
-//     multi-partition sequence: M = max m_p, w_p = 2^(m_p - M),
-//     out = sum_p w_p o_p / sum_p w_p l_p.
+//     PT tokens (PT = 256, 512 or 1024, chosen from the shapes), writes the compact list of (sequence, partition)
+//     work items into the workspace, zeroes the work and merge counters, and
+//     writes the rows of empty (zero) and invalid (NaN) sequences.
+//  2. decode_kernel (persistent, warp-specialised).  In every CTA one
+//     producer warp takes work items (sequence, partition, kv head) from an
+//     atomic counter on behalf of NC consumer warps and streams each item's
+//     16-token chunks of K and V into that consumer's ring of DEPTH shared
+//     memory stages with TMA: 2-D tiled copies through a tensor map over the
+//     cache with a 128-byte swizzle, the gather being the TMA row coordinate
+//     read from the block table.  Full/empty mbarriers pace the rings.
+//     A consumer warp reduces one item at a time with m16n8k16 tensor-core
+//     MMAs, tokens on M and the G query heads of the kv head on N:
+//     S^T = K Q^T, an online softmax per head in fp32 (rescaling the running
+//     sums only when the maximum grows by more than 2^8), then
+//     O^T += V^T P^T, P^T moved into operand layout with movmatrix.  Each KV
+//     tile crosses HBM once for the whole group.  A single-partition sequence
+//     writes its fp16 output directly.  Otherwise the item stores (m, l,
+//     unnormalised o) in the workspace and takes a ticket; the item that
+//     completes its (sequence, kv head) group merges the group's partitions
+//     by the log-sum-exp rule
+//       M = max_p m_p,  w_p = 2^(m_p - M),  out = sum_p w_p o_p / sum_p w_p l_p.
 //
 // Results do not depend on the physical placement, on the block size or on
 // which warp ran which item: every item is reduced by one warp in a fixed
@@ -46,15 +48,40 @@
 
 #include "common.cuh"
 
+#ifndef PA_DECODE_CONSUMERS
+#define PA_DECODE_CONSUMERS 1
+#endif
+#ifndef PA_DECODE_DEPTH
+#define PA_DECODE_DEPTH 2
+#endif
+#ifndef PA_DECODE_MINB
+#define PA_DECODE_MINB 8
+#endif
+
 namespace pa {
 namespace {
 
-constexpr int PART_TOKENS = 512;       // tokens per partition (one work item)
-constexpr int CHUNK = 16;              // tokens per pipeline stage
-constexpr int NWARPS = 2;              // independent warps per CTA
-constexpr int DEPTH = 4;               // pipeline stages per warp
-constexpr long long WAIT_LIMIT = 1LL << 31;   // clock cycles (about a second)
+constexpr int MAX_PART_TOKENS = 1024;           // largest partition (one work item)
+constexpr long long TARGET_ITEMS = 4096;        // work items wanted for load balance
+constexpr int CHUNK = 16;                       // tokens per pipeline stage (one MMA K step of P V)
+constexpr int NC = PA_DECODE_CONSUMERS;         // consumer warps per CTA
+constexpr int DEPTH = PA_DECODE_DEPTH;          // pipeline stages per consumer
+constexpr int NWARPS = NC + 1;                  // + the producer warp
+constexpr long long WAIT_LIMIT = 1LL << 31;     // clock cycles (about a second)
 constexpr int PREP_THREADS = 1024;
+constexpr float RESCALE_THRESHOLD = 8.f;        // log2 units: rescale when the max grows by more than 2^8
+constexpr int ENTRIES = MAX_PART_TOKENS / 8 / 32;   // block-table entries per lane for one item (block size >= 8)
+
+// Partition size: the largest of 1024, 512, 256 tokens whose estimated item
+// count (sequences x kv heads x partitions of the longest context) reaches
+// TARGET_ITEMS, so that long batches get long, cheap items and short ones
+// still spread over every SM.  It depends on the shapes only, so a given
+// call always partitions the same way.
+int part_tokens(int B, int Hkv, int max_ctx) {
+    for (int pt = MAX_PART_TOKENS; pt > 256; pt /= 2)
+        if ((long long)B * Hkv * ((max_ctx + pt - 1) / pt) >= TARGET_ITEMS) return pt;
+    return 256;
+}
 
 struct WsHeader {
     int error;
@@ -65,20 +92,23 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
 struct WsLayout {
-    size_t part_off, sp_info, ml, o, total;
-    int pmax;
+    size_t part_off, sp_info, grp, ml, o, total;
+    int pmax, pt;
 };
 
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
-WsLayout ws_layout(int B, int Hq, int D, int max_ctx) {
+WsLayout ws_layout(int B, int Hq, int Hkv, int D, int max_ctx) {
     WsLayout w;
-    w.pmax = max_ctx > 0 ? (max_ctx + PART_TOKENS - 1) / PART_TOKENS : 1;
+    w.pt = part_tokens(B, Hkv, max_ctx);
+    w.pmax = max_ctx > 0 ? (max_ctx + w.pt - 1) / w.pt : 1;
     size_t off = sizeof(WsHeader);
     w.part_off = off;
     off += up256(sizeof(int) * ((size_t)B + 1));
     w.sp_info = off;
     off += up256(sizeof(int4) * (size_t)B * w.pmax);
+    w.grp = off;
+    if (w.pmax > 1) off += up256(sizeof(int) * (size_t)B * Hq);
     w.ml = off;
     if (w.pmax > 1) off += up256(sizeof(float2) * (size_t)B * w.pmax * Hq);
     w.o = off;
@@ -91,51 +121,53 @@ struct DecodeArgs {
     __half *out;
     const __half *query;
     const int32_t *block_tables;
-    int Hq, Hkv, G, bs, mbps;
+    int Hq, Hkv, G, bs, mbps, pt;
     long long num_blocks;
     float scale_log2;
     WsHeader *hdr;
+    const int *part_off;
     const int4 *sp_info;
+    int *grp;
     float2 *ws_ml;
     float *ws_o;
 };
 
-struct StageMeta {
-    int chunk, ntok, qslot, flags;     // flags: 1 = first chunk of the item, 2 = last
-};
-struct ItemInfo {
-    int seq, kvh, sp, P, bad, pad0, pad1, pad2;
+// What the producer tells a consumer about its next item (32 bytes).
+struct ItemDesc {
+    int seq, kvh, sp, P, nchunks, ntok_last, bad, end;
 };
 
-template <int D, int GPAD>
+template <int D, int NT>
 struct Cfg {
-    static constexpr int BOXES = D / 64;                  // 64-column (128-byte) boxes per tile row
-    static constexpr int TILE = BOXES * CHUNK * 128;      // one 16-token K or V tile
-    static constexpr int STAGE = 2 * TILE;                // K tile then V tile
-    static constexpr int QSLOT = GPAD * D * 2;
-    static constexpr int DATA = DEPTH * STAGE + 2 * QSLOT;   // per warp, multiple of 1024
-    static constexpr int CTRL = 256;                      // per warp: barriers, stage meta, item info
-    static constexpr int SMEM = NWARPS * (DATA + CTRL) + 1024;
+    static constexpr int BOXES = D / 64;                   // 64-column (128-byte) boxes per tile row
+    static constexpr int TILE = BOXES * CHUNK * 128;       // one 16-token K or V tile
+    static constexpr int STAGE = 2 * TILE;                 // K tile then V tile
+    static constexpr int QSLOT = NT * 8 * D * 2;           // the group's query rows
+    static constexpr int DATA = DEPTH * STAGE + 2 * QSLOT; // per consumer, a multiple of 1024
+    static constexpr int CTRL = 256;                       // per consumer: barriers and descriptors
+    static constexpr int SMEM = NC * (DATA + CTRL) + 1024;
     static_assert(DATA % 1024 == 0, "stages must stay 1024-byte aligned for the 128-byte swizzle");
-    static_assert(DEPTH * 8 + DEPTH * 16 + 2 * 32 <= CTRL, "control block too small");
+    static_assert((2 * DEPTH + 2) * 8 + 2 * 32 <= CTRL, "control block too small");
 };
 
-// Address of 16-byte column `col` (0 .. D/8-1) of row `row` of a swizzled
-// tile: 64-column boxes of CHUNK rows x 128 bytes, chunk j of row r stored at
-// position j ^ (r & 7) (the TMA 128-byte swizzle).
-__device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int col) {
-    return tile + (uint32_t)((col >> 3) * (CHUNK * 128) + row * 128 + (((col & 7) ^ (row & 7)) << 4));
+// Byte offset, inside a swizzled tile, of 16-byte column `col` (0 .. D/8-1)
+// of row `row`: 64-column boxes of CHUNK rows x 128 bytes; chunk j of row r
+// sits at position j ^ (r & 7) (the TMA 128-byte swizzle).
+__host__ __device__ constexpr int swz(int row, int col) {
+    return (col >> 3) * (CHUNK * 128) + row * 128 + (((col & 7) ^ (row & 7)) << 4);
 }
 
 // -------------------------------------------------------------- prep
 
 __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
     const int32_t *__restrict__ context_lens, int B, int Hq, int D, int Hkv, int max_ctx, long long max_table_tokens,
-    WsHeader *hdr, int *part_off, int4 *sp_info, __half *out) {
+    int pt, WsHeader *hdr, int *part_off, int4 *sp_info, int *grp, __half *out) {
     __shared__ int warp_sums[PREP_THREADS / 32];
     __shared__ int running;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
     if (threadIdx.x == 0) running = 0;
+    if (grp)
+        for (long long k = threadIdx.x; k < (long long)B * Hkv; k += PREP_THREADS) grp[k] = 0;
     __syncthreads();
     for (int base = 0; base < B; base += PREP_THREADS) {
         const int i = base + threadIdx.x;
@@ -147,7 +179,7 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
             else if (L == 0)
                 code = 1;
             else
-                P = (L + PART_TOKENS - 1) / PART_TOKENS;
+                P = (L + pt - 1) / pt;
         }
         int x = P;
 #pragma unroll
@@ -192,401 +224,554 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
 
 // ------------------------------------------------------------ decode
 
-template <int D, int GPAD>
-__global__ void __launch_bounds__(NWARPS * 32) decode_kernel(const __grid_constant__ CUtensorMap tmk,
-                                                             const __grid_constant__ CUtensorMap tmv,
-                                                             const DecodeArgs a) {
-    using C = Cfg<D, GPAD>;
-    constexpr bool TWO = GPAD == 16;             // query heads 8..15 of the group present
-    constexpr int KS = D / 16;                    // k-steps of Q K^T
-    constexpr int ND = D / 8;                     // n-tiles of P V
-    constexpr int NA = TWO ? 4 : 2;               // accumulator registers per n-tile
-    extern __shared__ uint8_t smem_raw[];
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int r = lane >> 2, c = lane & 3;        // mma fragment row / column pair
+struct ConsumerSmem {
+    uint32_t data;        // shared address of the consumer's stages and query slots
+    uint64_t *full;       // [DEPTH]: stage loaded (producer arrive + TMA bytes)
+    uint64_t *empty;      // [DEPTH]: stage consumed (consumer arrive)
+    uint64_t *qfree;      // [2]: query slot / descriptor free again
+    ItemDesc *desc;       // [2]
+};
 
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *wdata = smem + warp * C::DATA;
-    uint8_t *wctrl = smem + NWARPS * C::DATA + warp * C::CTRL;
-    const uint32_t sdata = smem_u32(wdata);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(wctrl);
-    StageMeta *meta = reinterpret_cast<StageMeta *>(wctrl + DEPTH * 8);
-    ItemInfo *info = reinterpret_cast<ItemInfo *>(wctrl + DEPTH * 8 + DEPTH * 16);
-    const uint32_t qslot0 = sdata + DEPTH * C::STAGE;
+template <int D, int NT>
+__device__ __forceinline__ ConsumerSmem consumer_smem(uint8_t *smem, int c) {
+    using C = Cfg<D, NT>;
+    uint8_t *ctrl = smem + NC * C::DATA + c * C::CTRL;
+    ConsumerSmem s;
+    s.data = smem_u32(smem + c * C::DATA);
+    s.full = reinterpret_cast<uint64_t *>(ctrl);
+    s.empty = s.full + DEPTH;
+    s.qfree = s.empty + DEPTH;
+    s.desc = reinterpret_cast<ItemDesc *>(ctrl + (2 * DEPTH + 2) * 8);
+    return s;
+}
 
-    if (lane == 0) {
-        for (int s = 0; s < DEPTH; ++s) mbar_init(smem_u32(&bars[s]), 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-
+// Producer warp: hands items to the consumers round-robin and keeps their
+// rings full.  All lanes run the loop; lane 0 issues the copies.
+template <int D, int NT>
+__device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMap *tmv, const DecodeArgs &a) {
+    using C = Cfg<D, NT>;
+    const int lane = threadIdx.x & 31;
     const int total = a.hdr->total_items;
     const uint64_t pol = policy_evict_first();
     const int box_rows = a.bs < CHUNK ? a.bs : CHUNK;
 
-    // ---- issue side: the item being issued (c_*) and the prefetched next one (n_*)
-    int n_item = -1, n_seq = 0, n_p = 0, n_L = 0, n_P = 0, n_fb = 0, n_tb0 = -1, n_tb1 = -1;
-    auto fetch_next = [&]() {
-        int j = 0;
-        if (lane == 0) j = atomicAdd(&a.hdr->counter, 1);
-        j = __shfl_sync(0xffffffffu, j, 0);
-        if (j >= total) {
-            n_item = -1;
-            return;
+    // Items are prefetched in three depths so that no latency is waited on
+    // when a consumer needs its next item: the work-counter ticket three items
+    // ahead (lane 0), the item record two ahead, and one ahead the item's
+    // fields plus, per lane, its block-table entries lane and lane + 32.
+    int raw = 0;
+    int nn_item = -1;
+    int4 nn_inf = make_int4(0, 0, 0, 0);
+    int n_item = -1, n_seq = 0, n_p = 0, n_L = 0, n_P = 0, n_fb = 0;
+    int n_e[ENTRIES];
+#pragma unroll
+    for (int e = 0; e < ENTRIES; ++e) n_e[e] = 0;
+    auto advance = [&]() {
+        n_item = nn_item;
+        if (n_item >= 0) {
+            n_seq = nn_inf.x;
+            n_p = nn_inf.y;
+            n_L = nn_inf.z;
+            n_P = nn_inf.w;
+            const int t0 = n_p * a.pt;
+            const int t1 = min(n_L, t0 + a.pt);
+            n_fb = t0 / a.bs;
+            const int nb = (t1 + a.bs - 1) / a.bs - n_fb;
+            const int32_t *row = a.block_tables + (long long)n_seq * a.mbps + n_fb;
+#pragma unroll
+            for (int e = 0; e < ENTRIES; ++e) n_e[e] = lane + 32 * e < nb ? row[lane + 32 * e] : 0;
         }
-        n_item = j;
-        const int4 inf = a.sp_info[j / a.Hkv];
-        n_seq = inf.x;
-        n_p = inf.y;
-        n_L = inf.z;
-        n_P = inf.w;
-        const int t0 = n_p * PART_TOKENS;
-        const int t1 = min(n_L, t0 + PART_TOKENS);
-        n_fb = t0 / a.bs;
-        const int nb = (t1 + a.bs - 1) / a.bs - n_fb;
-        const int32_t *row = a.block_tables + (long long)n_seq * a.mbps + n_fb;
-        n_tb0 = lane < nb ? row[lane] : -1;
-        n_tb1 = lane + 32 < nb ? row[lane + 32] : -1;
+        const int j = __shfl_sync(0xffffffffu, raw, 0);
+        nn_item = j < total ? j : -1;
+        if (nn_item >= 0) nn_inf = a.sp_info[nn_item / a.Hkv];
+        if (lane == 0) raw = atomicAdd(&a.hdr->counter, 1);
     };
 
-    int c_seq = 0, c_kvh = 0, c_t0 = 0, c_t1 = 0, c_fb = 0, c_tb0 = -1, c_tb1 = -1;
-    int c_chunk = 0, c_nchunks = 0, c_qslot = 0;
-    int started = 0, in_flight = 0, issued = 0, computed = 0;
-    bool done_issuing = false;
-
-    fetch_next();
-
-    // ---- compute side
-    float m0 = -INFINITY, l0 = 0.f, m1 = -INFINITY, l1 = 0.f;
-    float acc[ND][TWO ? 4 : 2];
-    uint32_t qf[KS][TWO ? 4 : 2];
+    // per-consumer state (NC is small and the loops over it are unrolled)
+    int sc[NC], ic[NC], chunk[NC], nch[NC], t0[NC], t1[NC], fb[NC], y[NC][ENTRIES], qrow[NC];
+    bool done[NC], bad[NC];
 #pragma unroll
-    for (int n = 0; n < ND; ++n)
+    for (int c = 0; c < NC; ++c) {
+        sc[c] = ic[c] = chunk[c] = nch[c] = t0[c] = t1[c] = fb[c] = qrow[c] = 0;
 #pragma unroll
-        for (int e = 0; e < (TWO ? 4 : 2); ++e) acc[n][e] = 0.f;
+        for (int e = 0; e < ENTRIES; ++e) y[c][e] = 0;
+        done[c] = bad[c] = false;
+    }
+    if (lane == 0) raw = atomicAdd(&a.hdr->counter, 1);
+    advance();
+    advance();
+    int live = NC;
+    while (live > 0) {
 #pragma unroll
-    for (int k = 0; k < KS; ++k)
-#pragma unroll
-        for (int e = 0; e < (TWO ? 4 : 2); ++e) qf[k][e] = 0u;
-
-    while (true) {
-        // -------- fill the ring
-        while (!done_issuing && issued - computed < DEPTH) {
-            if (c_chunk == c_nchunks) {
-                if (in_flight == 2) break;           // both query slots busy
-                if (n_item < 0) {
-                    done_issuing = true;
-                    break;
+        for (int c = 0; c < NC; ++c) {
+            if (done[c]) continue;
+            const ConsumerSmem cs = consumer_smem<D, NT>(smem, c);
+            const int s = sc[c] % DEPTH;
+            const uint32_t full = smem_u32(&cs.full[s]);
+            bool ok = mbar_wait_bounded(smem_u32(&cs.empty[s]), ((sc[c] / DEPTH) & 1) ^ 1, WAIT_LIMIT);
+            bool first = false;
+            if (ok && chunk[c] == nch[c]) {          // the consumer needs its next item
+                const int q = ic[c] & 1;
+                ok = mbar_wait_bounded(smem_u32(&cs.qfree[q]), ((ic[c] >> 1) & 1) ^ 1, WAIT_LIMIT);
+                if (ok && n_item < 0) {              // nothing left: tell the consumer to stop
+                    if (lane == 0) {
+                        ItemDesc e = {0, 0, 0, 0, 0, 0, 0, 1};
+                        cs.desc[q] = e;
+                        mbar_arrive(full);
+                    }
+                    done[c] = true;
+                    --live;
+                    continue;
                 }
-                const int sp = n_item / a.Hkv;
-                c_kvh = n_item - sp * a.Hkv;
-                c_seq = n_seq;
-                c_t0 = n_p * PART_TOKENS;
-                c_t1 = min(n_L, c_t0 + PART_TOKENS);
-                c_fb = n_fb;
-                c_tb0 = n_tb0;
-                c_tb1 = n_tb1;
-                c_chunk = 0;
-                c_nchunks = (c_t1 - c_t0 + CHUNK - 1) / CHUNK;
-                c_qslot = started & 1;
-                ++started;
-                ++in_flight;
-                if (lane == 0) {
-                    ItemInfo ii;
-                    ii.seq = n_seq;
-                    ii.kvh = c_kvh;
-                    ii.sp = sp;
-                    ii.P = n_P;
-                    ii.bad = 0;
-                    ii.pad0 = ii.pad1 = ii.pad2 = 0;
-                    info[c_qslot] = ii;
+                if (ok) {
+                    const int sp = n_item / a.Hkv;
+                    const int kvh = n_item - sp * a.Hkv;
+                    t0[c] = n_p * a.pt;
+                    t1[c] = min(n_L, t0[c] + a.pt);
+                    fb[c] = n_fb;
+                    nch[c] = (t1[c] - t0[c] + CHUNK - 1) / CHUNK;
+                    const int nb = (t1[c] + a.bs - 1) / a.bs - n_fb;
+                    bool bad_any = false;
+#pragma unroll
+                    for (int e = 0; e < ENTRIES; ++e) {
+                        bad_any |= lane + 32 * e < nb && (n_e[e] < 0 || n_e[e] >= a.num_blocks);
+                        y[c][e] = (int)(((long long)n_e[e] * a.Hkv + kvh) * a.bs);
+                    }
+                    bad[c] = __any_sync(0xffffffffu, bad_any);
+                    qrow[c] = n_seq * a.Hq + kvh * a.G;
+                    chunk[c] = 0;
+                    if (lane == 0) {
+                        ItemDesc d;
+                        d.seq = n_seq;
+                        d.kvh = kvh;
+                        d.sp = sp;
+                        d.P = n_P;
+                        d.nchunks = nch[c];
+                        d.ntok_last = t1[c] - (t0[c] + (nch[c] - 1) * CHUNK);
+                        d.bad = bad[c] ? 1 : 0;
+                        d.end = 0;
+                        cs.desc[q] = d;
+                    }
+                    ++ic[c];
+                    first = true;
+                    advance();
                 }
-                fetch_next();
             }
-            const int s = issued % DEPTH;
-            const int tok0 = c_t0 + c_chunk * CHUNK;
-            const int ntok = min(CHUNK, c_t1 - tok0);
-            const int lb0 = tok0 / a.bs - c_fb;
-            const int phys0 = __shfl_sync(0xffffffffu, lb0 < 32 ? c_tb0 : c_tb1, lb0 & 31);
-            const bool two_blocks = a.bs < CHUNK && ntok > a.bs;
+            if (!ok) {   // a consumer stopped answering: record it and stop feeding everyone
+                if (lane == 0) atomicExch(&a.hdr->error, PA_ERR_TIMEOUT);
+                return;
+            }
+            // issue chunk `chunk[c]` of the consumer's item into stage s
+            const int tok0 = t0[c] + chunk[c] * CHUNK;
+            const int ntok = min(CHUNK, t1[c] - tok0);
+            const int lb0 = tok0 / a.bs - fb[c];
             const int lb1 = lb0 + 1;
-            const int phys1 = __shfl_sync(0xffffffffu, lb1 < 32 ? c_tb0 : c_tb1, lb1 & 31);
+            int va = y[c][0], vb = y[c][0];
+#pragma unroll
+            for (int e = 1; e < ENTRIES; ++e) {
+                va = (lb0 >> 5) == e ? y[c][e] : va;
+                vb = (lb1 >> 5) == e ? y[c][e] : vb;
+            }
+            const int ya = __shfl_sync(0xffffffffu, va, lb0 & 31);
+            const int yb = __shfl_sync(0xffffffffu, vb, lb1 & 31);
             if (lane == 0) {
-                const bool bad = phys0 < 0 || phys0 >= a.num_blocks ||
-                                 (two_blocks && (phys1 < 0 || phys1 >= a.num_blocks));
-                const bool first = c_chunk == 0;
-                const bool last = c_chunk == c_nchunks - 1;
-                uint32_t bytes = 0;
-                if (!bad) bytes = 2u * C::BOXES * box_rows * 128u * (two_blocks ? 2u : 1u);
-                if (first) bytes += (uint32_t)(a.G * D * 2);
-                StageMeta mt;
-                mt.chunk = c_chunk;
-                mt.ntok = ntok;
-                mt.qslot = c_qslot;
-                mt.flags = (first ? 1 : 0) | (last ? 2 : 0);
-                meta[s] = mt;
-                if (bad) info[c_qslot].bad = 1;
-                const uint32_t bar = smem_u32(&bars[s]);
-                const uint32_t kdst = sdata + s * C::STAGE;
-                const uint32_t vdst = kdst + C::TILE;
-                mbar_arrive_expect_tx(bar, bytes);
-                if (!bad) {
-                    const int row0 = tok0 % a.bs;
-                    const int y0 = (int)(((long long)phys0 * a.Hkv + c_kvh) * a.bs + row0);
+                const bool two = a.bs < CHUNK && ntok > a.bs;
+                uint32_t bytes = bad[c] ? 0u : 2u * C::BOXES * box_rows * 128u * (two ? 2u : 1u);
+                if (first && !bad[c]) bytes += (uint32_t)(a.G * D * 2);
+                mbar_arrive_expect_tx(full, bytes);
+                if (!bad[c]) {
+                    const uint32_t kdst = cs.data + s * C::STAGE;
+                    const uint32_t vdst = kdst + C::TILE;
+                    const int y = ya + tok0 % a.bs;
 #pragma unroll
                     for (int b = 0; b < C::BOXES; ++b) {
-                        tma_load_2d(kdst + b * CHUNK * 128, &tmk, 64 * b, y0, bar, pol);
-                        tma_load_2d(vdst + b * CHUNK * 128, &tmv, 64 * b, y0, bar, pol);
+                        tma_load_2d(kdst + b * CHUNK * 128, tmk, 64 * b, y, full, pol);
+                        tma_load_2d(vdst + b * CHUNK * 128, tmv, 64 * b, y, full, pol);
                     }
-                    if (two_blocks) {
-                        const int y1 = (int)(((long long)phys1 * a.Hkv + c_kvh) * a.bs);
+                    if (two) {
 #pragma unroll
                         for (int b = 0; b < C::BOXES; ++b) {
-                            tma_load_2d(kdst + b * CHUNK * 128 + a.bs * 128, &tmk, 64 * b, y1, bar, pol);
-                            tma_load_2d(vdst + b * CHUNK * 128 + a.bs * 128, &tmv, 64 * b, y1, bar, pol);
+                            tma_load_2d(kdst + b * CHUNK * 128 + a.bs * 128, tmk, 64 * b, yb, full, pol);
+                            tma_load_2d(vdst + b * CHUNK * 128 + a.bs * 128, tmv, 64 * b, yb, full, pol);
                         }
                     }
-                }
-                if (first) {
-                    const __half *qsrc = a.query + ((long long)c_seq * a.Hq + (long long)c_kvh * a.G) * D;
-                    bulk_load(qslot0 + c_qslot * C::QSLOT, qsrc, (uint32_t)(a.G * D * 2), bar);
-                }
-            }
-            ++c_chunk;
-            ++issued;
-        }
-        __syncwarp();
-        if (computed == issued) break;
-
-        // -------- compute one stage
-        const int s = computed % DEPTH;
-        if (!mbar_wait_bounded(smem_u32(&bars[s]), (uint32_t)((computed / DEPTH) & 1), WAIT_LIMIT)) {
-            if (lane == 0) atomicExch(&a.hdr->error, PA_ERR_TIMEOUT);
-            // let this warp's other copies land (bounded) before leaving
-            for (int k = computed + 1; k < issued; ++k)
-                mbar_wait_bounded(smem_u32(&bars[k % DEPTH]), (uint32_t)((k / DEPTH) & 1), WAIT_LIMIT >> 4);
-            return;
-        }
-        const StageMeta mt = meta[s];
-        const uint32_t kt = sdata + s * C::STAGE;
-        const uint32_t vt = kt + C::TILE;
-
-        if (mt.flags & 1) {   // new item: load the group's query rows, reset the running state
-            const __half *q = reinterpret_cast<const __half *>(wdata + DEPTH * C::STAGE + mt.qslot * C::QSLOT);
-#pragma unroll
-            for (int k = 0; k < KS; ++k) {
-                qf[k][0] = *reinterpret_cast<const uint32_t *>(q + r * D + 16 * k + 2 * c);
-                qf[k][1] = *reinterpret_cast<const uint32_t *>(q + r * D + 16 * k + 8 + 2 * c);
-                if constexpr (TWO) {
-                    qf[k][TWO ? 2 : 0] = *reinterpret_cast<const uint32_t *>(q + (r + 8) * D + 16 * k + 2 * c);
-                    qf[k][TWO ? 3 : 0] = *reinterpret_cast<const uint32_t *>(q + (r + 8) * D + 16 * k + 8 + 2 * c);
+                    if (first)
+                        bulk_load(cs.data + DEPTH * C::STAGE + ((ic[c] - 1) & 1) * C::QSLOT,
+                                  a.query + (long long)qrow[c] * D, (uint32_t)(a.G * D * 2), full);
                 }
             }
-            m0 = m1 = -INFINITY;
-            l0 = l1 = 0.f;
-#pragma unroll
-            for (int n = 0; n < ND; ++n)
-#pragma unroll
-                for (int e = 0; e < (TWO ? 4 : 2); ++e) acc[n][e] = 0.f;
+            ++chunk[c];
+            ++sc[c];
         }
-
-        // S = Q K^T for the 16 tokens of the chunk: two n-tiles of 8 tokens
-        float sc[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
-#pragma unroll
-            for (int kp = 0; kp < D / 32; ++kp) {
-                uint32_t b0, b1, b2, b3;
-                ldmatrix_x4(swz(kt, nt * 8 + (lane & 7), kp * 4 + (lane >> 3)), b0, b1, b2, b3);
-#pragma unroll
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    const int k = 2 * kp + h2;
-                    uint32_t a1 = 0u, a3 = 0u;
-                    if constexpr (TWO) {
-                        a1 = qf[k][TWO ? 2 : 0];
-                        a3 = qf[k][TWO ? 3 : 0];
-                    }
-                    float d2, d3;
-                    mma_16816(sc[nt][0], sc[nt][1], d2, d3, qf[k][0], a1, qf[k][1], a3, h2 ? b2 : b0, h2 ? b3 : b1,
-                              sc[nt][0], sc[nt][1], sc[nt][2], sc[nt][3]);
-                    if constexpr (TWO) {
-                        sc[nt][2] = d2;
-                        sc[nt][3] = d3;
-                    }
-                }
-            }
-        }
-
-        // online softmax (base 2), rows r and r + 8
-        const int ntok = mt.ntok;
-        const float sl2 = a.scale_log2;
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int tok = nt * 8 + 2 * c + (e & 1);
-                sc[nt][e] = tok < ntok ? sc[nt][e] * sl2 : -INFINITY;
-            }
-        uint32_t pa0, pa1 = 0u, pa2, pa3 = 0u;
-        {
-            float mx = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float mn = fmaxf(m0, mx);
-            const float alpha = exp2f(m0 - mn);
-            const float p00 = exp2f(sc[0][0] - mn), p01 = exp2f(sc[0][1] - mn);
-            const float p10 = exp2f(sc[1][0] - mn), p11 = exp2f(sc[1][1] - mn);
-            l0 = l0 * alpha + ((p00 + p01) + (p10 + p11));
-            m0 = mn;
-#pragma unroll
-            for (int n = 0; n < ND; ++n) {
-                acc[n][0] *= alpha;
-                acc[n][1] *= alpha;
-            }
-            pa0 = pack_half2(p00, p01);
-            pa2 = pack_half2(p10, p11);
-        }
-        if constexpr (TWO) {
-            float mx = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float mn = fmaxf(m1, mx);
-            const float alpha = exp2f(m1 - mn);
-            const float p00 = exp2f(sc[0][2] - mn), p01 = exp2f(sc[0][3] - mn);
-            const float p10 = exp2f(sc[1][2] - mn), p11 = exp2f(sc[1][3] - mn);
-            l1 = l1 * alpha + ((p00 + p01) + (p10 + p11));
-            m1 = mn;
-#pragma unroll
-            for (int n = 0; n < ND; ++n) {
-                acc[n][TWO ? 2 : 0] *= alpha;
-                acc[n][TWO ? 3 : 0] *= alpha;
-            }
-            pa1 = pack_half2(p00, p01);
-            pa3 = pack_half2(p10, p11);
-        }
-
-        // O += P V: V^T fragments by transposing ldmatrix; masked tokens zeroed
-        // so that stale or poisoned slots past the context never reach O
-        uint32_t vmask_lo = 0xffffffffu, vmask_hi = 0xffffffffu;
-        if (ntok < CHUNK) {
-            vmask_lo = (2 * c < ntok ? 0x0000ffffu : 0u) | (2 * c + 1 < ntok ? 0xffff0000u : 0u);
-            vmask_hi = (2 * c + 8 < ntok ? 0x0000ffffu : 0u) | (2 * c + 9 < ntok ? 0xffff0000u : 0u);
-        }
-#pragma unroll
-        for (int np = 0; np < D / 16; ++np) {
-            const int mi = lane >> 3;
-            uint32_t v0, v1, v2, v3;
-            ldmatrix_x4_trans(swz(vt, ((mi & 1) << 3) + (lane & 7), 2 * np + (mi >> 1)), v0, v1, v2, v3);
-            v0 &= vmask_lo;
-            v2 &= vmask_lo;
-            v1 &= vmask_hi;
-            v3 &= vmask_hi;
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-                const int n = 2 * np + h2;
-                float c2 = 0.f, c3 = 0.f, d2, d3;
-                if constexpr (TWO) {
-                    c2 = acc[n][TWO ? 2 : 0];
-                    c3 = acc[n][TWO ? 3 : 0];
-                }
-                mma_16816(acc[n][0], acc[n][1], d2, d3, pa0, pa1, pa2, pa3, h2 ? v2 : v0, h2 ? v3 : v1, acc[n][0],
-                          acc[n][1], c2, c3);
-                if constexpr (TWO) {
-                    acc[n][TWO ? 2 : 0] = d2;
-                    acc[n][TWO ? 3 : 0] = d3;
-                }
-            }
-        }
-
-        if (mt.flags & 2) {   // item complete: write it out
-            const ItemInfo ii = info[mt.qslot];
-            float lr0 = l0 + __shfl_xor_sync(0xffffffffu, l0, 1);
-            lr0 += __shfl_xor_sync(0xffffffffu, lr0, 2);
-            float lr1 = 0.f;
-            if constexpr (TWO) {
-                lr1 = l1 + __shfl_xor_sync(0xffffffffu, l1, 1);
-                lr1 += __shfl_xor_sync(0xffffffffu, lr1, 2);
-            }
-            const float nanf_ = __int_as_float(0x7fc00000);
-#pragma unroll
-            for (int half_ = 0; half_ < (TWO ? 2 : 1); ++half_) {
-                const int row = r + 8 * half_;
-                if (row < a.G) {
-                    const int h = ii.kvh * a.G + row;
-                    const float lr = half_ ? lr1 : lr0;
-                    const float mrow = half_ ? m1 : m0;
-                    if (ii.P == 1) {
-                        const float inv = ii.bad ? nanf_ : 1.f / lr;
-                        __half *orow = a.out + ((long long)ii.seq * a.Hq + h) * D;
-#pragma unroll
-                        for (int n = 0; n < ND; ++n)
-                            *reinterpret_cast<uint32_t *>(orow + 8 * n + 2 * c) =
-                                pack_half2(acc[n][(2 * half_) % NA] * inv, acc[n][(2 * half_ + 1) % NA] * inv);
-                    } else {
-                        const long long wrow = (long long)ii.sp * a.Hq + h;
-                        float *orow = a.ws_o + wrow * D;
-#pragma unroll
-                        for (int n = 0; n < ND; ++n)
-                            *reinterpret_cast<float2 *>(orow + 8 * n + 2 * c) =
-                                ii.bad ? make_float2(nanf_, nanf_)
-                                       : make_float2(acc[n][(2 * half_) % NA], acc[n][(2 * half_ + 1) % NA]);
-                        if (c == 0) a.ws_ml[wrow] = ii.bad ? make_float2(nanf_, nanf_) : make_float2(mrow, lr);
-                    }
-                }
-            }
-            --in_flight;
-        }
-        __syncwarp();
-        fence_proxy_async_smem();   // this stage's reads before the next TMA write into it
-        ++computed;
     }
 }
 
-// ------------------------------------------------------------- merge
-
+// Log-sum-exp merge of the P partitions of one (sequence, kv head) group,
+// run by the consumer warp that completed the group.  Partials are read
+// through L2 (other warps wrote them) with many independent loads in flight.
+//  1. lane g < G walks the partitions of head g once, keeping the running
+//     maximum M_g and the rescaled normaliser L_g = sum_p 2^(m_p - M_g) l_p;
+//  2. all lanes sum the partial outputs: the G x D outputs, as float4s, are
+//     spread over the lanes; w = 2^(m_p - M_head) / L_head.
 template <int D>
-__global__ void __launch_bounds__(256) decode_merge_kernel(const int *__restrict__ part_off,
-                                                           const float2 *__restrict__ ws_ml,
-                                                           const float *__restrict__ ws_o, __half *__restrict__ out,
-                                                           int B, int Hq) {
-    constexpr int PER = D / 32;   // elements per lane
-    const long long row = (long long)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+__device__ void merge_group(const DecodeArgs &a, int seq, int kvh, int P) {
     const int lane = threadIdx.x & 31;
-    if (row >= (long long)B * Hq) return;
-    const int seq = (int)(row / Hq), h = (int)(row % Hq);
-    const int p0 = part_off[seq];
-    const int P = part_off[seq + 1] - p0;
-    if (P <= 1) return;
-    float M = -INFINITY;
-    for (int p = 0; p < P; ++p) M = fmaxf(M, ws_ml[(long long)(p0 + p) * Hq + h].x);
-    float acc[PER];
+    const long long p0 = a.part_off[seq];
+    const int h0 = kvh * a.G;
+    float M = -INFINITY, Ls = 0.f;
+    if (lane < a.G) {
+        const float2 *ml = a.ws_ml + p0 * a.Hq + h0 + lane;
+        int p = 0;
+        for (; p + 4 <= P; p += 4) {
+            float2 v[4];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc[e] = 0.f;
-    float lsum = 0.f;
-    for (int p = 0; p < P; ++p) {
-        const long long wrow = (long long)(p0 + p) * Hq + h;
-        const float2 ml = ws_ml[wrow];
-        const float w = exp2f(ml.x - M);
-        lsum += w * ml.y;
-        const float *o = ws_o + wrow * D + lane * PER;
-        if constexpr (PER == 4) {
-            const float4 v = *reinterpret_cast<const float4 *>(o);
-            acc[0] += w * v.x;
-            acc[1] += w * v.y;
-            acc[2] += w * v.z;
-            acc[3] += w * v.w;
-        } else {
-            const float2 v = *reinterpret_cast<const float2 *>(o);
-            acc[0] += w * v.x;
-            acc[1] += w * v.y;
+            for (int u = 0; u < 4; ++u) v[u] = __ldcg(ml + (long long)(p + u) * a.Hq);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float nm = fmaxf(M, v[u].x);
+                Ls = Ls * fast_exp2(M - nm) + v[u].y * fast_exp2(v[u].x - nm);
+                M = nm;
+            }
+        }
+        for (; p < P; ++p) {
+            const float2 v = __ldcg(ml + (long long)p * a.Hq);
+            const float nm = fmaxf(M, v.x);
+            Ls = Ls * fast_exp2(M - nm) + v.y * fast_exp2(v.x - nm);
+            M = nm;
         }
     }
-    const float inv = 1.f / lsum;
-    __half *orow = out + ((long long)seq * Hq + h) * D + lane * PER;
+    constexpr int PER_HEAD = D / 4;                 // float4s per output row
+    const int nvec = a.G * PER_HEAD;                // float4s of the group's outputs
+    const float *ob = a.ws_o + (p0 * a.Hq + h0) * D;
+    const float2 *mlb = a.ws_ml + p0 * a.Hq + h0;
+    const long long pstride = (long long)a.Hq * D / 4;   // float4s between partitions
+    __half *orow = a.out + ((long long)seq * a.Hq + h0) * D;
+    // 64 outputs (float4s) per pass, two per lane; partitions four at a time
+    for (int base = 0; base < nvec; base += 64) {
+        int k[2], hd[2];
+        bool on[2];
+        float Mh[2], inv[2];
+        float4 acc[2];
 #pragma unroll
-    for (int e = 0; e < PER; e += 2)
-        *reinterpret_cast<uint32_t *>(orow + e) = pack_half2(acc[e] * inv, acc[e + 1] * inv);
+        for (int i = 0; i < 2; ++i) {
+            k[i] = base + 32 * i + lane;
+            on[i] = k[i] < nvec;
+            hd[i] = min(k[i] / PER_HEAD, a.G - 1);
+            Mh[i] = __shfl_sync(0xffffffffu, M, hd[i]);
+            inv[i] = 1.f / __shfl_sync(0xffffffffu, Ls, hd[i]);
+            acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        const float4 *o4 = reinterpret_cast<const float4 *>(ob);
+        int p = 0;
+        for (; p + 4 <= P; p += 4) {
+            float4 v[4][2];
+            float mp[4][2];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+                    if (on[i]) {
+                        v[u][i] = __ldcg(o4 + (p + u) * pstride + k[i]);
+                        mp[u][i] = __ldcg(&mlb[(long long)(p + u) * a.Hq + hd[i]].x);
+                    }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+#pragma unroll
+                for (int i = 0; i < 2; ++i)
+                    if (on[i]) {
+                        const float w = fast_exp2(mp[u][i] - Mh[i]) * inv[i];
+                        acc[i].x += w * v[u][i].x;
+                        acc[i].y += w * v[u][i].y;
+                        acc[i].z += w * v[u][i].z;
+                        acc[i].w += w * v[u][i].w;
+                    }
+        }
+        for (; p < P; ++p)
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                if (on[i]) {
+                    const float4 v = __ldcg(o4 + p * pstride + k[i]);
+                    const float w = fast_exp2(__ldcg(&mlb[(long long)p * a.Hq + hd[i]].x) - Mh[i]) * inv[i];
+                    acc[i].x += w * v.x;
+                    acc[i].y += w * v.y;
+                    acc[i].z += w * v.z;
+                    acc[i].w += w * v.w;
+                }
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            if (on[i]) {
+                uint2 h;
+                h.x = pack_half2(acc[i].x, acc[i].y);
+                h.y = pack_half2(acc[i].z, acc[i].w);
+                *reinterpret_cast<uint2 *>(orow + 4 * k[i]) = h;
+            }
+    }
+}
+
+// Consumer warp c: reduces the items its producer hands it.
+template <int D, int NT>
+__device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
+    using C = Cfg<D, NT>;
+    constexpr int KS = D / 16;     // MMA k-steps of S^T = K Q^T
+    constexpr int MT = D / 16;     // MMA m-tiles of O^T = V^T P^T
+    const int lane = threadIdx.x & 31;
+    const int r = lane >> 2, cq = lane & 3;
+    const ConsumerSmem cs = consumer_smem<D, NT>(smem, c);
+
+    // per-lane swizzled ldmatrix offsets; the rest of each address is a constant
+    const int mi = lane >> 3, li = lane & 7;
+    int koff[4], voff[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        koff[u] = swz((mi & 1) * 8 + li, 2 * u + (mi >> 1));       // A = K rows (tokens), d-chunk 2u + ..
+        voff[u] = swz((mi >> 1) * 8 + li, 2 * u + (mi & 1));       // A = V^T via transposed loads
+    }
+    const float sl2 = a.scale_log2;
+
+    // a group ticket taken at the end of the previous multi-partition item
+    int pend_ticket = 0, pend_seq = 0, pend_kvh = 0, pend_P = 0;
+    auto settle = [&]() {
+        const int t = __shfl_sync(0xffffffffu, pend_ticket, 0);
+        if (pend_P > 0 && t == pend_P - 1) {
+            __threadfence();
+            merge_group<D>(a, pend_seq, pend_kvh, pend_P);
+        }
+        pend_P = 0;
+    };
+
+    int stage = 0;
+    for (int item = 0;; ++item) {
+        const int q = item & 1;
+        int s = stage % DEPTH;
+        if (!mbar_wait_bounded(smem_u32(&cs.full[s]), (stage / DEPTH) & 1, WAIT_LIMIT)) {
+            if (lane == 0) atomicExch(&a.hdr->error, PA_ERR_TIMEOUT);
+            return;
+        }
+        const ItemDesc dsc = cs.desc[q];
+        if (dsc.end) {
+            settle();
+            return;
+        }
+
+        // the group's query rows as MMA B fragments: B = Q^T (k = dim, n = head)
+        uint32_t qb[NT][KS][2];
+        {
+            const __half *qs = reinterpret_cast<const __half *>(smem + c * C::DATA + DEPTH * C::STAGE + q * C::QSLOT);
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int k = 0; k < KS; ++k) {
+                    const __half *row = qs + (t * 8 + r) * D + 16 * k + 2 * cq;
+                    qb[t][k][0] = *reinterpret_cast<const uint32_t *>(row);
+                    qb[t][k][1] = *reinterpret_cast<const uint32_t *>(row + 8);
+                }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&cs.qfree[q]));   // query slot and descriptor read
+
+        // running state per head column (2 * cq, 2 * cq + 1) of each head tile
+        float m[NT][2], l[NT][2];
+        float acc[MT][NT][4];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            m[t][0] = m[t][1] = -INFINITY;
+            l[t][0] = l[t][1] = 0.f;
+#pragma unroll
+            for (int i = 0; i < MT; ++i) acc[i][t][0] = acc[i][t][1] = acc[i][t][2] = acc[i][t][3] = 0.f;
+        }
+
+        for (int ch = 0; ch < dsc.nchunks; ++ch) {
+            if (ch > 0) {
+                s = stage % DEPTH;
+                if (!mbar_wait_bounded(smem_u32(&cs.full[s]), (stage / DEPTH) & 1, WAIT_LIMIT)) {
+                    if (lane == 0) atomicExch(&a.hdr->error, PA_ERR_TIMEOUT);
+                    return;
+                }
+            }
+            const uint32_t kt = cs.data + s * C::STAGE;
+            const uint32_t vt = kt + C::TILE;
+            const int ntok = ch == dsc.nchunks - 1 ? dsc.ntok_last : CHUNK;
+
+            // S^T (16 tokens x 8 heads per head tile): two accumulation chains
+            float sa[NT][4], sb[NT][4];
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sa[t][e] = sb[t][e] = 0.f;
+#pragma unroll
+            for (int k = 0; k < KS; ++k) {
+                uint32_t a0, a1, a2, a3;
+                ldmatrix_x4(kt + (k >> 2) * (C::BOXES > 1 ? CHUNK * 128 : 0) + koff[k & 3], a0, a1, a2, a3);
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    float *acc_s = (k & 1) ? sb[t] : sa[t];
+                    mma_16816(acc_s[0], acc_s[1], acc_s[2], acc_s[3], a0, a1, a2, a3, qb[t][k][0], qb[t][k][1],
+                              acc_s[0], acc_s[1], acc_s[2], acc_s[3]);
+                }
+            }
+            // V^T fragments, loaded ahead of the softmax
+            uint32_t va[MT][4];
+#pragma unroll
+            for (int i = 0; i < MT; ++i)
+                ldmatrix_x4_trans(vt + (i >> 2) * (C::BOXES > 1 ? CHUNK * 128 : 0) + voff[i & 3], va[i][0], va[i][1],
+                                  va[i][2], va[i][3]);
+
+            // softmax per head column; thread holds tokens r, r + 8
+            const bool tail = ntok < CHUNK;
+            const bool tok_lo = r < ntok, tok_hi = r + 8 < ntok;
+            uint32_t pb[NT][2];
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+                float s0 = sa[t][0] + sb[t][0], s1 = sa[t][1] + sb[t][1];   // token r, heads 2cq, 2cq+1
+                float s2 = sa[t][2] + sb[t][2], s3 = sa[t][3] + sb[t][3];   // token r + 8
+                if (tail) {
+                    s0 = tok_lo ? s0 : -INFINITY;
+                    s1 = tok_lo ? s1 : -INFINITY;
+                    s2 = tok_hi ? s2 : -INFINITY;
+                    s3 = tok_hi ? s3 : -INFINITY;
+                }
+                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+                for (int o = 4; o < 32; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                }
+                mx0 *= sl2;
+                mx1 *= sl2;
+                // keep a stale maximum until a score exceeds it by 2^8; then rescale
+                if (mx0 > m[t][0] + RESCALE_THRESHOLD || mx1 > m[t][1] + RESCALE_THRESHOLD) {
+                    const float n0 = fmaxf(m[t][0], mx0), n1 = fmaxf(m[t][1], mx1);
+                    const float al0 = fast_exp2(m[t][0] - n0), al1 = fast_exp2(m[t][1] - n1);
+                    m[t][0] = n0;
+                    m[t][1] = n1;
+                    l[t][0] *= al0;
+                    l[t][1] *= al1;
+#pragma unroll
+                    for (int i = 0; i < MT; ++i) {
+                        acc[i][t][0] *= al0;
+                        acc[i][t][1] *= al1;
+                        acc[i][t][2] *= al0;
+                        acc[i][t][3] *= al1;
+                    }
+                }
+                const float p0 = fast_exp2(fmaf(s0, sl2, -m[t][0])), p1 = fast_exp2(fmaf(s1, sl2, -m[t][1]));
+                const float p2 = fast_exp2(fmaf(s2, sl2, -m[t][0])), p3 = fast_exp2(fmaf(s3, sl2, -m[t][1]));
+                l[t][0] += p0 + p2;
+                l[t][1] += p1 + p3;
+                // P^T rows (tokens r, r+8) -> B operand of P V (k = token, n = head) by transposition
+                pb[t][0] = movmatrix_trans(pack_half2(p0, p1));
+                pb[t][1] = movmatrix_trans(pack_half2(p2, p3));
+            }
+            if (tail) {   // stale or poisoned slots past the context must not reach O
+                const uint32_t lo = (2 * cq < ntok ? 0x0000ffffu : 0u) | (2 * cq + 1 < ntok ? 0xffff0000u : 0u);
+                const uint32_t hi = (2 * cq + 8 < ntok ? 0x0000ffffu : 0u) | (2 * cq + 9 < ntok ? 0xffff0000u : 0u);
+#pragma unroll
+                for (int i = 0; i < MT; ++i) {
+                    va[i][0] &= lo;
+                    va[i][1] &= lo;
+                    va[i][2] &= hi;
+                    va[i][3] &= hi;
+                }
+            }
+            // O^T += V^T P^T
+#pragma unroll
+            for (int i = 0; i < MT; ++i)
+#pragma unroll
+                for (int t = 0; t < NT; ++t)
+                    mma_16816(acc[i][t][0], acc[i][t][1], acc[i][t][2], acc[i][t][3], va[i][0], va[i][1], va[i][2],
+                              va[i][3], pb[t][0], pb[t][1], acc[i][t][0], acc[i][t][1], acc[i][t][2], acc[i][t][3]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&cs.empty[s]));   // stage free for the next copy
+            ++stage;
+        }
+
+        // ---- item complete: row sums over the 8 token lanes, then write out
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                float v = l[t][e];
+                v += __shfl_xor_sync(0xffffffffu, v, 4);
+                v += __shfl_xor_sync(0xffffffffu, v, 8);
+                v += __shfl_xor_sync(0xffffffffu, v, 16);
+                l[t][e] = v;
+            }
+        const float qnan = __int_as_float(0x7fc00000);
+        if (dsc.P == 1) {
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int g = t * 8 + 2 * cq + e;
+                    if (g < a.G) {
+                        const float inv = dsc.bad ? qnan : 1.f / l[t][e];
+                        __half *orow = a.out + ((long long)dsc.seq * a.Hq + dsc.kvh * a.G + g) * D;
+#pragma unroll
+                        for (int i = 0; i < MT; ++i) {
+                            orow[16 * i + r] = __float2half_rn(acc[i][t][e] * inv);
+                            orow[16 * i + r + 8] = __float2half_rn(acc[i][t][e + 2] * inv);
+                        }
+                    }
+                }
+        } else {
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int g = t * 8 + 2 * cq + e;
+                    if (g < a.G) {
+                        const long long wrow = (long long)dsc.sp * a.Hq + dsc.kvh * a.G + g;
+                        float *orow = a.ws_o + wrow * D;
+#pragma unroll
+                        for (int i = 0; i < MT; ++i) {
+                            orow[16 * i + r] = dsc.bad ? qnan : acc[i][t][e];
+                            orow[16 * i + r + 8] = dsc.bad ? qnan : acc[i][t][e + 2];
+                        }
+                        if (r == 0) a.ws_ml[wrow] = dsc.bad ? make_float2(qnan, qnan) : make_float2(m[t][e], l[t][e]);
+                    }
+                }
+        }
+        // a merge owed from the previous multi-partition item (its ticket has
+        // had a whole item's time to come back)
+        settle();
+        if (dsc.P > 1) {
+            // take a ticket for the group; the warp that takes the last one
+            // merges the group, after its next item
+            __threadfence();
+            __syncwarp();
+            pend_ticket = 0;
+            if (lane == 0) pend_ticket = atomicAdd(&a.grp[dsc.seq * a.Hkv + dsc.kvh], 1);
+            pend_seq = dsc.seq;
+            pend_kvh = dsc.kvh;
+            pend_P = dsc.P;
+        }
+    }
+}
+
+template <int D, int NT>
+__global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? PA_DECODE_MINB : PA_DECODE_MINB / 2) decode_kernel(const __grid_constant__ CUtensorMap tmk,
+                                                             const __grid_constant__ CUtensorMap tmv,
+                                                             const DecodeArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        for (int c = 0; c < NC; ++c) {
+            const ConsumerSmem cs = consumer_smem<D, NT>(smem, c);
+            for (int s = 0; s < DEPTH; ++s) {
+                mbar_init(smem_u32(&cs.full[s]), 1);
+                mbar_init(smem_u32(&cs.empty[s]), 1);
+            }
+            mbar_init(smem_u32(&cs.qfree[0]), 1);
+            mbar_init(smem_u32(&cs.qfree[1]), 1);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (warp == 0)
+        producer<D, NT>(smem, &tmk, &tmv, a);
+    else
+        consumer<D, NT>(smem, warp - 1, a);
 }
 
 // ------------------------------------------------------------ host side
@@ -641,29 +826,25 @@ bool cache_tensor_map(CUtensorMap *map, const void *base, long long rows, int D,
     return true;
 }
 
-struct Launch {
-    int grid = 0;
-};
-
-template <int D, int GPAD>
+template <int D, int NT>
 int launch_decode(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeArgs &args, cudaStream_t st) {
-    using C = Cfg<D, GPAD>;
+    using C = Cfg<D, NT>;
     static int grid = 0;
     static std::once_flag once;
     static cudaError_t init_err = cudaSuccess;
     std::call_once(once, [] {
-        init_err = cudaFuncSetAttribute(decode_kernel<D, GPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        init_err = cudaFuncSetAttribute(decode_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (init_err != cudaSuccess) return;
         int dev = 0, sms = 0, per_sm = 0;
         init_err = cudaGetDevice(&dev);
         if (init_err == cudaSuccess) init_err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (init_err == cudaSuccess)
-            init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, GPAD>, NWARPS * 32,
+            init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, NT>, NWARPS * 32,
                                                                      C::SMEM);
         if (init_err == cudaSuccess) grid = sms * (per_sm > 0 ? per_sm : 1);
     });
     if (init_err != cudaSuccess || grid <= 0) return PA_ERR_CUDA;
-    decode_kernel<D, GPAD><<<grid, NWARPS * 32, C::SMEM, st>>>(tmk, tmv, args);
+    decode_kernel<D, NT><<<grid, NWARPS * 32, C::SMEM, st>>>(tmk, tmv, args);
     return cuda_status(cudaGetLastError());
 }
 
@@ -672,9 +853,10 @@ int launch_decode(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeAr
 
 using namespace pa;
 
-extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_heads, int head_dim, int max_context_len) {
-    if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
-    return ws_layout(num_seqs, num_heads, head_dim, max_context_len).total;
+extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                           int max_context_len) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
+    return ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len).total;
 }
 
 extern "C" int pa_workspace_status(const void *workspace, int *status_out, void *stream) {
@@ -693,7 +875,7 @@ extern "C" int pa_decode(uint16_t *out, const uint16_t *query, const uint16_t *k
                          int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, int max_blocks_per_seq,
                          int max_context_len, float scale, void *workspace, size_t workspace_bytes, void *stream) {
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
-        max_context_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || !std::isfinite(scale))
+        max_context_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || !std::isfinite(scale) || !(scale > 0.f))
         return PA_ERR_INVALID_ARG;
     const int G = num_heads / num_kv_heads;
     if ((head_dim != 64 && head_dim != 128) || (block_size != 8 && block_size != 16 && block_size != 32) || G > 16)
@@ -704,7 +886,7 @@ extern "C" int pa_decode(uint16_t *out, const uint16_t *query, const uint16_t *k
         return PA_ERR_INVALID_ARG;
     const long long rows = (long long)num_blocks * num_kv_heads * block_size;
     if (rows >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
-    const WsLayout L = ws_layout(num_seqs, num_heads, head_dim, max_context_len);
+    const WsLayout L = ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total)
         return PA_ERR_WORKSPACE;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -736,15 +918,15 @@ extern "C" int pa_decode(uint16_t *out, const uint16_t *query, const uint16_t *k
     WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
     int *part_off = reinterpret_cast<int *>(ws + L.part_off);
     int4 *sp_info = reinterpret_cast<int4 *>(ws + L.sp_info);
+    int *grp = L.pmax > 1 ? reinterpret_cast<int *>(ws + L.grp) : nullptr;
     float2 *ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
     float *ws_o = reinterpret_cast<float *>(ws + L.o);
     __half *hout = reinterpret_cast<__half *>(out);
 
     decode_prep_kernel<<<1, PREP_THREADS, 0, st>>>(context_lens, num_seqs, num_heads, head_dim, num_kv_heads,
-                                                   max_context_len, (long long)max_blocks_per_seq * block_size, hdr,
-                                                   part_off, sp_info, hout);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return PA_ERR_CUDA;
+                                                   max_context_len, (long long)max_blocks_per_seq * block_size, L.pt,
+                                                   hdr, part_off, sp_info, grp, hout);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
 
     DecodeArgs args;
     args.out = hout;
@@ -755,29 +937,21 @@ extern "C" int pa_decode(uint16_t *out, const uint16_t *query, const uint16_t *k
     args.G = G;
     args.bs = block_size;
     args.mbps = max_blocks_per_seq;
+    args.pt = L.pt;
     args.num_blocks = num_blocks;
     args.scale_log2 = scale * 1.4426950408889634f;
     args.hdr = hdr;
+    args.part_off = part_off;
     args.sp_info = sp_info;
+    args.grp = grp;
     args.ws_ml = ws_ml;
     args.ws_o = ws_o;
     int rc;
     if (head_dim == 128)
-        rc = G <= 8 ? launch_decode<128, 8>(tmk, tmv, args, st) : launch_decode<128, 16>(tmk, tmv, args, st);
+        rc = G <= 8 ? launch_decode<128, 1>(tmk, tmv, args, st) : launch_decode<128, 2>(tmk, tmv, args, st);
     else
-        rc = G <= 8 ? launch_decode<64, 8>(tmk, tmv, args, st) : launch_decode<64, 16>(tmk, tmv, args, st);
+        rc = G <= 8 ? launch_decode<64, 1>(tmk, tmv, args, st) : launch_decode<64, 2>(tmk, tmv, args, st);
     if (rc != PA_OK) return rc;
-
-    if (L.pmax > 1) {
-        const long long rows_out = (long long)num_seqs * num_heads;
-        const int per_cta = 8;
-        const unsigned grid = (unsigned)((rows_out + per_cta - 1) / per_cta);
-        if (head_dim == 128)
-            decode_merge_kernel<128><<<grid, 32 * per_cta, 0, st>>>(part_off, ws_ml, ws_o, hout, num_seqs, num_heads);
-        else
-            decode_merge_kernel<64><<<grid, 32 * per_cta, 0, st>>>(part_off, ws_ml, ws_o, hout, num_seqs, num_heads);
-        if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-    }
     return PA_OK;
 }
 
@@ -817,8 +991,10 @@ extern "C" int pa_decode_static_ws(uint16_t *out, const uint16_t *query, const u
                                    const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
                                    int head_dim, int block_size, int64_t num_blocks, int max_blocks_per_seq,
                                    int max_context_len, float scale, void *stream) {
-    if (num_seqs < 0 || num_heads <= 0 || head_dim <= 0 || max_context_len < 0) return PA_ERR_INVALID_ARG;
-    if (ws_layout(num_seqs, num_heads, head_dim, max_context_len).total > (size_t)PA_DECODE_STATIC_WS_BYTES)
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len < 0)
+        return PA_ERR_INVALID_ARG;
+    if (ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len).total >
+        (size_t)PA_DECODE_STATIC_WS_BYTES)
         return PA_ERR_WORKSPACE;
     if (num_seqs == 0) return PA_OK;
     int device = -1;

@@ -111,7 +111,7 @@ class Step:
             "tables": t(self.tables), "lens": t(self.lens),
         }
         d["out"] = torch.full_like(d["q"], float("nan"))
-        nws = pa.pa_decode_workspace_size(self.w.num_seqs, self.w.num_heads, self.w.head_dim,
+        nws = pa.pa_decode_workspace_size(self.w.num_seqs, self.w.num_heads, self.w.num_kv_heads, self.w.head_dim,
                                           self.w.max_context_len)
         d["ws"] = torch.zeros(nws, dtype=torch.uint8, device=device)
         return d

@@ -37,12 +37,16 @@ def test_status_strings_and_version():
 
 
 def test_workspace_size_is_a_host_bound():
-    small = pa.pa_decode_workspace_size(4, 4, 64, 100)
-    big = pa.pa_decode_workspace_size(100, 64, 128, 8192)
+    small = pa.pa_decode_workspace_size(4, 4, 2, 64, 100)
+    big = pa.pa_decode_workspace_size(100, 64, 8, 128, 8192)
     # header + offsets + item list; partial results only when a sequence can span partitions
     assert 0 < small < 8192
-    assert big >= 100 * 16 * 64 * 128 * 4
-    assert pa.pa_decode_workspace_size(100, 64, 128, 512) < 100 * 64 * 128 * 4
+    # 100 x 8 x 8 partitions of 1024 tokens reach 4096 items: 8 partials per head
+    assert big >= 100 * 8 * 64 * 128 * 4 and big < 100 * 16 * 64 * 128 * 4
+    assert pa.pa_decode_workspace_size(100, 64, 8, 128, 256) < 100 * 64 * 128 * 4
+    # few sequences: shorter partitions (256 tokens) so that the work still spreads
+    assert pa.pa_decode_workspace_size(2, 8, 1, 128, 8192) >= 2 * 32 * 8 * 128 * 4
+    assert pa.lib().pa_decode_workspace_size(1, 8, 0, 128, 10) == 0
 
 
 def test_host_checks_fail_before_any_launch():
@@ -62,3 +66,4 @@ def test_host_checks_fail_before_any_launch():
     assert L.pa_kv_write(nul, nul, nul, nul, nul, 0, 8, 128, 16, 10, nul) == pa.PA_OK
     assert L.pa_block_copy(nul, nul, nul, 0, 8, 128, 16, 10, nul) == pa.PA_OK
     assert L.pa_decode(nul, nul, nul, nul, nul, nul, 0, 8, 1, 128, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_OK
+    assert L.pa_decode(nul, nul, nul, nul, nul, nul, 1, 8, 1, 128, 16, 10, 1, 16, -0.1, nul, 0, nul) == pa.PA_ERR_INVALID_ARG

@@ -208,3 +208,18 @@ def test_streams_are_respected():
     s.synchronize()
     kc, vc = st.oracle_caches()
     compare(to_np(d["out"]), st.oracle_out(kc, vc))
+
+
+@pytest.mark.parametrize("B,H,Hkv,max_ctx,pt", [(4, 8, 2, 3000, 256), (32, 16, 16, 4000, 512), (25, 16, 8, 21000, 1024)])
+def test_partition_sizes(B, H, Hkv, max_ctx, pt):
+    """The partition size follows the shapes (256, 512 or 1024 tokens); each is
+    checked against the oracle on ragged lengths."""
+    rng = np.random.default_rng(B + max_ctx)
+    lens = rng.integers(1, max_ctx, size=B, endpoint=True)
+    lens[0] = max_ctx
+    w = workloads.custom(seed=B + H, num_seqs=B, num_heads=H, num_kv_heads=Hkv, head_dim=128, block_size=16,
+                         context_lens=lens)
+    # the size the library picks: largest of 1024/512/256 reaching 4096 estimated items
+    picked = next((p for p in (1024, 512) if B * Hkv * -(-max_ctx // p) >= 4096), 256)
+    assert picked == pt
+    run_step(w)

@@ -52,7 +52,7 @@ def test_too_large_is_refused():
                          context_lens=[40, 40])
     st = Step(w)
     d = st.upload(torch)
-    need = pa.pa_decode_workspace_size(4096, 64, 128, 32768)
+    need = pa.pa_decode_workspace_size(4096, 64, 8, 128, 32768)
     assert need > pa.PA_DECODE_STATIC_WS_BYTES
     big_q = torch.zeros((4096, 64, 128), dtype=torch.float16, device="cuda")
     big_t = torch.zeros((4096, 1), dtype=torch.int32, device="cuda")
