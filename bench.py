@@ -58,6 +58,23 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def max_over_ranks(ms: float, device=None) -> float:
+    """The largest of every rank's timing (ranks run independent replicas, so
+    the job takes as long as the slowest one); the value itself when alone."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(ms)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tokens_per_s(world: int, seqs: int, steps: int, max_ms: float) -> float:
+    """Whole-job decode throughput: every rank decodes `seqs` sequences per step."""
+    return world * seqs * steps / (max_ms / 1e3)
+
+
 def decode_bytes(w) -> int:
     """Algorithmic bytes of one decode over the workload: every context token's
     K and V rows, the query, the output, the block-table entries the contexts
@@ -72,6 +89,21 @@ def decode_bytes(w) -> int:
 def kv_write_bytes(w) -> int:
     T = w.num_new_tokens
     return 2 * (2 * T * w.num_kv_heads * w.head_dim * 2) + 8 * T
+
+
+def kernel_traffic():
+    """DRAM bytes per full decode launch from the committed ncu capture, or None
+    when the decode kernel's source has changed since the capture was taken."""
+    import hashlib
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "decode_kernel_traffic.json")))
+        src = b"".join(open(os.path.join(ROOT, "paged_kv_cache_12_gb300", "csrc", f), "rb").read()
+                       for f in ("decode.cu", "common.cuh"))
+        if hashlib.sha256(src).hexdigest() == rec["source_sha256"]:
+            return int(rec["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
 
 
 def measured_peaks():
@@ -134,37 +166,38 @@ class ClockSampler:
 
 # --------------------------------------------------------------- oracle timing
 
-def oracle_sample_rate(w, target_s=10.0):
-    """Time the oracle (as it stands) on a bounded sample of the workload:
-    n sequences of the same shape and length, one layer, on all host cores.
-    Returns (tokens/s for the 80-layer step, seconds, n, threads)."""
-    import oracle
-    from paged_kv_cache_12_gb300 import workloads as W
+class OracleSample:
+    """The oracle (as it stands, never tuned) on a bounded sample of the same
+    workload: the first n of its sequences, one layer, on all host cores.
+    n is calibrated once so that one timed call takes about `target_s`."""
 
-    threads = oracle.default_threads()
+    def __init__(self, w, tables, lens, target_s):
+        import oracle
+        self.oracle, self.w, self.tables, self.lens = oracle, w, tables, lens
+        self.threads = oracle.default_threads()
+        n = min(self.threads, w.num_seqs)
+        t = self.run(n)
+        if t < target_s / 2 and n < w.num_seqs:
+            n = min(w.num_seqs, int(n * target_s / max(t, 1e-3)))
+            if n >= self.threads:
+                n = (n // self.threads) * self.threads
+        self.n = max(1, n)
 
-    def run(n):
-        s = W.custom(name="oracle-sample", seed=w.seed, num_seqs=n, num_heads=w.num_heads,
-                     num_kv_heads=w.num_kv_heads, head_dim=w.head_dim, block_size=w.block_size,
-                     context_lens=[int(w.context_lens[0])] * n, permute=True)
-        al = oracle.OracleAllocator(s.num_blocks, s.block_size, free_order=s.free_order)
-        ids = list(range(n))
-        for i in ids:
-            al.add_seq(i)
-        al.append_batch(ids, [int(x) for x in s.context_lens])
-        tab, lens = al.tables(ids, s.max_blocks_per_seq)
-        k, v, q = s.k_pool, s.v_pool, s.query
+    def run(self, n):
+        w = self.w
         t0 = time.perf_counter()
-        oracle.paged_decode(q, k, v, tab, lens, s.num_kv_heads, s.block_size, s.scale, threads=threads)
+        self.oracle.paged_decode(w.query, w.k_pool, w.v_pool, self.tables, self.lens, w.num_kv_heads,
+                                 w.block_size, w.scale, threads=self.threads, seq_range=(0, n))
         return time.perf_counter() - t0
 
-    n = min(threads, w.num_seqs)
-    t = run(n)
-    if t < target_s / 3 and n < w.num_seqs:
-        n = int(min(w.num_seqs, max(n, n * math.floor(target_s / max(t, 1e-3)))))
-        n = max(threads, (n // threads) * threads) if n >= threads else n
-        t = run(n)
-    return n / (t * LAYERS), t, n, threads
+    def rate(self):
+        """(tokens/s for the 80-layer step, seconds of this call)"""
+        secs = self.run(self.n)
+        return self.n / (secs * LAYERS), secs
+
+    def describe(self, secs):
+        return (f"{self.n} of {self.w.num_seqs} sequences x {int(self.w.context_lens[0])} tokens, "
+                f"1 of {LAYERS} layers ({secs:.1f} s per call), scaled to the {LAYERS}-layer step")
 
 
 # ------------------------------------------------------------------ our arm
@@ -209,7 +242,6 @@ def run_ours(args):
     # ---- device-resident inputs
     k = torch.from_numpy(w.k_pool).to(dev)
     v = torch.from_numpy(w.v_pool).to(dev)
-    w.drop_arrays()
     q = torch.from_numpy(w.query).to(dev)
     nk = torch.from_numpy(w.new_key).to(dev)
     nv = torch.from_numpy(w.new_value).to(dev)
@@ -252,12 +284,8 @@ def run_ours(args):
         stop.record(stream)
         barrier()
     assert pa.pa_workspace_status(ws) == pa.PA_OK
-    total_ms = start.elapsed_time(stop)
+    total_ms = max_over_ranks(start.elapsed_time(stop), dev)
     dec_ms = [a.elapsed_time(b) for a, b in ev]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
 
     # ---- end to end through the public API with pinned host buffers
     h_tables = torch.from_numpy(tables).pin_memory()
@@ -289,11 +317,7 @@ def run_ours(args):
         e2e_step()
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     h2d = h_tables.numel() * 4 + h_lens.numel() * 4 + h_slots.numel() * 8 + layers * (
         h_q.numel() * 2 + h_nk.numel() * 2 + h_nv.numel() * 2)
     d2h = layers * out.numel() * 2
@@ -306,7 +330,7 @@ def run_ours(args):
 
     # ---- numbers
     B = w.num_seqs
-    tok_s = world * B * args.steps / (total_ms / 1e3)
+    tok_s = job_tokens_per_s(world, B, args.steps, total_ms)
     dbytes = decode_bytes(w)
     step_bytes = layers * (dbytes + kv_write_bytes(w))
     kv_gbs = world * step_bytes * args.steps / (total_ms / 1e3) / 1e9
@@ -342,21 +366,22 @@ def run_ours(args):
         "roofline": {
             "kernel": "pa_decode (prep + partition + log-sum-exp merge launches)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": None,
+            "frac": round(achieved / peak, 4),
+            "traffic": kernel_traffic() if (args.seqs is None and w.num_seqs == 100) else None,
             "algorithmic_bytes_per_launch": dbytes,
             "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback 6.8 TB/s (of fallback)",
         },
-        "e2e": {"value": round(world * B * args.steps / (e2e_ms / 1e3), 2), "unit": "tokens/s",
+        "e2e": {"value": round(job_tokens_per_s(world, B, args.steps, e2e_ms), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": args.steps * layers * (1 + 3),
         "alloc_us_per_step": round(alloc_us, 1),
         "clocks": clk.summary(),
     }
     if not args.no_cpu_baseline and world == 1:
-        rate, secs, n, threads = oracle_sample_rate(w)
-        line["cpu_baseline"] = {"value": round(rate, 6), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                                "sample": f"{n} of {B} sequences x 8192 tokens, 1 of {layers} layers "
-                                          f"({secs:.1f} s), scaled to the {layers}-layer step"}
+        smp = OracleSample(w, tables, lens, target_s=10.0)
+        rate, secs = smp.rate()
+        line["cpu_baseline"] = {"value": round(rate, 6), "unit": "tokens/s", "cores": smp.threads, "kind": "oracle",
+                                "sample": smp.describe(secs)}
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.barrier()
@@ -367,20 +392,26 @@ def run_ours(args):
 
 def run_reference(args):
     """The oracle, as it stands, on the host cores: same workload, metric and
-    unit; each step is a bounded sample (a few sequences, one layer) scaled to
-    the 80-layer step."""
+    unit; each step times one bounded sample (the first n sequences, one
+    layer, about two seconds) and scales it to the 80-layer step."""
     rank, _, world = dist_env()
     if rank != 0:
         return
+    import oracle
     from paged_kv_cache_12_gb300 import workloads
     w = workloads.make(WORKLOAD)
-    rates, secs_all = [], []
-    n = threads = 0
+    al = oracle.OracleAllocator(w.num_blocks, w.block_size, free_order=w.free_order)
+    ids = list(range(w.num_seqs))
+    for i in ids:
+        al.add_seq(i)
+    al.append_batch(ids, [int(x) for x in w.context_lens])
+    tables, lens = al.tables(ids, w.max_blocks_per_seq)
+    smp = OracleSample(w, tables, lens, target_s=2.0)
+    rates, secs = [], 0.0
     for i in range(args.warmup + args.steps):
-        rate, secs, n, threads = oracle_sample_rate(w, target_s=2.0)
+        rate, secs = smp.rate()
         if i >= args.warmup:
             rates.append(rate)
-            secs_all.append(secs)
     value = statistics.mean(rates)
     line = {
         "impl": "reference",
@@ -388,9 +419,10 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(1e3 * w.num_seqs / value, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{WORKLOAD}: GQA 72B-shaped decode, {w.num_seqs} sequences x 8192-token context, "
-                               f"64 query / 8 KV heads, head_dim 128, block 16, {LAYERS} layers per step"},
-        "cpu_baseline": {"value": round(value, 6), "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": f"{n} sequences x 8192 tokens x 1 layer per step, scaled to {LAYERS} layers"},
+                               f"64 query / 8 KV heads, head_dim 128, block 16, {LAYERS} layers per step",
+                   "num_seqs": w.num_seqs, "context_len": int(w.context_lens[0]), "layers": LAYERS},
+        "cpu_baseline": {"value": round(value, 6), "unit": "tokens/s", "cores": smp.threads, "kind": "oracle",
+                         "sample": smp.describe(secs)},
         "e2e": {"value": round(value, 6), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
