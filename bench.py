@@ -47,7 +47,8 @@ def parse():
     p.add_argument("--steps", type=int, default=30)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--layers", type=int, default=LAYERS)
+    p.add_argument("--layers", type=int, default=None, help="default: 80 for gqa72b, 1 for the others")
+    p.add_argument("--workload", default=WORKLOAD, help="gqa72b (the headline), mha7b, mix, cow16, cow32, tiny")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--seqs", type=int, default=None,
                    help="same shape with fewer sequences (small cases for profiling); default: the full 100")
@@ -204,19 +205,69 @@ class OracleSample:
 
 def workload(args):
     from paged_kv_cache_12_gb300 import workloads
-    w = workloads.make(WORKLOAD)
+    w = workloads.make(args.workload)
     if args.seqs is None or args.seqs == w.num_seqs:
         return w
-    return workloads.custom(name=f"{WORKLOAD}-{args.seqs}seqs", seed=w.seed, num_seqs=args.seqs,
+    if w.num_prompts:
+        raise SystemExit("--seqs applies to the single-context workloads only")
+    return workloads.custom(name=f"{w.name}-{args.seqs}seqs", seed=w.seed, num_seqs=args.seqs,
                             num_heads=w.num_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
-                            block_size=w.block_size, context_lens=[int(w.context_lens[0])] * args.seqs)
+                            block_size=w.block_size, context_lens=list(w.context_lens[: args.seqs])
+                            if args.seqs <= w.num_seqs else [int(w.context_lens[0])] * args.seqs)
+
+
+def allocate(w, pa):
+    """Run the workload's history through the host allocator (parallel-sampling
+    workloads: one prompt per group, forked to its samples, the parent
+    released), then this step's appends.  Returns the allocator, the step's
+    slot mapping and copy pairs, block tables, lengths and the step's
+    allocation time in microseconds."""
+    al = pa.Allocator(w.num_blocks, w.block_size, free_order=w.free_order)
+    ids = list(range(w.num_seqs))
+    if w.num_prompts:
+        for p in range(w.num_prompts):
+            parent = 1_000_000 + p
+            al.add_seq(parent)
+            al.append([parent], [w.prompt_len])
+            for k in range(w.samples_per_prompt):
+                al.fork(parent, p * w.samples_per_prompt + k)
+            al.free_seq(parent)
+    else:
+        for s in ids:
+            al.add_seq(s)
+        al.append(ids, w.history_lens)
+    t0 = time.perf_counter()
+    slots, pairs = al.append(ids, w.new_counts)
+    alloc_us = (time.perf_counter() - t0) * 1e6
+    tables, lens = al.block_tables(ids, w.max_blocks_per_seq)
+    return al, slots, pairs.reshape(-1, 2), tables, lens, alloc_us
+
+
+def unique_kv_bytes(w, tables, lens) -> int:
+    """K/V bytes of the distinct cache slots the decode reads (shared prompt
+    blocks counted once)."""
+    bs = w.block_size
+    slots = []
+    for i in range(w.num_seqs):
+        t = np.arange(int(lens[i]))
+        slots.append(tables[i][t // bs].astype(np.int64) * bs + t % bs)
+    n = len(np.unique(np.concatenate(slots))) if slots else 0
+    return n * 2 * w.num_kv_heads * w.head_dim * 2
+
+
+def describe(w, layers):
+    L = w.context_lens
+    ctx = f"{int(L[0])}-token context" if (L == L[0]).all() else f"context {int(L.min())}..{int(L.max())} tokens"
+    extra = (f", {w.num_prompts} prompts x {w.samples_per_prompt} samples sharing a {w.prompt_len}-token prompt"
+             if w.num_prompts else "")
+    return (f"{w.name}: {w.num_seqs} sequences, {ctx}{extra}, {w.num_heads} query / {w.num_kv_heads} KV heads, "
+            f"head_dim {w.head_dim}, block {w.block_size}, {layers} layer(s) per step sharing one layer's cache")
 
 
 def run_ours(args):
     import torch
 
     import paged_kv_cache_12_gb300 as pa
-    from paged_kv_cache_12_gb300 import workloads
 
     rank, local_rank, world = dist_env()
     if world > 1:
@@ -225,19 +276,11 @@ def run_ours(args):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = workload(args)
-    layers = args.layers
+    layers = args.layers if args.layers is not None else (LAYERS if w.name == WORKLOAD else 1)
 
-    # ---- allocation (host): history, then this step's token for every sequence
-    al = pa.Allocator(w.num_blocks, w.block_size, free_order=w.free_order)
-    ids = list(range(w.num_seqs))
-    for s in ids:
-        al.add_seq(s)
-    al.append(ids, w.history_lens)
-    t_alloc = time.perf_counter()
-    slots, pairs = al.append(ids, w.new_counts)
-    alloc_us = (time.perf_counter() - t_alloc) * 1e6
-    assert len(pairs) == 0
-    tables, lens = al.block_tables(ids, w.max_blocks_per_seq)
+    # ---- allocation (host) for this step
+    al, slots, pairs, tables, lens, alloc_us = allocate(w, pa)
+    has_pairs = len(pairs) > 0
 
     # ---- device-resident inputs
     k = torch.from_numpy(w.k_pool).to(dev)
@@ -246,15 +289,20 @@ def run_ours(args):
     nk = torch.from_numpy(w.new_key).to(dev)
     nv = torch.from_numpy(w.new_value).to(dev)
     d_slots = torch.from_numpy(slots).to(dev)
+    d_pairs = torch.from_numpy(np.ascontiguousarray(pairs)).to(dev)
     d_tables = torch.from_numpy(tables).to(dev)
     d_lens = torch.from_numpy(lens).to(dev)
     out = torch.empty_like(q)
-    ws = torch.zeros(pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.max_context_len),
-                     dtype=torch.uint8, device=dev)
+    ws = torch.zeros(pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                                 w.max_context_len), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def layer():
+    def writes():
+        if has_pairs:
+            pa.pa_block_copy(k, v, d_pairs, stream)
         pa.pa_kv_write(nk, nv, d_slots, k, v, stream)
+
+    def decode():
         pa.pa_decode(out, q, k, v, d_tables, d_lens, w.scale, w.max_context_len, ws, stream)
 
     def barrier():
@@ -265,7 +313,8 @@ def run_ours(args):
     # ---- device-resident timing, with per-decode events for the roofline
     for _ in range(args.warmup):
         for _ in range(layers):
-            layer()
+            writes()
+            decode()
     barrier()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps * layers)]
@@ -276,9 +325,9 @@ def run_ours(args):
         i = 0
         for _ in range(args.steps):
             for _ in range(layers):
-                pa.pa_kv_write(nk, nv, d_slots, k, v, stream)
+                writes()
                 ev[i][0].record(stream)
-                pa.pa_decode(out, q, k, v, d_tables, d_lens, w.scale, w.max_context_len, ws, stream)
+                decode()
                 ev[i][1].record(stream)
                 i += 1
         stop.record(stream)
@@ -291,21 +340,24 @@ def run_ours(args):
     h_tables = torch.from_numpy(tables).pin_memory()
     h_lens = torch.from_numpy(lens).pin_memory()
     h_slots = torch.from_numpy(slots).pin_memory()
-    h_q = torch.from_numpy(np.ascontiguousarray(q.cpu().numpy())).pin_memory()
-    h_nk = nk.cpu().pin_memory()
-    h_nv = nv.cpu().pin_memory()
+    h_pairs = torch.from_numpy(np.ascontiguousarray(pairs)).pin_memory()
+    h_q = torch.from_numpy(np.ascontiguousarray(w.query)).pin_memory()
+    h_nk = torch.from_numpy(np.ascontiguousarray(w.new_key)).pin_memory()
+    h_nv = torch.from_numpy(np.ascontiguousarray(w.new_value)).pin_memory()
     h_out = torch.empty((layers,) + tuple(out.shape), dtype=out.dtype).pin_memory()
 
     def e2e_step():
         d_tables.copy_(h_tables, non_blocking=True)
         d_lens.copy_(h_lens, non_blocking=True)
         d_slots.copy_(h_slots, non_blocking=True)
+        if has_pairs:
+            d_pairs.copy_(h_pairs, non_blocking=True)
         for l in range(layers):
             q.copy_(h_q, non_blocking=True)
             nk.copy_(h_nk, non_blocking=True)
             nv.copy_(h_nv, non_blocking=True)
-            pa.pa_kv_write(nk, nv, d_slots, k, v, stream)
-            pa.pa_decode(out, q, k, v, d_tables, d_lens, w.scale, w.max_context_len, ws, stream)
+            writes()
+            decode()
             h_out[l].copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -318,8 +370,8 @@ def run_ours(args):
     e1.record(stream)
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
-    h2d = h_tables.numel() * 4 + h_lens.numel() * 4 + h_slots.numel() * 8 + layers * (
-        h_q.numel() * 2 + h_nk.numel() * 2 + h_nv.numel() * 2)
+    h2d = h_tables.numel() * 4 + h_lens.numel() * 4 + h_slots.numel() * 8 + (h_pairs.numel() * 8 if has_pairs else 0) \
+        + layers * (h_q.numel() * 2 + h_nk.numel() * 2 + h_nv.numel() * 2)
     d2h = layers * out.numel() * 2
 
     if rank != 0:
@@ -332,12 +384,14 @@ def run_ours(args):
     B = w.num_seqs
     tok_s = job_tokens_per_s(world, B, args.steps, total_ms)
     dbytes = decode_bytes(w)
-    step_bytes = layers * (dbytes + kv_write_bytes(w))
+    step_bytes = layers * (dbytes + kv_write_bytes(w) + (2 * len(pairs) * w.num_kv_heads * w.block_size *
+                                                        w.head_dim * 2 * 2))
     kv_gbs = world * step_bytes * args.steps / (total_ms / 1e3) / 1e9
     dec_avg_ms = statistics.mean(dec_ms)
     achieved = dbytes / (dec_avg_ms / 1e3) / 1e9
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks else 6800.0
+    headline = w.name == WORKLOAD and args.seqs is None
     line = {
         "metric": METRIC,
         "value": round(tok_s, 2),
@@ -352,32 +406,35 @@ def run_ours(args):
         "dtype": "f16",
         "data": "synthetic",
         "config": {
-            "workload": f"{w.name}: GQA 72B-shaped decode, {B} sequences x 8192-token context, "
-                        f"{w.num_heads} query / {w.num_kv_heads} KV heads, head_dim {w.head_dim}, block {w.block_size}, "
-                        f"{layers} layers per step sharing one layer's cache",
-            "num_seqs": B, "context_len": int(w.context_lens[0]), "num_heads": w.num_heads,
+            "workload": describe(w, layers),
+            "num_seqs": B, "context_len_max": int(w.context_lens.max()), "num_heads": w.num_heads,
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
             "layers": layers, "parallelism": f"replicas x{world}",
-            "l2": "inputs 3.36 GB per layer >> 129 MB L2; no flush",
+            "l2": f"K/V read per layer {dbytes / 1e9:.2f} GB vs 129 MB L2; no flush",
         },
         "kv_gbs": round(kv_gbs, 1),
         "decode_ms": {"mean": round(dec_avg_ms, 5), "p10": round(float(np.percentile(dec_ms, 10)), 5),
                       "p90": round(float(np.percentile(dec_ms, 90)), 5)},
         "roofline": {
-            "kernel": "pa_decode (prep + partition + log-sum-exp merge launches)",
+            "kernel": "pa_decode (prep + persistent partition kernel with fused log-sum-exp merge)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
-            "traffic": kernel_traffic() if (args.seqs is None and w.num_seqs == 100) else None,
+            "traffic": kernel_traffic() if headline else None,
             "algorithmic_bytes_per_launch": dbytes,
             "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback 6.8 TB/s (of fallback)",
         },
         "e2e": {"value": round(job_tokens_per_s(world, B, args.steps, e2e_ms), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": args.steps * layers * (1 + 3),
+        "gpu_launches": args.steps * layers * (3 + (1 if has_pairs else 0)),
         "alloc_us_per_step": round(alloc_us, 1),
         "clocks": clk.summary(),
     }
-    if not args.no_cpu_baseline and world == 1:
+    if w.num_prompts:
+        ub = unique_kv_bytes(w, tables, lens)
+        line["roofline"]["unique_kv_bytes_per_launch"] = ub
+        line["roofline"]["achieved_unique"] = round(ub / (dec_avg_ms / 1e3) / 1e9, 1)
+        line["copy_pairs"] = int(len(pairs))
+    if not args.no_cpu_baseline and world == 1 and not w.num_prompts:
         smp = OracleSample(w, tables, lens, target_s=10.0)
         rate, secs = smp.rate()
         line["cpu_baseline"] = {"value": round(rate, 6), "unit": "tokens/s", "cores": smp.threads, "kind": "oracle",

@@ -159,19 +159,57 @@ __host__ __device__ constexpr int swz(int row, int col) {
 
 // -------------------------------------------------------------- prep
 
+// Block-wide exclusive scan of one int per thread (PREP_THREADS threads);
+// returns the thread's exclusive prefix and writes the block total to *total.
+__device__ __forceinline__ int block_exclusive_scan(int x, int *warp_sums, int *total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int inc = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) warp_sums[wid] = inc;
+    __syncthreads();
+    if (wid == 0) {
+        int s = warp_sums[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        warp_sums[lane] = s;
+    }
+    __syncthreads();
+    const int excl = (wid ? warp_sums[wid - 1] : 0) + inc - x;
+    *total = warp_sums[PREP_THREADS / 32 - 1];
+    __syncthreads();
+    return excl;
+}
+
+// Work list, longest first: every sequence's partitions but its last are
+// full (pt tokens) and come first, in sequence order; the last partitions
+// follow in decreasing length (a counting sort on 16-token buckets), so
+// that the dynamically scheduled tail of the kernel runs the shortest items.
+// An item record is {seq, partition, L, canonical index}; partial results
+// are stored at the canonical index part_off[seq] + partition, independent
+// of the order.
 __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
     const int32_t *__restrict__ context_lens, int B, int Hq, int D, int Hkv, int max_ctx, long long max_table_tokens,
     int pt, WsHeader *hdr, int *part_off, int4 *sp_info, int *grp, __half *out) {
+    constexpr int NBK = MAX_PART_TOKENS / CHUNK;     // length buckets of the last partitions
     __shared__ int warp_sums[PREP_THREADS / 32];
-    __shared__ int running;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    if (threadIdx.x == 0) running = 0;
+    __shared__ int hist[NBK], cursor[NBK];
+    int run_p = 0, run_f = 0;                        // uniform running totals
+    for (int k = threadIdx.x; k < NBK; k += PREP_THREADS) hist[k] = cursor[k] = 0;
     if (grp)
         for (long long k = threadIdx.x; k < (long long)B * Hkv; k += PREP_THREADS) grp[k] = 0;
     __syncthreads();
+    const int nbk = pt / CHUNK;
+    // pass 1: partition counts, canonical offsets, full items, bucket histogram
     for (int base = 0; base < B; base += PREP_THREADS) {
         const int i = base + threadIdx.x;
-        int L = 0, P = 0, code = 0;   // code 1: zero row, 2: NaN row
+        int L = 0, P = 0, code = 0;                  // code 1: zero row, 2: NaN row
         if (i < B) {
             L = context_lens[i];
             if (L < 0 || L > max_ctx || (long long)L > max_table_tokens)
@@ -181,28 +219,13 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
             else
                 P = (L + pt - 1) / pt;
         }
-        int x = P;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-        }
-        if (lane == 31) warp_sums[wid] = x;
-        __syncthreads();
-        if (wid == 0) {
-            int s = warp_sums[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(0xffffffffu, s, o);
-                if (lane >= o) s += y;
-            }
-            warp_sums[lane] = s;
-        }
-        __syncthreads();
-        const int excl = running + (wid ? warp_sums[wid - 1] : 0) + x - P;
+        int tp, tf;
+        const int ep = run_p + block_exclusive_scan(P, warp_sums, &tp);
+        const int ef = run_f + block_exclusive_scan(P > 0 ? P - 1 : 0, warp_sums, &tf);
         if (i < B) {
-            part_off[i] = excl;
-            for (int p = 0; p < P; ++p) sp_info[excl + p] = make_int4(i, p, L, P);
+            part_off[i] = ep;
+            for (int p = 0; p + 1 < P; ++p) sp_info[ef + p] = make_int4(i, p, L, ep + p);
+            if (P > 0) atomicAdd(&hist[(pt - (L - (P - 1) * pt)) / CHUNK], 1);
             if (code) {
                 const uint32_t h = code == 1 ? 0u : 0x7e007e00u;
                 uint4 fill = make_uint4(h, h, h, h);
@@ -210,13 +233,30 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
                 for (int k = 0; k < Hq * D / 8; ++k) row[k] = fill;
             }
         }
-        __syncthreads();
-        if (threadIdx.x == 0) running += warp_sums[PREP_THREADS / 32 - 1];
-        __syncthreads();
+        run_p += tp;
+        run_f += tf;
+    }
+    __syncthreads();
+    // bucket starts, largest last partitions first
+    if (threadIdx.x == 0) {
+        int acc = run_f;
+        for (int k = 0; k < nbk; ++k) {
+            cursor[k] = acc;
+            acc += hist[k];
+        }
+    }
+    __syncthreads();
+    // pass 2: place the last partitions
+    for (int i = threadIdx.x; i < B; i += PREP_THREADS) {
+        const int L = context_lens[i];
+        if (L <= 0 || L > max_ctx || (long long)L > max_table_tokens) continue;
+        const int P = (L + pt - 1) / pt;
+        const int slot = atomicAdd(&cursor[(pt - (L - (P - 1) * pt)) / CHUNK], 1);
+        sp_info[slot] = make_int4(i, P - 1, L, part_off[i] + P - 1);
     }
     if (threadIdx.x == 0) {
-        part_off[B] = running;
-        hdr->total_items = running * Hkv;
+        part_off[B] = run_p;
+        hdr->total_items = run_p * Hkv;
         hdr->counter = 0;
         hdr->error = 0;
     }
@@ -262,7 +302,7 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
     int raw = 0;
     int nn_item = -1;
     int4 nn_inf = make_int4(0, 0, 0, 0);
-    int n_item = -1, n_seq = 0, n_p = 0, n_L = 0, n_P = 0, n_fb = 0;
+    int n_item = -1, n_seq = 0, n_p = 0, n_L = 0, n_P = 0, n_fb = 0, n_canon = 0;
     int n_e[ENTRIES];
 #pragma unroll
     for (int e = 0; e < ENTRIES; ++e) n_e[e] = 0;
@@ -272,7 +312,8 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
             n_seq = nn_inf.x;
             n_p = nn_inf.y;
             n_L = nn_inf.z;
-            n_P = nn_inf.w;
+            n_canon = nn_inf.w;
+            n_P = (n_L + a.pt - 1) / a.pt;
             const int t0 = n_p * a.pt;
             const int t1 = min(n_L, t0 + a.pt);
             n_fb = t0 / a.bs;
@@ -344,7 +385,7 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
                         ItemDesc d;
                         d.seq = n_seq;
                         d.kvh = kvh;
-                        d.sp = sp;
+                        d.sp = n_canon;
                         d.P = n_P;
                         d.nchunks = nch[c];
                         d.ntok_last = t1[c] - (t0[c] + (nch[c] - 1) * CHUNK);
@@ -528,8 +569,25 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
     }
     const float sl2 = a.scale_log2;
 
-    // a group ticket taken at the end of the previous multi-partition item
+    // Merge tickets.  After an item of a multi-partition sequence has stored
+    // its partial, it owes a ticket for its (sequence, kv head) group: the
+    // ticket is taken after the next item's first chunk (by then the partial's
+    // stores have drained, so the fence is cheap) and inspected at that item's
+    // end (so the atomic's latency is hidden); the warp holding the group's
+    // last ticket merges the group then.
+    bool owe = false;
+    int owe_seq = 0, owe_kvh = 0, owe_P = 0;
     int pend_ticket = 0, pend_seq = 0, pend_kvh = 0, pend_P = 0;
+    auto take_ticket = [&]() {
+        __syncwarp();
+        __threadfence();
+        pend_ticket = 0;
+        if (lane == 0) pend_ticket = atomicAdd(&a.grp[owe_seq * a.Hkv + owe_kvh], 1);
+        pend_seq = owe_seq;
+        pend_kvh = owe_kvh;
+        pend_P = owe_P;
+        owe = false;
+    };
     auto settle = [&]() {
         const int t = __shfl_sync(0xffffffffu, pend_ticket, 0);
         if (pend_P > 0 && t == pend_P - 1) {
@@ -549,6 +607,7 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
         }
         const ItemDesc dsc = cs.desc[q];
         if (dsc.end) {
+            if (owe) take_ticket();
             settle();
             return;
         }
@@ -683,6 +742,7 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&cs.empty[s]));   // stage free for the next copy
             ++stage;
+            if (ch == 0 && owe) take_ticket();
         }
 
         // ---- item complete: row sums over the 8 token lanes, then write out
@@ -731,19 +791,13 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                     }
                 }
         }
-        // a merge owed from the previous multi-partition item (its ticket has
-        // had a whole item's time to come back)
+        // the ticket taken during this item: merge its group if it was the last
         settle();
         if (dsc.P > 1) {
-            // take a ticket for the group; the warp that takes the last one
-            // merges the group, after its next item
-            __threadfence();
-            __syncwarp();
-            pend_ticket = 0;
-            if (lane == 0) pend_ticket = atomicAdd(&a.grp[dsc.seq * a.Hkv + dsc.kvh], 1);
-            pend_seq = dsc.seq;
-            pend_kvh = dsc.kvh;
-            pend_P = dsc.P;
+            owe = true;
+            owe_seq = dsc.seq;
+            owe_kvh = dsc.kvh;
+            owe_P = dsc.P;
         }
     }
 }
@@ -827,7 +881,8 @@ bool cache_tensor_map(CUtensorMap *map, const void *base, long long rows, int D,
 }
 
 template <int D, int NT>
-int launch_decode(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeArgs &args, cudaStream_t st) {
+int launch_decode(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeArgs &args, long long max_items,
+                  cudaStream_t st) {
     using C = Cfg<D, NT>;
     static int grid = 0;
     static std::once_flag once;
@@ -844,7 +899,10 @@ int launch_decode(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeAr
         if (init_err == cudaSuccess) grid = sms * (per_sm > 0 ? per_sm : 1);
     });
     if (init_err != cudaSuccess || grid <= 0) return PA_ERR_CUDA;
-    decode_kernel<D, NT><<<grid, NWARPS * 32, C::SMEM, st>>>(tmk, tmv, args);
+    // no more CTAs than there can be items for their consumers
+    const long long need = (max_items + NC - 1) / NC;
+    const int g = (int)(need < grid ? (need > 0 ? need : 1) : grid);
+    decode_kernel<D, NT><<<g, NWARPS * 32, C::SMEM, st>>>(tmk, tmv, args);
     return cuda_status(cudaGetLastError());
 }
 
@@ -946,11 +1004,14 @@ extern "C" int pa_decode(uint16_t *out, const uint16_t *query, const uint16_t *k
     args.grp = grp;
     args.ws_ml = ws_ml;
     args.ws_o = ws_o;
+    const long long max_items = (long long)num_seqs * num_kv_heads * L.pmax;
     int rc;
     if (head_dim == 128)
-        rc = G <= 8 ? launch_decode<128, 1>(tmk, tmv, args, st) : launch_decode<128, 2>(tmk, tmv, args, st);
+        rc = G <= 8 ? launch_decode<128, 1>(tmk, tmv, args, max_items, st)
+                    : launch_decode<128, 2>(tmk, tmv, args, max_items, st);
     else
-        rc = G <= 8 ? launch_decode<64, 1>(tmk, tmv, args, st) : launch_decode<64, 2>(tmk, tmv, args, st);
+        rc = G <= 8 ? launch_decode<64, 1>(tmk, tmv, args, max_items, st)
+                    : launch_decode<64, 2>(tmk, tmv, args, max_items, st);
     if (rc != PA_OK) return rc;
     return PA_OK;
 }
