@@ -50,6 +50,7 @@ def parse():
     p.add_argument("--layers", type=int, default=None, help="default: 80 for gqa72b, 1 for the others")
     p.add_argument("--workload", default=WORKLOAD, help="gqa72b (the headline), mha7b, mix, cow16, cow32, tiny")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-graph", action="store_true", help="skip the CUDA Graph replay measurement")
     p.add_argument("--seqs", type=int, default=None,
                    help="same shape with fewer sequences (small cases for profiling); default: the full 100")
     return p.parse_args()
@@ -297,13 +298,19 @@ def run_ours(args):
                                                  w.max_context_len), dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def writes():
+    def writes_on(st):
         if has_pairs:
-            pa.pa_block_copy(k, v, d_pairs, stream)
-        pa.pa_kv_write(nk, nv, d_slots, k, v, stream)
+            pa.pa_block_copy(k, v, d_pairs, st)
+        pa.pa_kv_write(nk, nv, d_slots, k, v, st)
+
+    def decode_on(st):
+        pa.pa_decode(out, q, k, v, d_tables, d_lens, w.scale, w.max_context_len, ws, st)
+
+    def writes():
+        writes_on(stream)
 
     def decode():
-        pa.pa_decode(out, q, k, v, d_tables, d_lens, w.scale, w.max_context_len, ws, stream)
+        decode_on(stream)
 
     def barrier():
         if world > 1:
@@ -335,6 +342,30 @@ def run_ours(args):
     assert pa.pa_workspace_status(ws) == pa.PA_OK
     total_ms = max_over_ranks(start.elapsed_time(stop), dev)
     dec_ms = [a.elapsed_time(b) for a, b in ev]
+
+    # ---- the same step captured once in a CUDA Graph and replayed
+    graph_ms = None
+    if not args.no_graph:
+        cs = torch.cuda.Stream()
+        cs.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(cs):
+            with torch.cuda.graph(g, stream=cs):
+                for _ in range(layers):
+                    writes_on(cs)
+                    decode_on(cs)
+        stream.wait_stream(cs)
+        for _ in range(args.warmup):
+            g.replay()
+        barrier()
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        g0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        g1.record(stream)
+        barrier()
+        graph_ms = max_over_ranks(g0.elapsed_time(g1), dev)
+        del g
 
     # ---- end to end through the public API with pinned host buffers
     h_tables = torch.from_numpy(tables).pin_memory()
@@ -425,6 +456,10 @@ def run_ours(args):
         },
         "e2e": {"value": round(job_tokens_per_s(world, B, args.steps, e2e_ms), 2), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "graph": None if graph_ms is None else {
+            "value": round(job_tokens_per_s(world, B, args.steps, graph_ms), 2), "unit": "tokens/s",
+            "ms_per_step": round(graph_ms / args.steps, 4),
+            "note": "the whole step captured once in a CUDA Graph and replayed"},
         "gpu_launches": args.steps * layers * (3 + (1 if has_pairs else 0)),
         "alloc_us_per_step": round(alloc_us, 1),
         "clocks": clk.summary(),
