@@ -260,6 +260,55 @@ PA_API int pa_alloc_seq_len(const pa_allocator *a, int64_t seq_id, int64_t *len_
  * sequence holds more than max_blocks blocks. */
 PA_API int pa_alloc_block_tables(const pa_allocator *a, int num_seqs, const int64_t *seq_ids,
                           int32_t *tables_out, int max_blocks, int32_t *lens_out);
+/* The free queue, head first: *count_out blocks into blocks_out (int32,
+ * capacity entries; PA_ERR_INVALID_ARG if capacity is too small, with
+ * *count_out still set). */
+PA_API int pa_alloc_free_queue(const pa_allocator *a, int32_t *blocks_out, int64_t capacity, int64_t *count_out);
+
+/* ------------------------------------------------------- prefix caching */
+
+/* Prefix caching of full blocks (deepsonar page section 2.4 and section VII
+ * step 5).  Each full block of a sequence whose token ids are known gets the
+ * chained hash SHA-256(parent hash || token ids || extra key), where the
+ * parent hash is the previous block's (32 zero bytes for the first block),
+ * token ids are little-endian int32 and the extra key a little-endian
+ * uint64; the first block registered with a hash is the one the map keeps.
+ * A released block stays in the map while it waits in the free queue; when
+ * it is handed out again from the queue head, its entry is dropped (the
+ * queue order is the eviction order). */
+
+/* Turn prefix caching on; only before any sequence exists. */
+PA_API int pa_alloc_enable_prefix_cache(pa_allocator *a);
+
+/* Start a new sequence seq_id for a prompt of num_tokens token ids: walk the
+ * prompt's full blocks that lie inside its first num_tokens - 1 tokens (the
+ * last prompt token is always computed, so that its logits exist), hash each
+ * in chain, and take every block found in the map, in order, until the first
+ * miss (a hit still in the free queue leaves the queue; its count rises by
+ * one).  *cached_tokens_out = tokens now covered (a multiple of block_size);
+ * the caller appends the rest with pa_alloc_append_ids.  PA_ERR_INVALID_ARG
+ * if prefix caching is off or seq_id exists. */
+PA_API int pa_alloc_match_prefix(pa_allocator *a, int64_t seq_id, const int32_t *tokens, int num_tokens,
+                                 uint64_t extra_key, int *cached_tokens_out);
+
+/* pa_alloc_append with the token ids of the appended tokens (token_ids:
+ * sum(counts) int32, sequence by sequence), so that the blocks they complete
+ * are hashed and cached.  A sequence appended to once without ids is never
+ * hashed again. */
+PA_API int pa_alloc_append_ids(pa_allocator *a, int num_seqs, const int64_t *seq_ids, const int32_t *counts,
+                               const int32_t *token_ids, int64_t *slots_out, int64_t *pairs_out,
+                               int pairs_capacity, int *num_pairs_out);
+
+/* The hash recorded for a block (32 bytes, zeros if none) and whether the
+ * map currently points at this block (*cached_out = 1). */
+PA_API int pa_alloc_block_hash(const pa_allocator *a, int64_t block, uint8_t *hash_out, int *cached_out);
+
+/* Blocks in the hash map, block lookups made by pa_alloc_match_prefix, hits. */
+PA_API int pa_alloc_prefix_stats(const pa_allocator *a, int64_t *cached_blocks, int64_t *queries, int64_t *hits);
+
+/* SHA-256 (FIPS 180-4) of num_bytes bytes: the hash the prefix cache uses. */
+PA_API int pa_sha256(const void *data, size_t num_bytes, uint8_t *digest_out);
+
 /* Reference count of one block (0 if free). */
 PA_API int pa_alloc_refcount(const pa_allocator *a, int64_t block, int32_t *count_out);
 PA_API int pa_alloc_stats(const pa_allocator *a, pa_alloc_stats_t *out);

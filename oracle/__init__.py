@@ -18,6 +18,10 @@ Contents, each with the passage it follows:
   counts with copy-on-write (deepsonar page section 2.3), free queue handing out
   from the head and taking freed blocks back at the tail (deepsonar page
   section 2.4).
+* prefix caching in ``OracleAllocator`` (deepsonar page section 2.4 and
+  section VII step 5): chained block hashes sha256(parent hash, block tokens,
+  extra key), a hash -> block map, the free queue as eviction order, prefix
+  matching block by block with the last prompt token always recomputed.
 * ``kv_write`` / ``block_copy`` -- the new token's K/V go into the free slot of
   the sequence's current block (deeplearn.tn page, same section); a writer that
   finds a shared block copies it first (deepsonar page section 2.3).
@@ -29,10 +33,12 @@ Readings where the pages are silent are listed with each function.
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
+import struct
 import subprocess
 import threading
-from collections import deque
+from collections import OrderedDict
 from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
@@ -98,6 +104,19 @@ class OracleError(Exception):
         self.code = code
 
 
+ZERO_HASH = bytes(32)
+
+
+def block_hash(parent: bytes, tokens, extra_key: int) -> bytes:
+    """Chained block hash: sha256(parent hash || token ids as little-endian
+    int32 || extra key as little-endian uint64); parent = 32 zero bytes for a
+    sequence's first block (deepsonar page section 2.4: hash of the parent
+    block, the block's tokens and an extra key)."""
+    data = parent + struct.pack("<%di" % len(tokens), *[int(t) for t in tokens]) + \
+        struct.pack("<Q", int(extra_key) & (2 ** 64 - 1))
+    return hashlib.sha256(data).digest()
+
+
 class OracleAllocator:
     """Plain Python block allocator.
 
@@ -117,9 +136,16 @@ class OracleAllocator:
       copy, and drops the shared block's count by one (copy-on-write).
     * A call that runs out of blocks raises ``OracleError('OUT_OF_BLOCKS')``
       and leaves the state as it was.
+    * With ``prefix_cache``: a full block whose tokens are known is hashed
+      (``block_hash``, chained from its predecessor) and entered in a map
+      unless the map already has that hash.  Released blocks keep their entry
+      while free; a block taken from the queue head drops it.
+      ``match_prefix`` starts a sequence by taking, in order, the cached
+      blocks of its prompt's full blocks within all but the last token,
+      stopping at the first miss.
     """
 
-    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+    def __init__(self, num_blocks: int, block_size: int, free_order=None, prefix_cache: bool = False):
         if num_blocks <= 0 or block_size <= 0:
             raise OracleError("INVALID_ARG")
         self.num_blocks = int(num_blocks)
@@ -127,15 +153,31 @@ class OracleAllocator:
         order = list(range(num_blocks)) if free_order is None else [int(b) for b in free_order]
         if sorted(order) != list(range(num_blocks)):
             raise OracleError("INVALID_ARG")
-        self.free = deque(order)
+        self.free = OrderedDict((b, None) for b in order)   # head first
         self.ref = [0] * num_blocks
-        self.seqs: dict[int, dict] = {}
+        self.seqs: dict = {}
+        self.prefix_cache = bool(prefix_cache)
+        self.hash_of: dict = {}       # block -> hash recorded for it
+        self.cached: dict = {}        # hash -> block
+        self.queries = 0
+        self.hits = 0
+
+    # -- free queue ---------------------------------------------------------
+    def _pop_free(self):
+        b, _ = self.free.popitem(last=False)
+        h = self.hash_of.pop(b, None)
+        if h is not None and self.cached.get(h) == b:
+            del self.cached[h]
+        return b
 
     # -- sequences --------------------------------------------------------
+    def _new_seq(self):
+        return {"len": 0, "blocks": [], "ids": [], "chain": [], "extra": 0}
+
     def add_seq(self, seq_id: int):
         if seq_id in self.seqs:
             raise OracleError("INVALID_ARG")
-        self.seqs[seq_id] = {"len": 0, "blocks": []}
+        self.seqs[seq_id] = self._new_seq()
 
     def _blocks_needed(self, seq, n):
         bs = self.block_size
@@ -154,10 +196,11 @@ class OracleAllocator:
         those tokens are written."""
         return self.append_batch([seq_id], [n])
 
-    def append_batch(self, seq_ids, counts):
+    def append_batch(self, seq_ids, counts, token_ids=None):
         """Same as append_tokens for several sequences, in the order given.
         All-or-nothing: if the blocks needed by the whole call exceed the free
-        queue, nothing changes."""
+        queue, nothing changes.  ``token_ids`` (concatenated, sequence by
+        sequence) lets completed blocks be hashed when prefix caching is on."""
         if len(seq_ids) != len(counts):
             raise OracleError("INVALID_ARG")
         for s, n in zip(seq_ids, counts):
@@ -170,26 +213,75 @@ class OracleAllocator:
             raise OracleError("OUT_OF_BLOCKS")
         bs = self.block_size
         slots, pairs = [], []
+        w = 0
         for s, n in zip(seq_ids, counts):
             seq = self.seqs[s]
+            if token_ids is None:
+                seq["ids"] = None
             for _ in range(n):
                 t = seq["len"]
                 off = t % bs
                 if off == 0:
-                    b = self.free.popleft()
+                    b = self._pop_free()
                     self.ref[b] = 1
                     seq["blocks"].append(b)
                 else:
                     tail = seq["blocks"][-1]
                     if self.ref[tail] > 1:
-                        nb = self.free.popleft()
+                        nb = self._pop_free()
                         self.ref[nb] = 1
                         self.ref[tail] -= 1
                         seq["blocks"][-1] = nb
                         pairs.append((tail, nb))
                 slots.append(seq["blocks"][t // bs] * bs + off)
+                if token_ids is not None and seq["ids"] is not None:
+                    seq["ids"].append(int(token_ids[w]))
+                w += 1
                 seq["len"] = t + 1
+                self._maybe_hash(seq, t)
         return slots, pairs
+
+    def _maybe_hash(self, seq, t):
+        bs = self.block_size
+        if not self.prefix_cache or seq["ids"] is None or (t + 1) % bs != 0:
+            return
+        j = t // bs
+        if len(seq["chain"]) != j:
+            return
+        parent = seq["chain"][j - 1] if j else ZERO_HASH
+        h = block_hash(parent, seq["ids"][j * bs:(j + 1) * bs], seq["extra"])
+        seq["chain"].append(h)
+        b = seq["blocks"][j]
+        if b not in self.hash_of:
+            self.hash_of[b] = h
+            self.cached.setdefault(h, b)
+
+    def match_prefix(self, seq_id: int, tokens, extra_key: int = 0) -> int:
+        """Start ``seq_id`` on a prompt; returns the tokens covered by cached blocks."""
+        if not self.prefix_cache or seq_id in self.seqs:
+            raise OracleError("INVALID_ARG")
+        bs = self.block_size
+        tokens = [int(x) for x in tokens]
+        seq = self._new_seq()
+        seq["extra"] = int(extra_key)
+        candidates = (len(tokens) - 1) // bs if tokens else 0
+        for j in range(candidates):
+            parent = seq["chain"][j - 1] if j else ZERO_HASH
+            h = block_hash(parent, tokens[j * bs:(j + 1) * bs], extra_key)
+            self.queries += 1
+            if h not in self.cached:
+                break
+            self.hits += 1
+            b = self.cached[h]
+            if b in self.free:
+                del self.free[b]
+            self.ref[b] += 1
+            seq["blocks"].append(b)
+            seq["chain"].append(h)
+            seq["ids"].extend(tokens[j * bs:(j + 1) * bs])
+            seq["len"] += bs
+        self.seqs[seq_id] = seq
+        return seq["len"]
 
     def fork(self, parent: int, child: int):
         if parent not in self.seqs or child in self.seqs:
@@ -197,18 +289,24 @@ class OracleAllocator:
         p = self.seqs[parent]
         for b in p["blocks"]:
             self.ref[b] += 1
-        self.seqs[child] = {"len": p["len"], "blocks": list(p["blocks"])}
+        self.seqs[child] = {"len": p["len"], "blocks": list(p["blocks"]),
+                            "ids": None if p["ids"] is None else list(p["ids"]),
+                            "chain": list(p["chain"]), "extra": p["extra"]}
 
     def free_seq(self, seq_id: int):
         if seq_id not in self.seqs:
             raise OracleError("INVALID_ARG")
-        seq = self.seqs.pop(seq_id)
+        seq = self.seqs[seq_id]
+        uses: dict = {}
         for b in seq["blocks"]:
-            if self.ref[b] <= 0:
+            uses[b] = uses.get(b, 0) + 1
+            if uses[b] > self.ref[b]:
                 raise OracleError("STATE")
+        del self.seqs[seq_id]
+        for b in seq["blocks"]:
             self.ref[b] -= 1
             if self.ref[b] == 0:
-                self.free.append(b)
+                self.free[b] = None
 
     # -- views --------------------------------------------------------------
     def block_table(self, seq_id: int):
@@ -232,6 +330,9 @@ class OracleAllocator:
             "num_seqs": len(self.seqs),
             "logical_tokens": sum(s["len"] for s in self.seqs.values()),
         }
+
+    def prefix_stats(self):
+        return {"cached_blocks": len(self.cached), "queries": self.queries, "hits": self.hits}
 
     def used_slot_mask(self):
         """Boolean [num_blocks, block_size]: True where some sequence holds a

@@ -37,7 +37,8 @@ EXPORTS = (
     "pa_status_string", "pa_version", "pa_kv_write", "pa_block_copy", "pa_decode_workspace_size", "pa_decode",
     "pa_workspace_status", "pa_alloc_create", "pa_alloc_destroy", "pa_alloc_add_seq", "pa_alloc_append",
     "pa_alloc_fork", "pa_alloc_free_seq", "pa_alloc_seq_len", "pa_alloc_block_tables", "pa_alloc_refcount",
-    "pa_alloc_stats", "pa_decode_static_ws",
+    "pa_alloc_stats", "pa_decode_static_ws", "pa_alloc_free_queue", "pa_alloc_enable_prefix_cache",
+    "pa_alloc_match_prefix", "pa_alloc_append_ids", "pa_alloc_block_hash", "pa_alloc_prefix_stats", "pa_sha256",
 )
 
 # bytes of the library's built-in scratch array used by pa_decode_static_ws
@@ -86,6 +87,13 @@ def lib():
             "pa_alloc_stats": ([vp, ctypes.POINTER(AllocStats)], i32),
             "pa_decode_static_ws": ([vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, i32, i32,
                                      ctypes.c_float, vp], i32),
+            "pa_alloc_free_queue": ([vp, vp, i64, ctypes.POINTER(i64)], i32),
+            "pa_alloc_enable_prefix_cache": ([vp], i32),
+            "pa_alloc_match_prefix": ([vp, i64, vp, i32, ctypes.c_uint64, ctypes.POINTER(i32)], i32),
+            "pa_alloc_append_ids": ([vp, i32, vp, vp, vp, vp, vp, i32, ctypes.POINTER(i32)], i32),
+            "pa_alloc_block_hash": ([vp, i64, vp, ctypes.POINTER(i32)], i32),
+            "pa_alloc_prefix_stats": ([vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i64)], i32),
+            "pa_sha256": ([vp, sz, vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -221,16 +229,26 @@ def _i64(a):
     return np.ascontiguousarray(a, dtype=np.int64)
 
 
+def pa_sha256(data: bytes) -> bytes:
+    """SHA-256 of a byte string, as the prefix cache computes it."""
+    out = (ctypes.c_uint8 * 32)()
+    buf = bytes(data)
+    _check(lib().pa_sha256(buf, len(buf), out), "pa_sha256")
+    return bytes(out)
+
+
 class Allocator:
     """Host block allocator (pa_alloc_* calls)."""
 
-    def __init__(self, num_blocks: int, block_size: int, free_order=None):
+    def __init__(self, num_blocks: int, block_size: int, free_order=None, prefix_cache: bool = False):
         self._h = ctypes.c_void_p()
         self.num_blocks, self.block_size = int(num_blocks), int(block_size)
         order = None if free_order is None else np.ascontiguousarray(free_order, dtype=np.int32)
         _check(lib().pa_alloc_create(self.num_blocks, self.block_size,
                                      None if order is None else order.ctypes.data, ctypes.byref(self._h)),
                "pa_alloc_create")
+        if prefix_cache:
+            _check(lib().pa_alloc_enable_prefix_cache(self._h), "pa_alloc_enable_prefix_cache")
 
     def close(self):
         if self._h:
@@ -256,6 +274,47 @@ class Allocator:
         _check(lib().pa_alloc_append(self._h, len(ids), ids.ctypes.data, cnt.ctypes.data, slots.ctypes.data,
                                      pairs.ctypes.data, pairs.shape[0], ctypes.byref(n)), "pa_alloc_append")
         return slots, pairs[: n.value].copy()
+
+    def append_ids(self, seq_ids, counts, token_ids):
+        """append() with the appended tokens' ids (concatenated in sequence order)."""
+        ids = _i64(seq_ids)
+        cnt = np.ascontiguousarray(counts, dtype=np.int32)
+        toks = np.ascontiguousarray(token_ids, dtype=np.int32)
+        slots = np.empty(max(0, int(cnt[cnt > 0].sum())), dtype=np.int64)
+        pairs = np.empty((max(1, len(ids)), 2), dtype=np.int64)
+        n = ctypes.c_int(0)
+        _check(lib().pa_alloc_append_ids(self._h, len(ids), ids.ctypes.data, cnt.ctypes.data, toks.ctypes.data,
+                                         slots.ctypes.data, pairs.ctypes.data, pairs.shape[0], ctypes.byref(n)),
+               "pa_alloc_append_ids")
+        return slots, pairs[: n.value].copy()
+
+    def match_prefix(self, seq_id: int, tokens, extra_key: int = 0) -> int:
+        """Start seq_id on a prompt, reusing cached full blocks; returns the tokens covered."""
+        toks = np.ascontiguousarray(tokens, dtype=np.int32)
+        got = ctypes.c_int(0)
+        _check(lib().pa_alloc_match_prefix(self._h, int(seq_id), toks.ctypes.data, len(toks),
+                                           ctypes.c_uint64(int(extra_key) & (2 ** 64 - 1)), ctypes.byref(got)),
+               "pa_alloc_match_prefix")
+        return got.value
+
+    def free_queue(self):
+        n = ctypes.c_int64(0)
+        lib().pa_alloc_free_queue(self._h, None, 0, ctypes.byref(n))
+        out = np.empty(n.value, dtype=np.int32)
+        _check(lib().pa_alloc_free_queue(self._h, out.ctypes.data, len(out), ctypes.byref(n)), "pa_alloc_free_queue")
+        return out.tolist()
+
+    def block_hash(self, block: int):
+        h = (ctypes.c_uint8 * 32)()
+        c = ctypes.c_int(0)
+        _check(lib().pa_alloc_block_hash(self._h, int(block), h, ctypes.byref(c)), "pa_alloc_block_hash")
+        return bytes(h), bool(c.value)
+
+    def prefix_stats(self) -> dict:
+        c, q, h = ctypes.c_int64(0), ctypes.c_int64(0), ctypes.c_int64(0)
+        _check(lib().pa_alloc_prefix_stats(self._h, ctypes.byref(c), ctypes.byref(q), ctypes.byref(h)),
+               "pa_alloc_prefix_stats")
+        return {"cached_blocks": c.value, "queries": q.value, "hits": h.value}
 
     def fork(self, parent: int, child: int):
         _check(lib().pa_alloc_fork(self._h, int(parent), int(child)), "pa_alloc_fork")

@@ -223,3 +223,49 @@ def test_partition_sizes(B, H, Hkv, max_ctx, pt):
     picked = next((p for p in (1024, 512) if B * Hkv * -(-max_ctx // p) >= 4096), 256)
     assert picked == pt
     run_step(w)
+
+
+def test_prefix_cached_batch():
+    """Requests that reuse cached prompt blocks (prefix caching in the
+    allocator) decode exactly like the oracle over the same tables."""
+    bs, H, Hkv, D = 16, 16, 2, 128
+    rng = np.random.default_rng(77)
+    systems = [list(rng.integers(0, 30000, size=n)) for n in (300, 517)]
+    prompts = []
+    for i in range(10):
+        sysp = systems[i % 2]
+        prompts.append(sysp + list(rng.integers(0, 30000, size=int(rng.integers(1, 200)))))
+    total = sum(len(p) for p in prompts) + len(prompts)
+    w = workloads.custom(seed=78, num_seqs=len(prompts), num_heads=H, num_kv_heads=Hkv, head_dim=D, block_size=bs,
+                         context_lens=[len(p) + 1 for p in prompts], num_blocks=total // bs + 64)
+    ref = oracle.OracleAllocator(w.num_blocks, bs, free_order=w.free_order, prefix_cache=True)
+    dut = pa.Allocator(w.num_blocks, bs, free_order=w.free_order, prefix_cache=True)
+    for i, p in enumerate(prompts):
+        c_ref = ref.match_prefix(i, p)
+        c_dut = dut.match_prefix(i, p)
+        assert c_ref == c_dut
+        ref.append_batch([i], [len(p) - c_ref], p[c_ref:])
+        dut.append_ids([i], [len(p) - c_dut], p[c_dut:])
+    assert dut.prefix_stats() == ref.prefix_stats() and dut.prefix_stats()["hits"] > 20
+    used = ref.used_slot_mask()
+    ids = list(range(len(prompts)))
+    rs, rp = ref.append_batch(ids, [1] * len(ids))
+    ds, dp = dut.append(ids, [1] * len(ids))
+    assert list(ds) == rs and len(dp) == 0 and rp == []
+    tables, lens = dut.block_tables(ids, w.max_blocks_per_seq)
+    rt, rl = ref.tables(ids, w.max_blocks_per_seq)
+    assert np.array_equal(tables, rt) and np.array_equal(lens, rl)
+    # poison every slot no history token uses, then one decode step
+    from scenario import poisoned_pools
+    k0, v0 = poisoned_pools(w, used)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    k, v = t(k0), t(v0)
+    q, out = t(w.query), torch.empty(w.query.shape, dtype=torch.float16, device="cuda")
+    ws = torch.zeros(pa.pa_decode_workspace_size(w.num_seqs, H, Hkv, D, w.max_context_len), dtype=torch.uint8,
+                     device="cuda")
+    pa.pa_kv_write(t(w.new_key), t(w.new_value), t(np.asarray(ds)), k, v)
+    pa.pa_decode(out, q, k, v, t(tables), t(lens), w.scale, w.max_context_len, ws)
+    torch.cuda.synchronize()
+    kc, vc = oracle.kv_write(k0, v0, w.new_key, w.new_value, np.asarray(rs), bs)
+    expect = oracle.paged_decode(w.query, kc, vc, rt, rl, Hkv, bs, w.scale)
+    compare(out.cpu().numpy(), expect)
