@@ -51,6 +51,9 @@ def parse():
     p.add_argument("--workload", default=WORKLOAD, help="gqa72b (the headline), mha7b, mix, cow16, cow32, tiny")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="skip the CUDA Graph replay measurement")
+    p.add_argument("--shared-prefix", action="store_true",
+                   help="parallel-sampling workloads: decode with pa_decode_shared_prefix (samples of one prompt "
+                        "read its blocks together)")
     p.add_argument("--seqs", type=int, default=None,
                    help="same shape with fewer sequences (small cases for profiling); default: the full 100")
     return p.parse_args()
@@ -294,8 +297,16 @@ def run_ours(args):
     d_tables = torch.from_numpy(tables).to(dev)
     d_lens = torch.from_numpy(lens).to(dev)
     out = torch.empty_like(q)
-    ws = torch.zeros(pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
-                                                 w.max_context_len), dtype=torch.uint8, device=dev)
+    shared_mode = bool(args.shared_prefix and w.num_prompts)
+    if shared_mode:
+        S = w.samples_per_prompt
+        d_lead = torch.from_numpy(np.repeat(np.arange(w.num_prompts) * S, S).astype(np.int32)).to(dev)
+        d_shl = torch.full((w.num_seqs,), w.prompt_len, dtype=torch.int32, device=dev)
+        nws = pa.pa_decode_shared_prefix_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                                        w.max_context_len)
+    else:
+        nws = pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.max_context_len)
+    ws = torch.zeros(nws, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
     def writes_on(st):
@@ -304,7 +315,11 @@ def run_ours(args):
         pa.pa_kv_write(nk, nv, d_slots, k, v, st)
 
     def decode_on(st):
-        pa.pa_decode(out, q, k, v, d_tables, d_lens, w.scale, w.max_context_len, ws, st)
+        if shared_mode:
+            pa.pa_decode_shared_prefix(out, q, k, v, d_tables, d_lens, d_lead, d_shl, w.scale, w.max_context_len, ws,
+                                       st)
+        else:
+            pa.pa_decode(out, q, k, v, d_tables, d_lens, w.scale, w.max_context_len, ws, st)
 
     def writes():
         writes_on(stream)
@@ -469,6 +484,7 @@ def run_ours(args):
         line["roofline"]["unique_kv_bytes_per_launch"] = ub
         line["roofline"]["achieved_unique"] = round(ub / (dec_avg_ms / 1e3) / 1e9, 1)
         line["copy_pairs"] = int(len(pairs))
+        line["decode_call"] = "pa_decode_shared_prefix" if shared_mode else "pa_decode"
     if not args.no_cpu_baseline and world == 1 and not w.num_prompts:
         smp = OracleSample(w, tables, lens, target_s=10.0)
         rate, secs = smp.rate()

@@ -163,6 +163,41 @@ PA_API int pa_decode(uint16_t *out, const uint16_t *query,
               int64_t num_blocks, int max_blocks_per_seq, int max_context_len, float scale,
               void *workspace, size_t workspace_bytes, void *stream);
 
+/* ------------------------------------------- decode with shared prefixes */
+
+/* Workspace bytes pa_decode_shared_prefix needs (a host-side bound). */
+PA_API size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                                     int max_context_len);
+
+/* pa_decode for a batch in which groups of sequences share the physical
+ * blocks of a common prefix (parallel sampling or beam search over one
+ * prompt: deepsonar page section 2.3; a prompt shared by several requests:
+ * deeplearn.tn page, "Les benefices concrets a l'usage").  A shared block is
+ * then read from HBM and reduced once for several members together (up to
+ * 16 query rows, i.e. 16 / G members, per pass) instead of once per member.
+ * Same arguments as pa_decode, plus two device int32 arrays of num_seqs:
+ *   group_leader[i]  the first sequence of i's group (i itself when it leads
+ *                    a group or shares nothing).  A group is the run of
+ *                    consecutive sequences, starting at its leader, that all
+ *                    name that leader; a sequence outside its leader's run is
+ *                    treated as sharing nothing.
+ *   shared_len[i]    read at leaders only: tokens at the start of every
+ *                    member's context that live in the same physical blocks
+ *                    (the first shared_len / block_size table entries of all
+ *                    members are equal).  Rounded down to whole blocks and
+ *                    capped by the shortest member's context; 0 = no sharing.
+ * The caller guarantees the equal table entries (PA_DEBUG_VALIDATE checks
+ * them).  The result is the same attention as pa_decode's (the partitioning
+ * differs, so the bits may differ within the fp32 rounding).  Workspace:
+ * pa_decode_shared_prefix_workspace_size. */
+PA_API int pa_decode_shared_prefix(uint16_t *out, const uint16_t *query, const uint16_t *k_cache,
+                                   const uint16_t *v_cache, const int32_t *block_tables,
+                                   const int32_t *context_lens, const int32_t *group_leader,
+                                   const int32_t *shared_len, int num_seqs, int num_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int64_t num_blocks, int max_blocks_per_seq,
+                                   int max_context_len, float scale, void *workspace, size_t workspace_bytes,
+                                   void *stream);
+
 /* Read the error word a pa_decode call left in its workspace: PA_OK, or
  * PA_ERR_TIMEOUT if a kernel gave up waiting for its own copies into shared
  * memory (the affected outputs are NaN).  Synchronises `stream`. */

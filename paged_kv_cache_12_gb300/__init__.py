@@ -39,6 +39,7 @@ EXPORTS = (
     "pa_alloc_fork", "pa_alloc_free_seq", "pa_alloc_seq_len", "pa_alloc_block_tables", "pa_alloc_refcount",
     "pa_alloc_stats", "pa_decode_static_ws", "pa_alloc_free_queue", "pa_alloc_enable_prefix_cache",
     "pa_alloc_match_prefix", "pa_alloc_append_ids", "pa_alloc_block_hash", "pa_alloc_prefix_stats", "pa_sha256",
+    "pa_decode_shared_prefix_workspace_size", "pa_decode_shared_prefix",
 )
 
 # bytes of the library's built-in scratch array used by pa_decode_static_ws
@@ -94,6 +95,9 @@ def lib():
             "pa_alloc_block_hash": ([vp, i64, vp, ctypes.POINTER(i32)], i32),
             "pa_alloc_prefix_stats": ([vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i64)], i32),
             "pa_sha256": ([vp, sz, vp], i32),
+            "pa_decode_shared_prefix_workspace_size": ([i32, i32, i32, i32, i32], sz),
+            "pa_decode_shared_prefix": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, i32, i32,
+                                         ctypes.c_float, vp, sz, vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -215,6 +219,38 @@ def pa_decode_static_ws(out, query, k_cache, v_cache, block_tables, context_lens
                                      block_tables.data_ptr(), context_lens.data_ptr(), B, hq, hkv, d, bs, nb,
                                      block_tables.shape[1], int(max_context_len), float(scale), _stream(stream)),
            "pa_decode_static_ws")
+
+
+def pa_decode_shared_prefix_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len) -> int:
+    n = lib().pa_decode_shared_prefix_workspace_size(int(num_seqs), int(num_heads), int(num_kv_heads),
+                                                     int(head_dim), int(max_context_len))
+    if n == 0:
+        raise PAError(PA_ERR_INVALID_ARG, "pa_decode_shared_prefix_workspace_size")
+    return n
+
+
+def pa_decode_shared_prefix(out, query, k_cache, v_cache, block_tables, context_lens, group_leader, shared_len,
+                            scale, max_context_len, workspace, stream=None):
+    """pa_decode where runs of sequences share the blocks of a common prefix:
+    group_leader[i] = first sequence of i's group, shared_len[leader] = tokens
+    shared (int32 device tensors of num_seqs)."""
+    import torch
+    for t, dt, nd, nm in ((out, torch.float16, 3, "out"), (query, torch.float16, 3, "query"),
+                          (k_cache, torch.float16, 4, "k_cache"), (v_cache, torch.float16, 4, "v_cache"),
+                          (block_tables, torch.int32, 2, "block_tables"), (context_lens, torch.int32, 1, "context_lens"),
+                          (group_leader, torch.int32, 1, "group_leader"), (shared_len, torch.int32, 1, "shared_len"),
+                          (workspace, torch.uint8, 1, "workspace")):
+        _need(t, dt, nd, nm)
+    nb, hkv, bs, d = k_cache.shape
+    B, hq, d2 = query.shape
+    if out.shape != query.shape or d2 != d or v_cache.shape != k_cache.shape or block_tables.shape[0] != B \
+            or context_lens.shape[0] != B or group_leader.shape[0] != B or shared_len.shape[0] != B:
+        raise ValueError("pa_decode_shared_prefix: shape mismatch")
+    _check(lib().pa_decode_shared_prefix(out.data_ptr(), query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                         block_tables.data_ptr(), context_lens.data_ptr(), group_leader.data_ptr(),
+                                         shared_len.data_ptr(), B, hq, hkv, d, bs, nb, block_tables.shape[1],
+                                         int(max_context_len), float(scale), workspace.data_ptr(), workspace.numel(),
+                                         _stream(stream)), "pa_decode_shared_prefix")
 
 
 def pa_workspace_status(workspace, stream=None) -> int:

@@ -92,49 +92,72 @@ struct WsHeader {
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
 struct WsLayout {
-    size_t part_off, sp_info, grp, ml, o, total;
+    size_t part_off, gsize, gshared, items, grp, ml, o, total;
     int pmax, pt;
+    long long item_cap;
 };
 
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 
-WsLayout ws_layout(int B, int Hq, int Hkv, int D, int max_ctx) {
+// Workspace of one call.  grouped: sequences may share a prefix, which adds
+// at most one partition per sequence and as many shared items again.
+WsLayout ws_layout(int B, int Hq, int Hkv, int D, int max_ctx, bool grouped) {
     WsLayout w;
     w.pt = part_tokens(B, Hkv, max_ctx);
     w.pmax = max_ctx > 0 ? (max_ctx + w.pt - 1) / w.pt : 1;
+    const long long parts = (long long)B * (w.pmax + (grouped ? 1 : 0));   // partial-result rows per head
+    w.item_cap = (long long)B * w.pmax * (grouped ? 2 : 1);
     size_t off = sizeof(WsHeader);
     w.part_off = off;
     off += up256(sizeof(int) * ((size_t)B + 1));
-    w.sp_info = off;
-    off += up256(sizeof(int4) * (size_t)B * w.pmax);
+    w.gsize = off;
+    if (grouped) off += up256(sizeof(int) * (size_t)B);
+    w.gshared = off;
+    if (grouped) off += up256(sizeof(int) * (size_t)B);
+    w.items = off;
+    off += up256(2 * sizeof(int4) * (size_t)w.item_cap);
+    const bool multi = w.pmax > 1 || grouped;
     w.grp = off;
-    if (w.pmax > 1) off += up256(sizeof(int) * (size_t)B * Hq);
+    if (multi) off += up256(sizeof(int) * (size_t)B * Hq);
     w.ml = off;
-    if (w.pmax > 1) off += up256(sizeof(float2) * (size_t)B * w.pmax * Hq);
+    if (multi) off += up256(sizeof(float2) * (size_t)parts * Hq);
     w.o = off;
-    if (w.pmax > 1) off += up256(sizeof(float) * (size_t)B * w.pmax * Hq * D);
+    if (multi) off += up256(sizeof(float) * (size_t)parts * Hq * D);
     w.total = off;
     return w;
 }
+
+// A work item record (two int4): a token range [t0, t1) of the caches read
+// for nmem consecutive sequences seq0 .. seq0 + nmem - 1 that share those
+// blocks, the range's partition index in each member's partition list, the
+// group's shared length, the context length of seq0 and the partial's
+// canonical row index -- or -1 for a shared-prefix item, whose members each
+// have their own (part_off[member] + partition).
+struct ItemRec {
+    int4 a;   // seq0, nmem, t0, t1
+    int4 b;   // pidx, shared, L0, canon
+};
 
 struct DecodeArgs {
     __half *out;
     const __half *query;
     const int32_t *block_tables;
-    int Hq, Hkv, G, bs, mbps, pt;
+    const int32_t *context_lens;
+    int Hq, Hkv, G, bs, mbps, pt, ms;
     long long num_blocks;
     float scale_log2;
     WsHeader *hdr;
     const int *part_off;
-    const int4 *sp_info;
+    const ItemRec *items;
     int *grp;
     float2 *ws_ml;
     float *ws_o;
 };
 
-// What the producer tells a consumer about its next item (32 bytes).
+// What the producer tells a consumer about its next item (64 bytes).
 struct ItemDesc {
-    int seq, kvh, sp, P, nchunks, ntok_last, bad, end;
+    int seq0, kvh, nmem, pidx, shared, P0, canon0, nchunks;
+    int ntok_last, bad, end, pad[5];
 };
 
 template <int D, int NT>
@@ -147,7 +170,7 @@ struct Cfg {
     static constexpr int CTRL = 256;                       // per consumer: barriers and descriptors
     static constexpr int SMEM = NC * (DATA + CTRL) + 1024;
     static_assert(DATA % 1024 == 0, "stages must stay 1024-byte aligned for the 128-byte swizzle");
-    static_assert((2 * DEPTH + 2) * 8 + 2 * 32 <= CTRL, "control block too small");
+    static_assert((2 * DEPTH + 2) * 8 + 16 + 2 * 64 <= CTRL, "control block too small");
 };
 
 // Byte offset, inside a swizzled tile, of 16-byte column `col` (0 .. D/8-1)
@@ -187,45 +210,119 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_sums, int *
     return excl;
 }
 
-// Work list, longest first: every sequence's partitions but its last are
-// full (pt tokens) and come first, in sequence order; the last partitions
-// follow in decreasing length (a counting sort on 16-token buckets), so
-// that the dynamically scheduled tail of the kernel runs the shortest items.
-// An item record is {seq, partition, L, canonical index}; partial results
-// are stored at the canonical index part_off[seq] + partition, independent
-// of the order.
+// Partitions of one sequence: its shared prefix [0, S) and its own range
+// [S, L), each cut into pieces of pt tokens (S = 0 for a sequence that
+// shares nothing).
+__device__ __forceinline__ int partitions_of(int L, int S, int pt) {
+    return (S + pt - 1) / pt + (L - S + pt - 1) / pt;
+}
+
+// Work list, longest first.  Items of full length (pt tokens) come first:
+// shared-prefix items of every group, then each sequence's own partitions
+// but its last, in sequence order; every sequence's last partition and the
+// shorter shared items follow in decreasing length (a counting sort on
+// 16-token buckets).  So the dynamically scheduled tail of the kernel runs
+// the shortest items, and the merges, which follow a sequence's last
+// partition, land mostly in that tail where consumers would idle anyway.  Partial results are
+// stored at canonical rows part_off[seq] + partition, independent of the
+// order.
+//
+// Groups (optional): sequence i names the leader of its group in lead[i];
+// the group is the run of consecutive sequences from the leader that all name
+// it, and shares the leader's shared_len[] tokens (rounded down to whole
+// blocks, capped by every member's context).  A shared range is read once per
+// item for up to ms members together.
 __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
-    const int32_t *__restrict__ context_lens, int B, int Hq, int D, int Hkv, int max_ctx, long long max_table_tokens,
-    int pt, WsHeader *hdr, int *part_off, int4 *sp_info, int *grp, __half *out) {
-    constexpr int NBK = MAX_PART_TOKENS / CHUNK;     // length buckets of the last partitions
+    const int32_t *__restrict__ context_lens, const int32_t *__restrict__ lead,
+    const int32_t *__restrict__ shared_len, int B, int Hq, int D, int Hkv, int bs, int max_ctx,
+    long long max_table_tokens, int pt, int ms, WsHeader *hdr, int *part_off, int *gsize, int *gshared,
+    ItemRec *items, int *grp, __half *out) {
+    constexpr int NBK = MAX_PART_TOKENS / CHUNK;     // length buckets of the short items
     __shared__ int warp_sums[PREP_THREADS / 32];
     __shared__ int hist[NBK], cursor[NBK];
     int run_p = 0, run_f = 0;                        // uniform running totals
     for (int k = threadIdx.x; k < NBK; k += PREP_THREADS) hist[k] = cursor[k] = 0;
     if (grp)
         for (long long k = threadIdx.x; k < (long long)B * Hkv; k += PREP_THREADS) grp[k] = 0;
+    auto valid_len = [&](int L) { return L >= 0 && L <= max_ctx && (long long)L <= max_table_tokens; };
+    // pass 0: group sizes and shared lengths, at each leader
+    if (lead)
+        for (int i = threadIdx.x; i < B; i += PREP_THREADS) {
+            int M = 0, S = 0;
+            if (lead[i] == i) {
+                S = shared_len[i] > 0 ? shared_len[i] / bs * bs : 0;
+                bool ok = true;
+                for (int j = i; j < B && lead[j] == i; ++j, ++M) {
+                    const int L = context_lens[j];
+                    ok = ok && valid_len(L) && L > 0;
+                    S = min(S, ok ? L : 0);
+                }
+                S = S / bs * bs;   // whole blocks only, also after capping by a member's context
+                if (!ok || M < 2) S = 0;
+            }
+            gsize[i] = M;
+            gshared[i] = S;
+        }
     __syncthreads();
+    // the shared length of sequence i: its leader's, if i is in the leader's run
+    auto shared_of = [&](int i, int &ld) -> int {
+        ld = i;
+        if (!lead) return 0;
+        const int l = lead[i];
+        if (l < 0 || l > i || i - l >= gsize[l] || gshared[l] == 0) return 0;
+        ld = l;
+        return gshared[l];
+    };
     const int nbk = pt / CHUNK;
-    // pass 1: partition counts, canonical offsets, full items, bucket histogram
+    // pass 1: partitions and canonical offsets; full-length items; histogram of the short ones
     for (int base = 0; base < B; base += PREP_THREADS) {
         const int i = base + threadIdx.x;
-        int L = 0, P = 0, code = 0;                  // code 1: zero row, 2: NaN row
+        int L = 0, P = 0, code = 0, S = 0, ld = i, nfull = 0;   // code 1: zero row, 2: NaN row
+        int Ms = 0, Ps = 0;                                      // leader: members, shared partitions
         if (i < B) {
             L = context_lens[i];
-            if (L < 0 || L > max_ctx || (long long)L > max_table_tokens)
+            S = shared_of(i, ld);
+            if (!valid_len(L))
                 code = 2;
             else if (L == 0)
                 code = 1;
             else
-                P = (L + pt - 1) / pt;
+                P = partitions_of(L, S, pt);
+            if (P > 0) {
+                nfull = (L - S + pt - 1) / pt - 1;   // own partitions but the last
+                if (ld == i && S > 0) {
+                    Ms = gsize[i];
+                    Ps = (S + pt - 1) / pt;
+                    nfull += (S / pt) * ((Ms + ms - 1) / ms);
+                }
+            }
         }
         int tp, tf;
         const int ep = run_p + block_exclusive_scan(P, warp_sums, &tp);
-        const int ef = run_f + block_exclusive_scan(P > 0 ? P - 1 : 0, warp_sums, &tf);
+        int ef = run_f + block_exclusive_scan(nfull, warp_sums, &tf);
         if (i < B) {
             part_off[i] = ep;
-            for (int p = 0; p + 1 < P; ++p) sp_info[ef + p] = make_int4(i, p, L, ep + p);
-            if (P > 0) atomicAdd(&hist[(pt - (L - (P - 1) * pt)) / CHUNK], 1);
+            if (P > 0) {
+                const int ps_i = (S + pt - 1) / pt;
+                if (Ps > 0) {   // leader: full shared items
+                    for (int p = 0; p < S / pt; ++p)
+                        for (int k = 0; k < Ms; k += ms) {
+                            ItemRec r;
+                            r.a = make_int4(i + k, min(ms, Ms - k), p * pt, (p + 1) * pt);
+                            r.b = make_int4(p, S, L, -1);
+                            items[ef++] = r;
+                        }
+                    if (S % pt) atomicAdd(&hist[(pt - S % pt) / CHUNK], (Ms + ms - 1) / ms);
+                }
+                const int pp = (L - S + pt - 1) / pt;      // own partitions
+                for (int p = 0; p + 1 < pp; ++p) {         // all full but the last
+                    ItemRec r;
+                    r.a = make_int4(i, 1, S + p * pt, S + (p + 1) * pt);
+                    r.b = make_int4(ps_i + p, S, L, ep + ps_i + p);
+                    items[ef++] = r;
+                }
+                if (pp > 0) atomicAdd(&hist[(pt - (L - S - (pp - 1) * pt)) / CHUNK], 1);
+            }
             if (code) {
                 const uint32_t h = code == 1 ? 0u : 0x7e007e00u;
                 uint4 fill = make_uint4(h, h, h, h);
@@ -237,7 +334,7 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
         run_f += tf;
     }
     __syncthreads();
-    // bucket starts, largest last partitions first
+    int total_items = run_f;
     if (threadIdx.x == 0) {
         int acc = run_f;
         for (int k = 0; k < nbk; ++k) {
@@ -246,17 +343,36 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
         }
     }
     __syncthreads();
-    // pass 2: place the last partitions
+    // pass 2: short items, longest first
     for (int i = threadIdx.x; i < B; i += PREP_THREADS) {
         const int L = context_lens[i];
-        if (L <= 0 || L > max_ctx || (long long)L > max_table_tokens) continue;
-        const int P = (L + pt - 1) / pt;
-        const int slot = atomicAdd(&cursor[(pt - (L - (P - 1) * pt)) / CHUNK], 1);
-        sp_info[slot] = make_int4(i, P - 1, L, part_off[i] + P - 1);
+        if (L <= 0 || !valid_len(L)) continue;
+        int ld;
+        const int S = shared_of(i, ld);
+        const int ps_i = (S + pt - 1) / pt;
+        if (ld == i && S > 0 && S % pt) {
+            const int Ms = gsize[i];
+            for (int k = 0; k < Ms; k += ms) {
+                ItemRec r;
+                r.a = make_int4(i + k, min(ms, Ms - k), S / pt * pt, S);
+                r.b = make_int4(ps_i - 1, S, L, -1);
+                items[atomicAdd(&cursor[(pt - S % pt) / CHUNK], 1)] = r;
+            }
+        }
+        const int pp = (L - S + pt - 1) / pt;
+        if (pp > 0) {
+            const int p = pp - 1;
+            ItemRec r;
+            r.a = make_int4(i, 1, S + p * pt, L);
+            r.b = make_int4(ps_i + p, S, L, part_off[i] + ps_i + p);
+            items[atomicAdd(&cursor[(pt - (L - S - p * pt)) / CHUNK], 1)] = r;
+        }
     }
+    __syncthreads();
     if (threadIdx.x == 0) {
+        total_items = cursor[nbk - 1];
         part_off[B] = run_p;
-        hdr->total_items = run_p * Hkv;
+        hdr->total_items = total_items * Hkv;
         hdr->counter = 0;
         hdr->error = 0;
     }
@@ -281,7 +397,7 @@ __device__ __forceinline__ ConsumerSmem consumer_smem(uint8_t *smem, int c) {
     s.full = reinterpret_cast<uint64_t *>(ctrl);
     s.empty = s.full + DEPTH;
     s.qfree = s.empty + DEPTH;
-    s.desc = reinterpret_cast<ItemDesc *>(ctrl + (2 * DEPTH + 2) * 8);
+    s.desc = reinterpret_cast<ItemDesc *>(ctrl + (2 * DEPTH + 2) * 8 + 16);
     return s;
 }
 
@@ -301,39 +417,35 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
     // fields plus, per lane, its block-table entries lane and lane + 32.
     int raw = 0;
     int nn_item = -1;
-    int4 nn_inf = make_int4(0, 0, 0, 0);
-    int n_item = -1, n_seq = 0, n_p = 0, n_L = 0, n_P = 0, n_fb = 0, n_canon = 0;
+    ItemRec nn_rec;
+    nn_rec.a = nn_rec.b = make_int4(0, 0, 0, 0);
+    int n_item = -1, n_fb = 0;
+    ItemRec n_rec = nn_rec;
     int n_e[ENTRIES];
 #pragma unroll
     for (int e = 0; e < ENTRIES; ++e) n_e[e] = 0;
     auto advance = [&]() {
         n_item = nn_item;
         if (n_item >= 0) {
-            n_seq = nn_inf.x;
-            n_p = nn_inf.y;
-            n_L = nn_inf.z;
-            n_canon = nn_inf.w;
-            n_P = (n_L + a.pt - 1) / a.pt;
-            const int t0 = n_p * a.pt;
-            const int t1 = min(n_L, t0 + a.pt);
-            n_fb = t0 / a.bs;
-            const int nb = (t1 + a.bs - 1) / a.bs - n_fb;
-            const int32_t *row = a.block_tables + (long long)n_seq * a.mbps + n_fb;
+            n_rec = nn_rec;
+            n_fb = n_rec.a.z / a.bs;
+            const int nb = (n_rec.a.w + a.bs - 1) / a.bs - n_fb;
+            const int32_t *row = a.block_tables + (long long)n_rec.a.x * a.mbps + n_fb;
 #pragma unroll
             for (int e = 0; e < ENTRIES; ++e) n_e[e] = lane + 32 * e < nb ? row[lane + 32 * e] : 0;
         }
         const int j = __shfl_sync(0xffffffffu, raw, 0);
         nn_item = j < total ? j : -1;
-        if (nn_item >= 0) nn_inf = a.sp_info[nn_item / a.Hkv];
+        if (nn_item >= 0) nn_rec = a.items[nn_item / a.Hkv];
         if (lane == 0) raw = atomicAdd(&a.hdr->counter, 1);
     };
 
     // per-consumer state (NC is small and the loops over it are unrolled)
-    int sc[NC], ic[NC], chunk[NC], nch[NC], t0[NC], t1[NC], fb[NC], y[NC][ENTRIES], qrow[NC];
+    int sc[NC], ic[NC], chunk[NC], nch[NC], t0[NC], t1[NC], fb[NC], y[NC][ENTRIES], qrow[NC], nmem[NC];
     bool done[NC], bad[NC];
 #pragma unroll
     for (int c = 0; c < NC; ++c) {
-        sc[c] = ic[c] = chunk[c] = nch[c] = t0[c] = t1[c] = fb[c] = qrow[c] = 0;
+        sc[c] = ic[c] = chunk[c] = nch[c] = t0[c] = t1[c] = fb[c] = qrow[c] = nmem[c] = 0;
 #pragma unroll
         for (int e = 0; e < ENTRIES; ++e) y[c][e] = 0;
         done[c] = bad[c] = false;
@@ -356,7 +468,11 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
                 ok = mbar_wait_bounded(smem_u32(&cs.qfree[q]), ((ic[c] >> 1) & 1) ^ 1, WAIT_LIMIT);
                 if (ok && n_item < 0) {              // nothing left: tell the consumer to stop
                     if (lane == 0) {
-                        ItemDesc e = {0, 0, 0, 0, 0, 0, 0, 1};
+                        ItemDesc e;
+                        e.seq0 = e.kvh = e.nmem = e.pidx = e.shared = e.P0 = e.canon0 = e.nchunks = 0;
+                        e.ntok_last = e.bad = 0;
+                        e.end = 1;
+                        e.pad[0] = e.pad[1] = e.pad[2] = e.pad[3] = e.pad[4] = 0;
                         cs.desc[q] = e;
                         mbar_arrive(full);
                     }
@@ -365,12 +481,12 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
                     continue;
                 }
                 if (ok) {
-                    const int sp = n_item / a.Hkv;
-                    const int kvh = n_item - sp * a.Hkv;
-                    t0[c] = n_p * a.pt;
-                    t1[c] = min(n_L, t0[c] + a.pt);
+                    const int kvh = n_item % a.Hkv;
+                    t0[c] = n_rec.a.z;
+                    t1[c] = n_rec.a.w;
                     fb[c] = n_fb;
                     nch[c] = (t1[c] - t0[c] + CHUNK - 1) / CHUNK;
+                    nmem[c] = n_rec.a.y;
                     const int nb = (t1[c] + a.bs - 1) / a.bs - n_fb;
                     bool bad_any = false;
 #pragma unroll
@@ -379,18 +495,22 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
                         y[c][e] = (int)(((long long)n_e[e] * a.Hkv + kvh) * a.bs);
                     }
                     bad[c] = __any_sync(0xffffffffu, bad_any);
-                    qrow[c] = n_seq * a.Hq + kvh * a.G;
+                    qrow[c] = n_rec.a.x * a.Hq + kvh * a.G;
                     chunk[c] = 0;
                     if (lane == 0) {
                         ItemDesc d;
-                        d.seq = n_seq;
+                        d.seq0 = n_rec.a.x;
                         d.kvh = kvh;
-                        d.sp = n_canon;
-                        d.P = n_P;
+                        d.nmem = n_rec.a.y;
+                        d.pidx = n_rec.b.x;
+                        d.shared = n_rec.b.y;
+                        d.P0 = partitions_of(n_rec.b.z, n_rec.b.y, a.pt);
+                        d.canon0 = n_rec.b.w;
                         d.nchunks = nch[c];
                         d.ntok_last = t1[c] - (t0[c] + (nch[c] - 1) * CHUNK);
                         d.bad = bad[c] ? 1 : 0;
                         d.end = 0;
+                        d.pad[0] = d.pad[1] = d.pad[2] = d.pad[3] = d.pad[4] = 0;
                         cs.desc[q] = d;
                     }
                     ++ic[c];
@@ -418,7 +538,7 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
             if (lane == 0) {
                 const bool two = a.bs < CHUNK && ntok > a.bs;
                 uint32_t bytes = bad[c] ? 0u : 2u * C::BOXES * box_rows * 128u * (two ? 2u : 1u);
-                if (first && !bad[c]) bytes += (uint32_t)(a.G * D * 2);
+                if (first && !bad[c]) bytes += (uint32_t)(nmem[c] * a.G * D * 2);
                 mbar_arrive_expect_tx(full, bytes);
                 if (!bad[c]) {
                     const uint32_t kdst = cs.data + s * C::STAGE;
@@ -436,9 +556,11 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
                             tma_load_2d(vdst + b * CHUNK * 128 + a.bs * 128, tmv, 64 * b, yb, full, pol);
                         }
                     }
-                    if (first)
-                        bulk_load(cs.data + DEPTH * C::STAGE + ((ic[c] - 1) & 1) * C::QSLOT,
-                                  a.query + (long long)qrow[c] * D, (uint32_t)(a.G * D * 2), full);
+                    if (first)   // the query rows of every member, one run of G rows each
+                        for (int m = 0; m < nmem[c]; ++m)
+                            bulk_load(cs.data + DEPTH * C::STAGE + ((ic[c] - 1) & 1) * C::QSLOT + m * a.G * D * 2,
+                                      a.query + ((long long)qrow[c] + (long long)m * a.Hq) * D,
+                                      (uint32_t)(a.G * D * 2), full);
                 }
             }
             ++chunk[c];
@@ -569,30 +691,35 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
     }
     const float sl2 = a.scale_log2;
 
-    // Merge tickets.  After an item of a multi-partition sequence has stored
-    // its partial, it owes a ticket for its (sequence, kv head) group: the
-    // ticket is taken after the next item's first chunk (by then the partial's
-    // stores have drained, so the fence is cheap) and inspected at that item's
-    // end (so the atomic's latency is hidden); the warp holding the group's
-    // last ticket merges the group then.
+    // Merge tickets.  After an item has stored partials for members of
+    // multi-partition sequences, it owes one ticket per such member for the
+    // (member, kv head) group; lane m holds member m's.  The tickets are taken
+    // after the next item's first chunk (by then the partials' stores have
+    // drained, so the fence is cheap) and inspected at that item's end (so the
+    // atomics' latency is hidden); a lane holding a group's last ticket has
+    // the warp merge that group.
     bool owe = false;
-    int owe_seq = 0, owe_kvh = 0, owe_P = 0;
+    int owe_seq = 0, owe_kvh = 0, owe_P = 0;          // per lane: member lane
     int pend_ticket = 0, pend_seq = 0, pend_kvh = 0, pend_P = 0;
     auto take_ticket = [&]() {
         __syncwarp();
         __threadfence();
         pend_ticket = 0;
-        if (lane == 0) pend_ticket = atomicAdd(&a.grp[owe_seq * a.Hkv + owe_kvh], 1);
+        if (owe_P > 1) pend_ticket = atomicAdd(&a.grp[owe_seq * a.Hkv + owe_kvh], 1);
         pend_seq = owe_seq;
         pend_kvh = owe_kvh;
         pend_P = owe_P;
         owe = false;
+        owe_P = 0;
     };
     auto settle = [&]() {
-        const int t = __shfl_sync(0xffffffffu, pend_ticket, 0);
-        if (pend_P > 0 && t == pend_P - 1) {
-            __threadfence();
-            merge_group<D>(a, pend_seq, pend_kvh, pend_P);
+        unsigned last = __ballot_sync(0xffffffffu, pend_P > 1 && pend_ticket == pend_P - 1);
+        if (last) __threadfence();
+        while (last) {
+            const int l0 = __ffs(last) - 1;
+            last &= last - 1;
+            merge_group<D>(a, __shfl_sync(0xffffffffu, pend_seq, l0), __shfl_sync(0xffffffffu, pend_kvh, l0),
+                           __shfl_sync(0xffffffffu, pend_P, l0));
         }
         pend_P = 0;
     };
@@ -605,8 +732,10 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
             if (lane == 0) atomicExch(&a.hdr->error, PA_ERR_TIMEOUT);
             return;
         }
-        const ItemDesc dsc = cs.desc[q];
-        if (dsc.end) {
+        // the descriptor stays in shared memory for the whole item (its slot is
+        // released at the item's end); only the chunk count lives in registers
+        const volatile ItemDesc *dp = &cs.desc[q];
+        if (dp->end) {
             if (owe) take_ticket();
             settle();
             return;
@@ -625,8 +754,7 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                     qb[t][k][1] = *reinterpret_cast<const uint32_t *>(row + 8);
                 }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&cs.qfree[q]));   // query slot and descriptor read
+        const int nchunks = dp->nchunks;
 
         // running state per head column (2 * cq, 2 * cq + 1) of each head tile
         float m[NT][2], l[NT][2];
@@ -639,7 +767,7 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
             for (int i = 0; i < MT; ++i) acc[i][t][0] = acc[i][t][1] = acc[i][t][2] = acc[i][t][3] = 0.f;
         }
 
-        for (int ch = 0; ch < dsc.nchunks; ++ch) {
+        for (int ch = 0; ch < nchunks; ++ch) {
             if (ch > 0) {
                 s = stage % DEPTH;
                 if (!mbar_wait_bounded(smem_u32(&cs.full[s]), (stage / DEPTH) & 1, WAIT_LIMIT)) {
@@ -649,7 +777,7 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
             }
             const uint32_t kt = cs.data + s * C::STAGE;
             const uint32_t vt = kt + C::TILE;
-            const int ntok = ch == dsc.nchunks - 1 ? dsc.ntok_last : CHUNK;
+            const int ntok = ch == nchunks - 1 ? dp->ntok_last : CHUNK;
 
             // S^T (16 tokens x 8 heads per head tile): two accumulation chains
             float sa[NT][4], sb[NT][4];
@@ -757,48 +885,54 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                 l[t][e] = v;
             }
         const float qnan = __int_as_float(0x7fc00000);
-        if (dsc.P == 1) {
+        const ItemDesc dsc = *const_cast<const ItemDesc *>(dp);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&cs.qfree[q]));   // query slot and descriptor free again
+        // per query row: member m = row / G of the item, head g = row % G;
+        // P and the partial's row are the member's own
 #pragma unroll
-            for (int t = 0; t < NT; ++t)
+        for (int t = 0; t < NT; ++t)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int g = t * 8 + 2 * cq + e;
-                    if (g < a.G) {
+            for (int e = 0; e < 2; ++e) {
+                const int row = t * 8 + 2 * cq + e;
+                if (row < dsc.nmem * a.G) {
+                    const int mbr = row / a.G, g = row - mbr * a.G;
+                    const int seq = dsc.seq0 + mbr;
+                    int P = dsc.P0, canon = dsc.canon0;
+                    if (dsc.canon0 < 0) {   // a shared-prefix item: every member has its own P and row
+                        P = partitions_of(__ldg(&a.context_lens[seq]), dsc.shared, a.pt);
+                        canon = __ldg(&a.part_off[seq]) + dsc.pidx;
+                    }
+                    const int h = dsc.kvh * a.G + g;
+                    if (P == 1) {
                         const float inv = dsc.bad ? qnan : 1.f / l[t][e];
-                        __half *orow = a.out + ((long long)dsc.seq * a.Hq + dsc.kvh * a.G + g) * D;
+                        __half *orow = a.out + ((long long)seq * a.Hq + h) * D;
 #pragma unroll
                         for (int i = 0; i < MT; ++i) {
                             orow[16 * i + r] = __float2half_rn(acc[i][t][e] * inv);
                             orow[16 * i + r + 8] = __float2half_rn(acc[i][t][e + 2] * inv);
                         }
-                    }
-                }
-        } else {
-#pragma unroll
-            for (int t = 0; t < NT; ++t)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int g = t * 8 + 2 * cq + e;
-                    if (g < a.G) {
-                        const long long wrow = (long long)dsc.sp * a.Hq + dsc.kvh * a.G + g;
+                    } else {
+                        const long long wrow = (long long)canon * a.Hq + h;
                         float *orow = a.ws_o + wrow * D;
 #pragma unroll
                         for (int i = 0; i < MT; ++i) {
                             orow[16 * i + r] = dsc.bad ? qnan : acc[i][t][e];
                             orow[16 * i + r + 8] = dsc.bad ? qnan : acc[i][t][e + 2];
                         }
-                        if (r == 0) a.ws_ml[wrow] = dsc.bad ? make_float2(qnan, qnan) : make_float2(m[t][e], l[t][e]);
+                        if (r == 0)
+                            a.ws_ml[wrow] = dsc.bad ? make_float2(qnan, qnan) : make_float2(m[t][e], l[t][e]);
                     }
                 }
-        }
-        // the ticket taken during this item: merge its group if it was the last
+            }
+        // the tickets taken during this item: merge the groups they completed
         settle();
-        if (dsc.P > 1) {
-            owe = true;
-            owe_seq = dsc.seq;
+        if (lane < dsc.nmem) {   // tickets owed for this item's members
+            owe_seq = dsc.seq0 + lane;
             owe_kvh = dsc.kvh;
-            owe_P = dsc.P;
+            owe_P = dsc.canon0 < 0 ? partitions_of(__ldg(&a.context_lens[owe_seq]), dsc.shared, a.pt) : dsc.P0;
         }
+        owe = __any_sync(0xffffffffu, owe_P > 1);
     }
 }
 
@@ -911,10 +1045,140 @@ int launch_decode(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeAr
 
 using namespace pa;
 
+namespace pa {
+namespace {
+
+// One decode call; lead/shared_len are null for pa_decode.
+int decode_impl(uint16_t *out, const uint16_t *query, const uint16_t *k_cache, const uint16_t *v_cache,
+                const int32_t *block_tables, const int32_t *context_lens, const int32_t *lead,
+                const int32_t *shared_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                int64_t num_blocks, int max_blocks_per_seq, int max_context_len, float scale, void *workspace,
+                size_t workspace_bytes, cudaStream_t st) {
+    const bool grouped = lead != nullptr;
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
+        max_context_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || !std::isfinite(scale) || !(scale > 0.f))
+        return PA_ERR_INVALID_ARG;
+    const int G = num_heads / num_kv_heads;
+    if ((head_dim != 64 && head_dim != 128) || (block_size != 8 && block_size != 16 && block_size != 32) || G > 16)
+        return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens || (grouped && !shared_len))
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    const long long rows = (long long)num_blocks * num_kv_heads * block_size;
+    if (rows >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
+    const WsLayout L = ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len, grouped);
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total)
+        return PA_ERR_WORKSPACE;
+    if (debug_validate()) {
+        std::vector<int32_t> lens((size_t)num_seqs), tab((size_t)num_seqs * max_blocks_per_seq);
+        std::vector<int32_t> ld, sl;
+        if (cudaMemcpyAsync(lens.data(), context_lens, sizeof(int32_t) * lens.size(), cudaMemcpyDeviceToHost, st) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(tab.data(), block_tables, sizeof(int32_t) * tab.size(), cudaMemcpyDeviceToHost, st) !=
+                cudaSuccess)
+            return PA_ERR_CUDA;
+        if (grouped) {
+            ld.resize((size_t)num_seqs);
+            sl.resize((size_t)num_seqs);
+            if (cudaMemcpyAsync(ld.data(), lead, sizeof(int32_t) * ld.size(), cudaMemcpyDeviceToHost, st) !=
+                    cudaSuccess ||
+                cudaMemcpyAsync(sl.data(), shared_len, sizeof(int32_t) * sl.size(), cudaMemcpyDeviceToHost, st) !=
+                    cudaSuccess)
+                return PA_ERR_CUDA;
+        }
+        if (cudaStreamSynchronize(st) != cudaSuccess) return PA_ERR_CUDA;
+        for (int i = 0; i < num_seqs; ++i) {
+            const int len = lens[(size_t)i];
+            if (len < 0 || len > max_context_len || (long long)len > (long long)max_blocks_per_seq * block_size)
+                return PA_ERR_INVALID_ARG;
+            for (int b = 0; b < (len + block_size - 1) / block_size; ++b) {
+                const int32_t id = tab[(size_t)i * max_blocks_per_seq + b];
+                if (id < 0 || id >= num_blocks) return PA_ERR_INVALID_ARG;
+            }
+            if (grouped) {   // a member's shared blocks must be its leader's
+                const int l = ld[(size_t)i];
+                if (l < 0 || l > i || (l < i && ld[(size_t)i - 1] != l)) return PA_ERR_INVALID_ARG;
+                if (l == i && sl[(size_t)i] < 0) return PA_ERR_INVALID_ARG;
+                const int S = sl[(size_t)l] / block_size * block_size;
+                if (l < i && S > len) return PA_ERR_INVALID_ARG;
+                for (int b = 0; l < i && b < S / block_size; ++b)
+                    if (tab[(size_t)i * max_blocks_per_seq + b] != tab[(size_t)l * max_blocks_per_seq + b])
+                        return PA_ERR_INVALID_ARG;
+            }
+        }
+    }
+    const int box_rows = block_size < CHUNK ? block_size : CHUNK;
+    CUtensorMap tmk, tmv;
+    if (!cache_tensor_map(&tmk, k_cache, rows, head_dim, box_rows) ||
+        !cache_tensor_map(&tmv, v_cache, rows, head_dim, box_rows))
+        return PA_ERR_CUDA;
+
+    // query rows per item: one sequence's G heads, or, for a shared range,
+    // as many members' G heads as two head tiles hold
+    const int NT = (G > 8 || grouped) ? 2 : 1;
+    const int ms = grouped ? (16 / G > 1 ? 16 / G : 1) : 1;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
+    int *part_off = reinterpret_cast<int *>(ws + L.part_off);
+    int *gsize = grouped ? reinterpret_cast<int *>(ws + L.gsize) : nullptr;
+    int *gshared = grouped ? reinterpret_cast<int *>(ws + L.gshared) : nullptr;
+    ItemRec *items = reinterpret_cast<ItemRec *>(ws + L.items);
+    const bool multi = L.pmax > 1 || grouped;
+    int *grp = multi ? reinterpret_cast<int *>(ws + L.grp) : nullptr;
+    float2 *ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
+    float *ws_o = reinterpret_cast<float *>(ws + L.o);
+    __half *hout = reinterpret_cast<__half *>(out);
+
+    decode_prep_kernel<<<1, PREP_THREADS, 0, st>>>(context_lens, lead, shared_len, num_seqs, num_heads, head_dim,
+                                                   num_kv_heads, block_size, max_context_len,
+                                                   (long long)max_blocks_per_seq * block_size, L.pt, ms, hdr,
+                                                   part_off, gsize, gshared, items, grp, hout);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+
+    DecodeArgs args;
+    args.out = hout;
+    args.query = reinterpret_cast<const __half *>(query);
+    args.block_tables = block_tables;
+    args.context_lens = context_lens;
+    args.Hq = num_heads;
+    args.Hkv = num_kv_heads;
+    args.G = G;
+    args.bs = block_size;
+    args.mbps = max_blocks_per_seq;
+    args.pt = L.pt;
+    args.ms = ms;
+    args.num_blocks = num_blocks;
+    args.scale_log2 = scale * 1.4426950408889634f;
+    args.hdr = hdr;
+    args.part_off = part_off;
+    args.items = items;
+    args.grp = grp;
+    args.ws_ml = ws_ml;
+    args.ws_o = ws_o;
+    const long long max_items = L.item_cap * num_kv_heads;
+    if (head_dim == 128)
+        return NT == 1 ? launch_decode<128, 1>(tmk, tmv, args, max_items, st)
+                       : launch_decode<128, 2>(tmk, tmv, args, max_items, st);
+    return NT == 1 ? launch_decode<64, 1>(tmk, tmv, args, max_items, st)
+                   : launch_decode<64, 2>(tmk, tmv, args, max_items, st);
+}
+
+}  // namespace
+}  // namespace pa
+
 extern "C" size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                            int max_context_len) {
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
-    return ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len).total;
+    return ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len, false).total;
+}
+
+extern "C" size_t pa_decode_shared_prefix_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                                         int max_context_len) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len < 0) return 0;
+    return ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len, true).total;
 }
 
 extern "C" int pa_workspace_status(const void *workspace, int *status_out, void *stream) {
@@ -932,88 +1196,22 @@ extern "C" int pa_decode(uint16_t *out, const uint16_t *query, const uint16_t *k
                          const int32_t *block_tables, const int32_t *context_lens, int num_seqs, int num_heads,
                          int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, int max_blocks_per_seq,
                          int max_context_len, float scale, void *workspace, size_t workspace_bytes, void *stream) {
-    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
-        max_context_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || !std::isfinite(scale) || !(scale > 0.f))
-        return PA_ERR_INVALID_ARG;
-    const int G = num_heads / num_kv_heads;
-    if ((head_dim != 64 && head_dim != 128) || (block_size != 8 && block_size != 16 && block_size != 32) || G > 16)
-        return PA_ERR_UNSUPPORTED;
-    if (num_seqs == 0) return PA_OK;
-    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens) return PA_ERR_INVALID_ARG;
-    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
-        return PA_ERR_INVALID_ARG;
-    const long long rows = (long long)num_blocks * num_kv_heads * block_size;
-    if (rows >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
-    const WsLayout L = ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len);
-    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total)
-        return PA_ERR_WORKSPACE;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (debug_validate()) {
-        std::vector<int32_t> lens((size_t)num_seqs), tab((size_t)num_seqs * max_blocks_per_seq);
-        if (cudaMemcpyAsync(lens.data(), context_lens, sizeof(int32_t) * lens.size(), cudaMemcpyDeviceToHost, st) !=
-                cudaSuccess ||
-            cudaMemcpyAsync(tab.data(), block_tables, sizeof(int32_t) * tab.size(), cudaMemcpyDeviceToHost, st) !=
-                cudaSuccess ||
-            cudaStreamSynchronize(st) != cudaSuccess)
-            return PA_ERR_CUDA;
-        for (int i = 0; i < num_seqs; ++i) {
-            const int len = lens[(size_t)i];
-            if (len < 0 || len > max_context_len || (long long)len > (long long)max_blocks_per_seq * block_size)
-                return PA_ERR_INVALID_ARG;
-            for (int b = 0; b < (len + block_size - 1) / block_size; ++b) {
-                const int32_t id = tab[(size_t)i * max_blocks_per_seq + b];
-                if (id < 0 || id >= num_blocks) return PA_ERR_INVALID_ARG;
-            }
-        }
-    }
-    const int box_rows = block_size < CHUNK ? block_size : CHUNK;
-    CUtensorMap tmk, tmv;
-    if (!cache_tensor_map(&tmk, k_cache, rows, head_dim, box_rows) ||
-        !cache_tensor_map(&tmv, v_cache, rows, head_dim, box_rows))
-        return PA_ERR_CUDA;
+    return decode_impl(out, query, k_cache, v_cache, block_tables, context_lens, nullptr, nullptr, num_seqs,
+                       num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len,
+                       scale, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
 
-    uint8_t *ws = static_cast<uint8_t *>(workspace);
-    WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
-    int *part_off = reinterpret_cast<int *>(ws + L.part_off);
-    int4 *sp_info = reinterpret_cast<int4 *>(ws + L.sp_info);
-    int *grp = L.pmax > 1 ? reinterpret_cast<int *>(ws + L.grp) : nullptr;
-    float2 *ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
-    float *ws_o = reinterpret_cast<float *>(ws + L.o);
-    __half *hout = reinterpret_cast<__half *>(out);
-
-    decode_prep_kernel<<<1, PREP_THREADS, 0, st>>>(context_lens, num_seqs, num_heads, head_dim, num_kv_heads,
-                                                   max_context_len, (long long)max_blocks_per_seq * block_size, L.pt,
-                                                   hdr, part_off, sp_info, grp, hout);
-    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
-
-    DecodeArgs args;
-    args.out = hout;
-    args.query = reinterpret_cast<const __half *>(query);
-    args.block_tables = block_tables;
-    args.Hq = num_heads;
-    args.Hkv = num_kv_heads;
-    args.G = G;
-    args.bs = block_size;
-    args.mbps = max_blocks_per_seq;
-    args.pt = L.pt;
-    args.num_blocks = num_blocks;
-    args.scale_log2 = scale * 1.4426950408889634f;
-    args.hdr = hdr;
-    args.part_off = part_off;
-    args.sp_info = sp_info;
-    args.grp = grp;
-    args.ws_ml = ws_ml;
-    args.ws_o = ws_o;
-    const long long max_items = (long long)num_seqs * num_kv_heads * L.pmax;
-    int rc;
-    if (head_dim == 128)
-        rc = G <= 8 ? launch_decode<128, 1>(tmk, tmv, args, max_items, st)
-                    : launch_decode<128, 2>(tmk, tmv, args, max_items, st);
-    else
-        rc = G <= 8 ? launch_decode<64, 1>(tmk, tmv, args, max_items, st)
-                    : launch_decode<64, 2>(tmk, tmv, args, max_items, st);
-    if (rc != PA_OK) return rc;
-    return PA_OK;
+extern "C" int pa_decode_shared_prefix(uint16_t *out, const uint16_t *query, const uint16_t *k_cache,
+                                       const uint16_t *v_cache, const int32_t *block_tables,
+                                       const int32_t *context_lens, const int32_t *group_leader,
+                                       const int32_t *shared_len, int num_seqs, int num_heads, int num_kv_heads,
+                                       int head_dim, int block_size, int64_t num_blocks, int max_blocks_per_seq,
+                                       int max_context_len, float scale, void *workspace, size_t workspace_bytes,
+                                       void *stream) {
+    if (!group_leader) return PA_ERR_INVALID_ARG;
+    return decode_impl(out, query, k_cache, v_cache, block_tables, context_lens, group_leader, shared_len, num_seqs,
+                       num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len,
+                       scale, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------ decode without allocation
@@ -1054,7 +1252,7 @@ extern "C" int pa_decode_static_ws(uint16_t *out, const uint16_t *query, const u
                                    int max_context_len, float scale, void *stream) {
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len < 0)
         return PA_ERR_INVALID_ARG;
-    if (ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len).total >
+    if (ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len, false).total >
         (size_t)PA_DECODE_STATIC_WS_BYTES)
         return PA_ERR_WORKSPACE;
     if (num_seqs == 0) return PA_OK;

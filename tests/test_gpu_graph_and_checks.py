@@ -136,6 +136,14 @@ def test_debug_validation_mode_reports_bad_indices():
         tab_ok = torch.tensor([[0, 4], [1, 2]], dtype=torch.int32, device=dev)
         codes.append(rc(lambda: pa.pa_decode(out, q, k, v, tab_bad, lens, 0.125, 32, ws)))
         codes.append(rc(lambda: pa.pa_decode(out, q, k, v, tab_ok, lens, 0.125, 32, ws)))
+        # shared prefix: two sequences claim to share 16 tokens; their first blocks differ
+        lead = torch.tensor([0, 0], dtype=torch.int32, device=dev)
+        shl = torch.tensor([16, 0], dtype=torch.int32, device=dev)
+        ws2 = torch.zeros(pa.pa_decode_shared_prefix_workspace_size(2, 4, 2, 64, 32), dtype=torch.uint8, device=dev)
+        tab_same = torch.tensor([[0, 4], [0, 2]], dtype=torch.int32, device=dev)
+        lens2 = torch.tensor([20, 18], dtype=torch.int32, device=dev)
+        codes.append(rc(lambda: pa.pa_decode_shared_prefix(out, q, k, v, tab_ok, lens2, lead, shl, 0.125, 32, ws2)))
+        codes.append(rc(lambda: pa.pa_decode_shared_prefix(out, q, k, v, tab_same, lens2, lead, shl, 0.125, 32, ws2)))
         print(" ".join(map(str, codes)))
     """ % ROOT)
     env = dict(os.environ, PA_DEBUG_VALIDATE="1")
@@ -143,4 +151,4 @@ def test_debug_validation_mode_reports_bad_indices():
     assert res.returncode == 0, res.stderr
     codes = [int(x) for x in res.stdout.split()]
     E = pa.PA_ERR_INVALID_ARG
-    assert codes == [E, E, 0, E, E, 0, E, 0]
+    assert codes == [E, E, 0, E, E, 0, E, 0, E, 0]
