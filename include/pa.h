@@ -242,6 +242,17 @@ PA_API int pa_decode_static_ws(uint16_t *out, const uint16_t *query,
                                int block_size, int64_t num_blocks, int max_blocks_per_seq,
                                int max_context_len, float scale, void *stream);
 
+/* Failure-detection self-test.  Every wait of the decode kernel's pipeline
+ * is bounded: after about a second it records PA_ERR_TIMEOUT in the
+ * workspace (see pa_workspace_status), lets its own copies land and returns,
+ * so a stuck pipeline never hangs the GPU.  This call runs that same bounded
+ * wait in a one-warp kernel on a barrier that nothing ever completes: after
+ * limit_cycles (1 .. 2^31) it must give up and write PA_ERR_TIMEOUT to the
+ * device int *status_device.  Asynchronous on `stream`.
+ * (PA_WAIT_LIMIT_CYCLES in the environment, read once, replaces the decode
+ * pipeline's one-second bound.) */
+PA_API int pa_selftest_wait_timeout(long long limit_cycles, int *status_device, void *stream);
+
 /* ------------------------------------------------------ block allocator */
 
 /* Host-side block allocator with reference counts (no GPU involved).

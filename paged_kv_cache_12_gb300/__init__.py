@@ -39,7 +39,7 @@ EXPORTS = (
     "pa_alloc_fork", "pa_alloc_free_seq", "pa_alloc_seq_len", "pa_alloc_block_tables", "pa_alloc_refcount",
     "pa_alloc_stats", "pa_decode_static_ws", "pa_alloc_free_queue", "pa_alloc_enable_prefix_cache",
     "pa_alloc_match_prefix", "pa_alloc_append_ids", "pa_alloc_block_hash", "pa_alloc_prefix_stats", "pa_sha256",
-    "pa_decode_shared_prefix_workspace_size", "pa_decode_shared_prefix",
+    "pa_decode_shared_prefix_workspace_size", "pa_decode_shared_prefix", "pa_selftest_wait_timeout",
 )
 
 # bytes of the library's built-in scratch array used by pa_decode_static_ws
@@ -96,6 +96,7 @@ def lib():
             "pa_alloc_prefix_stats": ([vp, ctypes.POINTER(i64), ctypes.POINTER(i64), ctypes.POINTER(i64)], i32),
             "pa_sha256": ([vp, sz, vp], i32),
             "pa_decode_shared_prefix_workspace_size": ([i32, i32, i32, i32, i32], sz),
+            "pa_selftest_wait_timeout": ([ctypes.c_longlong, vp, vp], i32),
             "pa_decode_shared_prefix": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, i32, i32,
                                          ctypes.c_float, vp, sz, vp], i32),
         }
@@ -251,6 +252,14 @@ def pa_decode_shared_prefix(out, query, k_cache, v_cache, block_tables, context_
                                          shared_len.data_ptr(), B, hq, hkv, d, bs, nb, block_tables.shape[1],
                                          int(max_context_len), float(scale), workspace.data_ptr(), workspace.numel(),
                                          _stream(stream)), "pa_decode_shared_prefix")
+
+
+def pa_selftest_wait_timeout(limit_cycles: int, status, stream=None):
+    """Run the bounded-wait self-test; `status` is an int32 CUDA tensor of one element."""
+    import torch
+    _need(status, torch.int32, 1, "status")
+    _check(lib().pa_selftest_wait_timeout(int(limit_cycles), status.data_ptr(), _stream(stream)),
+           "pa_selftest_wait_timeout")
 
 
 def pa_workspace_status(workspace, stream=None) -> int:

@@ -43,6 +43,7 @@
 #include <cudaTypedefs.h>
 
 #include <cmath>
+#include <cstdlib>
 #include <mutex>
 #include <vector>
 
@@ -67,7 +68,7 @@ constexpr int CHUNK = 16;                       // tokens per pipeline stage (on
 constexpr int NC = PA_DECODE_CONSUMERS;         // consumer warps per CTA
 constexpr int DEPTH = PA_DECODE_DEPTH;          // pipeline stages per consumer
 constexpr int NWARPS = NC + 1;                  // + the producer warp
-constexpr long long WAIT_LIMIT = 1LL << 31;     // clock cycles (about a second)
+constexpr long long WAIT_LIMIT = 1LL << 31;     // clock cycles (about a second): default wait bound, drain bound
 constexpr int PREP_THREADS = 1024;
 constexpr float RESCALE_THRESHOLD = 8.f;        // log2 units: rescale when the max grows by more than 2^8
 constexpr int ENTRIES = MAX_PART_TOKENS / 8 / 32;   // block-table entries per lane for one item (block size >= 8)
@@ -145,6 +146,7 @@ struct DecodeArgs {
     const int32_t *context_lens;
     int Hq, Hkv, G, bs, mbps, pt, ms;
     long long num_blocks;
+    long long wait_limit;   // bound of every pipeline wait, clock cycles
     float scale_log2;
     WsHeader *hdr;
     const int *part_off;
@@ -450,6 +452,21 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
         for (int e = 0; e < ENTRIES; ++e) y[c][e] = 0;
         done[c] = bad[c] = false;
     }
+    // Before the producer leaves, every copy it issued has landed: only the
+    // last issue into each ring slot can still be in flight (an earlier one
+    // was consumed before its slot was reused), so wait for those, bounded
+    // independently of the pipeline's own wait bound.
+    auto drain = [&]() {
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+            const ConsumerSmem cs = consumer_smem<D, NT>(smem, c);
+            for (int slot = 0; slot < DEPTH; ++slot)
+                if (sc[c] > slot) {
+                    const int k = slot + (sc[c] - 1 - slot) / DEPTH * DEPTH;
+                    mbar_wait_bounded(smem_u32(&cs.full[slot]), (uint32_t)((k / DEPTH) & 1), WAIT_LIMIT);
+                }
+        }
+    };
     if (lane == 0) raw = atomicAdd(&a.hdr->counter, 1);
     advance();
     advance();
@@ -461,11 +478,11 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
             const ConsumerSmem cs = consumer_smem<D, NT>(smem, c);
             const int s = sc[c] % DEPTH;
             const uint32_t full = smem_u32(&cs.full[s]);
-            bool ok = mbar_wait_bounded(smem_u32(&cs.empty[s]), ((sc[c] / DEPTH) & 1) ^ 1, WAIT_LIMIT);
+            bool ok = mbar_wait_bounded(smem_u32(&cs.empty[s]), ((sc[c] / DEPTH) & 1) ^ 1, a.wait_limit);
             bool first = false;
             if (ok && chunk[c] == nch[c]) {          // the consumer needs its next item
                 const int q = ic[c] & 1;
-                ok = mbar_wait_bounded(smem_u32(&cs.qfree[q]), ((ic[c] >> 1) & 1) ^ 1, WAIT_LIMIT);
+                ok = mbar_wait_bounded(smem_u32(&cs.qfree[q]), ((ic[c] >> 1) & 1) ^ 1, a.wait_limit);
                 if (ok && n_item < 0) {              // nothing left: tell the consumer to stop
                     if (lane == 0) {
                         ItemDesc e;
@@ -476,6 +493,7 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
                         cs.desc[q] = e;
                         mbar_arrive(full);
                     }
+                    ++sc[c];   // the end marker is this slot's last phase (no copies)
                     done[c] = true;
                     --live;
                     continue;
@@ -520,6 +538,7 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
             }
             if (!ok) {   // a consumer stopped answering: record it and stop feeding everyone
                 if (lane == 0) atomicExch(&a.hdr->error, PA_ERR_TIMEOUT);
+                drain();
                 return;
             }
             // issue chunk `chunk[c]` of the consumer's item into stage s
@@ -567,6 +586,7 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
             ++sc[c];
         }
     }
+    drain();
 }
 
 // Log-sum-exp merge of the P partitions of one (sequence, kv head) group,
@@ -728,9 +748,9 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
     for (int item = 0;; ++item) {
         const int q = item & 1;
         int s = stage % DEPTH;
-        if (!mbar_wait_bounded(smem_u32(&cs.full[s]), (stage / DEPTH) & 1, WAIT_LIMIT)) {
+        if (!mbar_wait_bounded(smem_u32(&cs.full[s]), (stage / DEPTH) & 1, a.wait_limit)) {
             if (lane == 0) atomicExch(&a.hdr->error, PA_ERR_TIMEOUT);
-            return;
+            return;   // the producer drains the copies in flight before the CTA ends
         }
         // the descriptor stays in shared memory for the whole item (its slot is
         // released at the item's end); only the chunk count lives in registers
@@ -770,9 +790,9 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
         for (int ch = 0; ch < nchunks; ++ch) {
             if (ch > 0) {
                 s = stage % DEPTH;
-                if (!mbar_wait_bounded(smem_u32(&cs.full[s]), (stage / DEPTH) & 1, WAIT_LIMIT)) {
+                if (!mbar_wait_bounded(smem_u32(&cs.full[s]), (stage / DEPTH) & 1, a.wait_limit)) {
                     if (lane == 0) atomicExch(&a.hdr->error, PA_ERR_TIMEOUT);
-                    return;
+                    return;   // the producer drains the copies in flight before the CTA ends
                 }
             }
             const uint32_t kt = cs.data + s * C::STAGE;
@@ -1048,6 +1068,18 @@ using namespace pa;
 namespace pa {
 namespace {
 
+// Bound of the kernel's pipeline waits: about a second, or the value of
+// PA_WAIT_LIMIT_CYCLES (read once) -- a small value makes the waits give up,
+// which is how the timeout path is tested without a fault or a hang.
+long long wait_limit_cycles() {
+    static const long long v = [] {
+        const char *e = std::getenv("PA_WAIT_LIMIT_CYCLES");
+        const long long x = e ? std::atoll(e) : 0;
+        return x > 0 ? x : WAIT_LIMIT;
+    }();
+    return v;
+}
+
 // One decode call; lead/shared_len are null for pa_decode.
 int decode_impl(uint16_t *out, const uint16_t *query, const uint16_t *k_cache, const uint16_t *v_cache,
                 const int32_t *block_tables, const int32_t *context_lens, const int32_t *lead,
@@ -1151,6 +1183,7 @@ int decode_impl(uint16_t *out, const uint16_t *query, const uint16_t *k_cache, c
     args.pt = L.pt;
     args.ms = ms;
     args.num_blocks = num_blocks;
+    args.wait_limit = wait_limit_cycles();
     args.scale_log2 = scale * 1.4426950408889634f;
     args.hdr = hdr;
     args.part_off = part_off;
@@ -1212,6 +1245,33 @@ extern "C" int pa_decode_shared_prefix(uint16_t *out, const uint16_t *query, con
     return decode_impl(out, query, k_cache, v_cache, block_tables, context_lens, group_leader, shared_len, num_seqs,
                        num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len,
                        scale, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------ failure-detection self-test
+
+namespace pa {
+namespace {
+
+// Waits, with the decode pipeline's bounded wait, on an mbarrier that nothing
+// ever completes; the wait must give up after `limit` cycles.
+__global__ void selftest_wait_kernel(long long limit, int *status) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait_bounded(smem_u32(&bar), 0, limit);
+    if (threadIdx.x == 0) *status = ok ? PA_OK : PA_ERR_TIMEOUT;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" int pa_selftest_wait_timeout(long long limit_cycles, int *status_device, void *stream) {
+    if (!status_device || limit_cycles <= 0 || limit_cycles > WAIT_LIMIT) return PA_ERR_INVALID_ARG;
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_cycles, status_device);
+    return cuda_status(cudaGetLastError());
 }
 
 // ------------------------------------------------ decode without allocation

@@ -152,3 +152,23 @@ def test_debug_validation_mode_reports_bad_indices():
     codes = [int(x) for x in res.stdout.split()]
     E = pa.PA_ERR_INVALID_ARG
     assert codes == [E, E, 0, E, E, 0, E, 0, E, 0]
+
+
+def test_bounded_wait_gives_up_and_context_survives():
+    """The decode pipeline's waits are bounded.  The self-test runs that same
+    bounded wait on a barrier nothing completes: it must give up, report
+    PA_ERR_TIMEOUT, and leave the context usable -- no fault and no hang."""
+    import time
+    status = torch.full((1,), 12345, dtype=torch.int32, device="cuda")
+    t0 = time.time()
+    pa.pa_selftest_wait_timeout(2_000_000, status)      # ~1 ms at 2 GHz
+    torch.cuda.synchronize()
+    assert int(status.item()) == pa.PA_ERR_TIMEOUT and time.time() - t0 < 10
+    # the context works on: a decode afterwards is correct and reports no error
+    w = workloads.make("tiny")
+    st = Step(w)
+    d = st.upload(torch)
+    st.run_library(d)
+    torch.cuda.synchronize()
+    assert pa.pa_workspace_status(d["ws"]) == pa.PA_OK
+    compare(d["out"].cpu().numpy(), st.oracle_out(*st.oracle_caches()))
