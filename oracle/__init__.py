@@ -27,6 +27,9 @@ Contents, each with the passage it follows:
   finds a shared block copies it first (deepsonar page section 2.3).
 * ``paged_decode`` / ``paged_decode_split`` -- fp64 attention over the gathered
   history, in C (``oracle.c``), see that file's header for the passages.
+* ``paged_attention_causal`` -- several new query tokens per sequence, each
+  attending causally to the positions up to its own (deepsonar page section
+  2.5: chunked prefill and speculative tokens), in C.
 
 Readings where the pages are silent are listed with each function.
 """
@@ -75,6 +78,9 @@ def _load():
             lib.or_paged_decode.restype = i32
             lib.or_paged_decode_split.argtypes = common + [i32, i32, i32]
             lib.or_paged_decode_split.restype = i32
+            lib.or_paged_attention_causal.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                                      i64, i64, i64, dbl, i32, i32]
+            lib.or_paged_attention_causal.restype = i32
             _lib = lib
     return _lib
 
@@ -456,3 +462,40 @@ def paged_decode_split(query, k_cache, v_cache, block_tables, context_lens, num_
     """fp64 split-context decode with the log-sum-exp merge (see oracle.c)."""
     return _decode_call(int(partition_tokens), query, k_cache, v_cache, block_tables, context_lens,
                         num_kv_heads, block_size, scale, threads, seq_range)
+
+
+def paged_attention_causal(query, k_cache, v_cache, block_tables, context_lens, query_start, num_kv_heads,
+                           block_size, scale, threads=None):
+    """fp64 causal attention of query rows [num_query_tokens, Hq, D]: sequence
+    i owns rows query_start[i] .. query_start[i+1] - 1, its last T_i context
+    positions; row j of it sees positions 0 .. L_i - T_i + j."""
+    lib = _load()
+    q = np.ascontiguousarray(query).view(np.uint16)
+    nq, num_heads, head_dim = q.shape
+    kc = np.asarray(k_cache).view(np.uint16)
+    vc = np.asarray(v_cache).view(np.uint16)
+    if kc.ndim != 4 or kc.strides != vc.strides or kc.strides[3] != 2:
+        raise ValueError("caches must be 4-d [block, kv_head, offset, dim] views with a unit-stride dim")
+    sb, sh, st = (s // 2 for s in kc.strides[:3])
+    tab = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    qs = np.ascontiguousarray(query_start, dtype=np.int32)
+    B = len(lens)
+    if len(qs) != B + 1 or qs[-1] != nq:
+        raise ValueError("query_start must have num_seqs + 1 entries ending at the query row count")
+    out = np.zeros((nq, num_heads, head_dim), dtype=np.float64)
+    kptr = kc.__array_interface__["data"][0]
+    vptr = vc.__array_interface__["data"][0]
+    threads = max(1, min(threads or default_threads(), B))
+
+    def run(a, b):
+        rc = lib.or_paged_attention_causal(out.ctypes.data, q.ctypes.data, kptr, vptr, tab.ctypes.data,
+                                           lens.ctypes.data, qs.ctypes.data, B, num_heads, num_kv_heads, head_dim,
+                                           block_size, tab.shape[1], sb, sh, st, float(scale), a, b)
+        if rc != 0:
+            raise RuntimeError("oracle causal attention failed")
+
+    bounds = np.linspace(0, B, threads + 1).astype(int)
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda ab: run(*ab), zip(bounds[:-1], bounds[1:])))
+    return out

@@ -269,3 +269,86 @@ int or_paged_decode_split(double *out, const uint16_t *query,
     }
     return 0;
 }
+
+/* Paged attention for several new query tokens per sequence, causal within
+ * the new chunk (chunked prefill or speculative tokens over the paged cache;
+ * "PagedAttention de vLLM", deepsonar.com.cn, section 2.5: a request may have
+ * several tokens computed in one step -- chunked prefill, speculative
+ * tokens).  Sequence i has T_i = query_start[i+1] - query_start[i] new
+ * tokens, which are the last T_i of its L_i = context_lens[i] positions.
+ * Query token j of sequence i (row query_start[i] + j of query and out)
+ * attends to positions t <= L_i - T_i + j:
+ *   s_t = scale * <q, K_t[g]>,  out = sum_t softmax(s)_t V_t[g].
+ * out: double [num_query_tokens][num_heads][head_dim].  Sequences with
+ * T_i = 0 have no rows.  Returns 0, or -1 on a bad argument. */
+int or_paged_attention_causal(double *out, const uint16_t *query,
+                              const uint16_t *k_cache, const uint16_t *v_cache,
+                              const int32_t *block_tables, const int32_t *context_lens,
+                              const int32_t *query_start,
+                              int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                              int block_size, int max_blocks_per_seq,
+                              int64_t stride_block, int64_t stride_head, int64_t stride_token,
+                              double scale, int seq_begin, int seq_end)
+{
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        block_size <= 0 || seq_begin < 0 || seq_end > num_seqs)
+        return -1;
+    int group = num_heads / num_kv_heads;
+    for (int i = seq_begin; i < seq_end; ++i) {
+        int L = context_lens[i];
+        int T = query_start[i + 1] - query_start[i];
+        if (T <= 0)
+            continue;
+        if (T > L)
+            return -1;
+        size_t n = (size_t)L * num_kv_heads * head_dim;
+        double *K = (double *)malloc(n * sizeof(double));
+        double *V = (double *)malloc(n * sizeof(double));
+        double *s = (double *)malloc((size_t)L * sizeof(double));
+        double *q = (double *)malloc((size_t)head_dim * sizeof(double));
+        if (!K || !V || !s || !q) {
+            free(K); free(V); free(s); free(q);
+            return -1;
+        }
+        gather_sequence(K, V, k_cache, v_cache,
+                        block_tables + (int64_t)i * max_blocks_per_seq, 0, L,
+                        num_kv_heads, head_dim, block_size,
+                        stride_block, stride_head, stride_token);
+        for (int j = 0; j < T; ++j) {
+            int visible = L - T + j + 1;     /* positions 0 .. L - T + j */
+            int64_t row = query_start[i] + j;
+            for (int h = 0; h < num_heads; ++h) {
+                int g = h / group;
+                const uint16_t *qh = query + (row * num_heads + h) * head_dim;
+                for (int d = 0; d < head_dim; ++d)
+                    q[d] = or_half_to_double(qh[d]);
+                double m = -INFINITY;
+                for (int t = 0; t < visible; ++t) {
+                    const double *k = K + ((int64_t)t * num_kv_heads + g) * head_dim;
+                    double dot = 0.0;
+                    for (int d = 0; d < head_dim; ++d)
+                        dot += q[d] * k[d];
+                    s[t] = scale * dot;
+                    if (s[t] > m)
+                        m = s[t];
+                }
+                double z = 0.0;
+                for (int t = 0; t < visible; ++t) {
+                    s[t] = exp(s[t] - m);
+                    z += s[t];
+                }
+                double *o = out + (row * num_heads + h) * head_dim;
+                for (int d = 0; d < head_dim; ++d)
+                    o[d] = 0.0;
+                for (int t = 0; t < visible; ++t) {
+                    double p = s[t] / z;
+                    const double *v = V + ((int64_t)t * num_kv_heads + g) * head_dim;
+                    for (int d = 0; d < head_dim; ++d)
+                        o[d] += p * v[d];
+                }
+            }
+        }
+        free(K); free(V); free(s); free(q);
+    }
+    return 0;
+}

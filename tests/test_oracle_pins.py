@@ -10,7 +10,9 @@ the oracle's own code.  CPU only.
   block size or the cache layout changes;
 * closed forms: one token gives its V row; a zero query or identical keys give
   the mean of V; a score boosted by 64 selects its V row; zero length gives 0;
-* the split-context form with the log-sum-exp merge equals the unsplit form.
+* the split-context form with the log-sum-exp merge equals the unsplit form;
+* the multi-token causal form equals a masked brute force and, with one token
+  per sequence, the decode.
 """
 import json
 import math
@@ -258,3 +260,34 @@ def test_kv_write_and_block_copy_by_hand():
     k3, v3 = oracle.block_copy(kc, vc, [(0, 2), (0, 1)])
     assert np.array_equal(k3[1], kc[0]) and np.array_equal(k3[2], kc[0]) and np.array_equal(k3[0], kc[0])
     assert np.array_equal(v3[2], vc[0])
+
+
+def test_causal_attention_pins():
+    """Multi-token causal attention: one query token per sequence is the
+    decode; several equal a brute force with the causal mask over contiguous
+    arrays; the last query token of a chunk sees the whole context."""
+    H, Hkv, D, bs = 8, 2, 64, 16
+    lens = [1, 40, 97, 130, 16]
+    T = [1, 3, 7, 0, 16]
+    q_all, Ks, Vs = make_case(lens, H, Hkv, D)
+    kc, vc, tab, ln = page_sequences(Ks, Vs, bs, RNG)
+    qs = np.concatenate([[0], np.cumsum(T)]).astype(np.int32)
+    query = rand_fp16(int(qs[-1]), H, D)
+    scale = 0.125
+    got = oracle.paged_attention_causal(query, kc, vc, tab, ln, qs, Hkv, bs, scale, threads=2)
+    for i, (L, t) in enumerate(zip(lens, T)):
+        K = Ks[i].astype(np.float64)
+        V = Vs[i].astype(np.float64)
+        for j in range(t):
+            visible = L - t + j + 1
+            for h in range(H):
+                s = scale * (K[:visible, h // 4, :] @ query[qs[i] + j, h].astype(np.float64))
+                p = np.exp(s - s.max())
+                p /= p.sum()
+                assert np.max(np.abs(got[qs[i] + j, h] - p @ V[:visible, h // 4, :])) < 1e-12
+    # one token per sequence: exactly the decode oracle
+    qs1 = np.arange(len(lens) + 1, dtype=np.int32)
+    q1 = rand_fp16(len(lens), H, D)
+    a = oracle.paged_attention_causal(q1, kc, vc, tab, ln, qs1, Hkv, bs, scale)
+    b = oracle.paged_decode(q1, kc, vc, tab, ln, Hkv, bs, scale)
+    assert np.array_equal(a, b)
