@@ -198,6 +198,42 @@ PA_API int pa_decode_shared_prefix(uint16_t *out, const uint16_t *query, const u
                                    int max_context_len, float scale, void *workspace, size_t workspace_bytes,
                                    void *stream);
 
+/* --------------------------------- several new tokens per sequence (causal) */
+
+/* Workspace bytes pa_attention_causal needs (a host-side bound). */
+PA_API size_t pa_attention_causal_workspace_size(int num_seqs, int num_query_tokens, int num_heads,
+                                                 int num_kv_heads, int head_dim, int max_context_len);
+
+/* Attention for a step in which a sequence computes several new tokens at
+ * once: a chunk of a long prompt (chunked prefill), the rest of a prompt after
+ * a prefix-cache hit, or speculative candidate tokens (deepsonar page section
+ * 2.5: the scheduler gives each request a token budget per step).  The new
+ * tokens' K and V are already in the cache (pa_kv_write), so sequence i has
+ * L = context_lens[i] positions, the last T = query_start[i + 1] -
+ * query_start[i] of them new.  New token j (0 <= j < T) is query row
+ * query_start[i] + j and attends causally to positions t <= L - T + j:
+ *   s_t = scale * <query[row][h], K_t[g]>,  out[row][h] = sum_t softmax(s)_t V_t[g],
+ * gather, GQA grouping, partitions, merge and arithmetic as in pa_decode.
+ * One token per sequence (query_start = 0, 1, ..., num_seqs) is the decode.
+ *
+ *   out, query     fp16 [num_query_tokens][num_heads][head_dim]
+ *   query_start    int32 [num_seqs + 1], device: 0 = query_start[0] <= ...
+ *                  <= query_start[num_seqs] = num_query_tokens (T = 0 allowed)
+ *   num_query_tokens  host-side row count of query and out
+ *   other arguments as in pa_decode.
+ * Up to 16 / G new tokens of a sequence are reduced together, so a KV tile is
+ * read once for that many tokens' query rows.  Device-side cases: a
+ * sequence with T > L or an invalid L (as in pa_decode) gets NaN rows; a
+ * query_start that is not a non-decreasing cover of [0, num_query_tokens)
+ * makes every row NaN.  num_query_tokens = 0 launches nothing.  Workspace:
+ * pa_attention_causal_workspace_size, 256-byte aligned.  Deterministic. */
+PA_API int pa_attention_causal(uint16_t *out, const uint16_t *query, const uint16_t *k_cache,
+                               const uint16_t *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                               const int32_t *query_start, int num_seqs, int num_query_tokens, int num_heads,
+                               int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                               int max_blocks_per_seq, int max_context_len, float scale, void *workspace,
+                               size_t workspace_bytes, void *stream);
+
 /* Read the error word a pa_decode call left in its workspace: PA_OK, or
  * PA_ERR_TIMEOUT if a kernel gave up waiting for its own copies into shared
  * memory (the affected outputs are NaN).  Synchronises `stream`. */

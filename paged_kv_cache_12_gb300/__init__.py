@@ -40,6 +40,7 @@ EXPORTS = (
     "pa_alloc_stats", "pa_decode_static_ws", "pa_alloc_free_queue", "pa_alloc_enable_prefix_cache",
     "pa_alloc_match_prefix", "pa_alloc_append_ids", "pa_alloc_block_hash", "pa_alloc_prefix_stats", "pa_sha256",
     "pa_decode_shared_prefix_workspace_size", "pa_decode_shared_prefix", "pa_selftest_wait_timeout",
+    "pa_attention_causal_workspace_size", "pa_attention_causal",
 )
 
 # bytes of the library's built-in scratch array used by pa_decode_static_ws
@@ -99,6 +100,9 @@ def lib():
             "pa_selftest_wait_timeout": ([ctypes.c_longlong, vp, vp], i32),
             "pa_decode_shared_prefix": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, i32, i32,
                                          ctypes.c_float, vp, sz, vp], i32),
+            "pa_attention_causal_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
+            "pa_attention_causal": ([vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i64, i32, i32,
+                                     ctypes.c_float, vp, sz, vp], i32),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -252,6 +256,38 @@ def pa_decode_shared_prefix(out, query, k_cache, v_cache, block_tables, context_
                                          shared_len.data_ptr(), B, hq, hkv, d, bs, nb, block_tables.shape[1],
                                          int(max_context_len), float(scale), workspace.data_ptr(), workspace.numel(),
                                          _stream(stream)), "pa_decode_shared_prefix")
+
+
+def pa_attention_causal_workspace_size(num_seqs, num_query_tokens, num_heads, num_kv_heads, head_dim,
+                                       max_context_len) -> int:
+    n = lib().pa_attention_causal_workspace_size(int(num_seqs), int(num_query_tokens), int(num_heads),
+                                                 int(num_kv_heads), int(head_dim), int(max_context_len))
+    if n == 0:
+        raise PAError(PA_ERR_INVALID_ARG, "pa_attention_causal_workspace_size")
+    return n
+
+
+def pa_attention_causal(out, query, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+                        max_context_len, workspace, stream=None):
+    """Several new tokens per sequence (chunked prefill, speculative tokens):
+    query rows query_start[i] .. query_start[i+1]-1 are sequence i's last new
+    tokens, each attending to the positions up to its own."""
+    import torch
+    for t, dt, nd, nm in ((out, torch.float16, 3, "out"), (query, torch.float16, 3, "query"),
+                          (k_cache, torch.float16, 4, "k_cache"), (v_cache, torch.float16, 4, "v_cache"),
+                          (block_tables, torch.int32, 2, "block_tables"), (context_lens, torch.int32, 1, "context_lens"),
+                          (query_start, torch.int32, 1, "query_start"), (workspace, torch.uint8, 1, "workspace")):
+        _need(t, dt, nd, nm)
+    nb, hkv, bs, d = k_cache.shape
+    nq, hq, d2 = query.shape
+    B = context_lens.shape[0]
+    if out.shape != query.shape or d2 != d or v_cache.shape != k_cache.shape or block_tables.shape[0] != B \
+            or query_start.shape[0] != B + 1:
+        raise ValueError("pa_attention_causal: shape mismatch")
+    _check(lib().pa_attention_causal(out.data_ptr(), query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                     block_tables.data_ptr(), context_lens.data_ptr(), query_start.data_ptr(), B, nq,
+                                     hq, hkv, d, bs, nb, block_tables.shape[1], int(max_context_len), float(scale),
+                                     workspace.data_ptr(), workspace.numel(), _stream(stream)), "pa_attention_causal")
 
 
 def pa_selftest_wait_timeout(limit_cycles: int, status, stream=None):

@@ -128,6 +128,37 @@ WsLayout ws_layout(int B, int Hq, int Hkv, int D, int max_ctx, bool grouped) {
     return w;
 }
 
+// Workspace of one call of the multi-token (causal) form: NQ query rows of B
+// sequences; per row its visible length and partial-row offset, per sequence
+// the first of its member groups (ms consecutive rows read together), and a
+// partial row per (query row, partition).
+WsLayout ws_layout_causal(int B, int NQ, int Hq, int Hkv, int D, int max_ctx) {
+    WsLayout w;
+    const int G = Hq / Hkv;
+    const int ms = 16 / G > 1 ? 16 / G : 1;
+    w.pt = part_tokens(B, Hkv, max_ctx);
+    w.pmax = max_ctx > 0 ? (max_ctx + w.pt - 1) / w.pt : 1;
+    w.item_cap = (long long)w.pmax * ((NQ + ms - 1) / ms + B);
+    const long long parts = (long long)NQ * w.pmax;
+    size_t off = sizeof(WsHeader);
+    w.part_off = off;
+    off += up256(sizeof(int) * ((size_t)NQ + 1));
+    w.gsize = off;   // visible length of every query row
+    off += up256(sizeof(int) * ((size_t)NQ + 1));
+    w.gshared = off;   // first member group of every sequence
+    off += up256(sizeof(int) * ((size_t)B + 1));
+    w.items = off;
+    off += up256(2 * sizeof(int4) * (size_t)w.item_cap);
+    w.grp = off;
+    off += up256(sizeof(int) * ((size_t)NQ + 1) * Hkv);
+    w.ml = off;
+    off += up256(sizeof(float2) * (size_t)parts * Hq);
+    w.o = off;
+    off += up256(sizeof(float) * (size_t)parts * Hq * D);
+    w.total = off;
+    return w;
+}
+
 // A work item record (two int4): a token range [t0, t1) of the caches read
 // for nmem consecutive sequences seq0 .. seq0 + nmem - 1 that share those
 // blocks, the range's partition index in each member's partition list, the
@@ -159,7 +190,7 @@ struct DecodeArgs {
 // What the producer tells a consumer about its next item (64 bytes).
 struct ItemDesc {
     int seq0, kvh, nmem, pidx, shared, P0, canon0, nchunks;
-    int ntok_last, bad, end, pad[5];
+    int ntok_last, bad, end, t0, pad[4];
 };
 
 template <int D, int NT>
@@ -380,6 +411,153 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
     }
 }
 
+// Index of the last entry of the non-decreasing array a[0 .. n] that is <= x
+// (a[0] <= x < a[n]): the sequence a query row or member group belongs to.
+__device__ __forceinline__ int last_le(const int32_t *a, int n, int x) {
+    int lo = 0, hi = n;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (a[mid] <= x)   // plain load: the group offsets are written by the same kernel
+            lo = mid;
+        else
+            hi = mid;
+    }
+    return lo;
+}
+
+// Work list of the multi-token form.  Sequence i computes T_i new tokens in
+// one step (a chunk of its prompt, or speculative tokens: "PagedAttention de
+// vLLM", section 2.5); they are the last T_i of its L_i positions and are
+// query rows query_start[i] + j, row j seeing positions [0, L_i - T_i + j].
+// Rows are cut into member groups of ms consecutive rows of one sequence; a
+// group's items are the partitions [p pt, (p + 1) pt) of the range its last
+// member sees, each for the group's members that see the partition's first
+// token (so every member of an item sees at least one of its tokens).  A row
+// sees ceil(vis / pt) partitions, stored at part_off[row] + p.  Items of full
+// length first, every group's last item after them by decreasing length, as
+// in the single-token form.  A sequence whose lengths are inconsistent gets
+// NaN rows; a query_start that is not a non-decreasing cover of [0, NQ) makes
+// every row NaN.
+__global__ void __launch_bounds__(PREP_THREADS) causal_prep_kernel(
+    const int32_t *__restrict__ context_lens, const int32_t *__restrict__ qs, int B, int NQ, int Hq, int D, int Hkv,
+    int max_ctx, long long max_table_tokens, int pt, int ms, WsHeader *hdr, int *part_off, int *vlen, int *gstart,
+    ItemRec *items, int *grp, __half *out) {
+    constexpr int NBK = MAX_PART_TOKENS / CHUNK;
+    __shared__ int warp_sums[PREP_THREADS / 32];
+    __shared__ int hist[NBK], cursor[NBK];
+    for (int k = threadIdx.x; k < NBK; k += PREP_THREADS) hist[k] = cursor[k] = 0;
+    for (long long k = threadIdx.x; k < (long long)NQ * Hkv; k += PREP_THREADS) grp[k] = 0;
+    bool ok = true;
+    for (int i = threadIdx.x; i <= B; i += PREP_THREADS) {
+        const int x = qs[i];
+        ok = ok && (i > 0 || x == 0) && (i < B || x == NQ) && (i == B || x <= qs[i + 1]);
+    }
+    const bool qs_ok = __syncthreads_and(ok) != 0;
+    auto seq_ok = [&](int i, int &L, int &T) {
+        L = context_lens[i];
+        T = qs[i + 1] - qs[i];
+        return L >= 0 && L <= max_ctx && (long long)L <= max_table_tokens && T <= L;
+    };
+    // pass 1: visible length and partial-row offset of every query row
+    int run = 0;
+    for (int base = 0; base < NQ; base += PREP_THREADS) {
+        const int v = base + threadIdx.x;
+        int vl = -1;
+        if (v < NQ && qs_ok) {
+            const int i = last_le(qs, B, v);
+            int L, T;
+            if (seq_ok(i, L, T)) vl = L - T + (v - qs[i]) + 1;
+        }
+        int tot;
+        const int e = run + block_exclusive_scan(vl > 0 ? (vl + pt - 1) / pt : 0, warp_sums, &tot);
+        if (v < NQ) {
+            vlen[v] = vl;
+            part_off[v] = e;
+            if (vl < 0) {
+                uint4 fill = make_uint4(0x7e007e00u, 0x7e007e00u, 0x7e007e00u, 0x7e007e00u);
+                uint4 *row = reinterpret_cast<uint4 *>(out + (long long)v * Hq * D);
+                for (int k = 0; k < Hq * D / 8; ++k) row[k] = fill;
+            }
+        }
+        run += tot;
+    }
+    // pass 2: member groups per sequence
+    int run_g = 0;
+    for (int base = 0; base < B; base += PREP_THREADS) {
+        const int i = base + threadIdx.x;
+        int n = 0, L, T;
+        if (i < B && qs_ok && seq_ok(i, L, T)) n = (T + ms - 1) / ms;
+        int tot;
+        const int e = run_g + block_exclusive_scan(n, warp_sums, &tot);
+        if (i < B) gstart[i] = e;
+        run_g += tot;
+    }
+    if (threadIdx.x == 0) {
+        gstart[B] = run_g;
+        part_off[NQ] = run;
+    }
+    __syncthreads();
+    const int NG = run_g;
+    // group g: rows [r0 + jl, r0 + jh) of sequence i; C = L - T + 1 positions
+    // seen by its first new token; the last member sees vis positions
+    auto group = [&](int g, int &r0, int &jl, int &jh, int &C, int &vis, int &np, int &i) {
+        i = last_le(gstart, B, g);
+        const int L = context_lens[i];
+        r0 = qs[i];
+        const int T = qs[i + 1] - r0;
+        jl = (g - gstart[i]) * ms;
+        jh = min(jl + ms, T);
+        C = L - T + 1;
+        vis = C + jh - 1;
+        np = (vis + pt - 1) / pt;
+    };
+    // pass 3: full-length items, and a histogram of every group's last item
+    int run_f = 0;
+    for (int base = 0; base < NG; base += PREP_THREADS) {
+        const int g = base + threadIdx.x;
+        int r0 = 0, jl = 0, jh = 0, C = 0, vis = 0, np = 0, i = 0;
+        if (g < NG) group(g, r0, jl, jh, C, vis, np, i);
+        int tot;
+        int ef = run_f + block_exclusive_scan(g < NG ? np - 1 : 0, warp_sums, &tot);
+        if (g < NG) {
+            for (int p = 0; p + 1 < np; ++p) {
+                const int t0 = p * pt, j0 = max(jl, t0 - C + 1);
+                ItemRec r;
+                r.a = make_int4(r0 + j0, jh - j0, t0, t0 + pt);
+                r.b = make_int4(p, 0, i, -1);
+                items[ef++] = r;
+            }
+            atomicAdd(&hist[(pt - (vis - (np - 1) * pt)) / CHUNK], 1);
+        }
+        run_f += tot;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int acc = run_f;
+        for (int k = 0; k < pt / CHUNK; ++k) {
+            cursor[k] = acc;
+            acc += hist[k];
+        }
+    }
+    __syncthreads();
+    // pass 4: every group's last item, longest first
+    for (int g = threadIdx.x; g < NG; g += PREP_THREADS) {
+        int r0, jl, jh, C, vis, np, i;
+        group(g, r0, jl, jh, C, vis, np, i);
+        const int p = np - 1, t0 = p * pt, j0 = max(jl, t0 - C + 1);
+        ItemRec r;
+        r.a = make_int4(r0 + j0, jh - j0, t0, vis);
+        r.b = make_int4(p, 0, i, -1);
+        items[atomicAdd(&cursor[(pt - (vis - t0)) / CHUNK], 1)] = r;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        hdr->total_items = cursor[pt / CHUNK - 1] * Hkv;
+        hdr->counter = 0;
+        hdr->error = 0;
+    }
+}
+
 // ------------------------------------------------------------ decode
 
 struct ConsumerSmem {
@@ -405,7 +583,7 @@ __device__ __forceinline__ ConsumerSmem consumer_smem(uint8_t *smem, int c) {
 
 // Producer warp: hands items to the consumers round-robin and keeps their
 // rings full.  All lanes run the loop; lane 0 issues the copies.
-template <int D, int NT>
+template <int D, int NT, bool CAUSAL>
 __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMap *tmv, const DecodeArgs &a) {
     using C = Cfg<D, NT>;
     const int lane = threadIdx.x & 31;
@@ -432,7 +610,8 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
             n_rec = nn_rec;
             n_fb = n_rec.a.z / a.bs;
             const int nb = (n_rec.a.w + a.bs - 1) / a.bs - n_fb;
-            const int32_t *row = a.block_tables + (long long)n_rec.a.x * a.mbps + n_fb;
+            const int trow = CAUSAL ? n_rec.b.z : n_rec.a.x;   // block-table row of the item
+            const int32_t *row = a.block_tables + (long long)trow * a.mbps + n_fb;
 #pragma unroll
             for (int e = 0; e < ENTRIES; ++e) n_e[e] = lane + 32 * e < nb ? row[lane + 32 * e] : 0;
         }
@@ -487,9 +666,9 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
                     if (lane == 0) {
                         ItemDesc e;
                         e.seq0 = e.kvh = e.nmem = e.pidx = e.shared = e.P0 = e.canon0 = e.nchunks = 0;
-                        e.ntok_last = e.bad = 0;
+                        e.ntok_last = e.bad = e.t0 = 0;
                         e.end = 1;
-                        e.pad[0] = e.pad[1] = e.pad[2] = e.pad[3] = e.pad[4] = 0;
+                        e.pad[0] = e.pad[1] = e.pad[2] = e.pad[3] = 0;
                         cs.desc[q] = e;
                         mbar_arrive(full);
                     }
@@ -522,13 +701,14 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
                         d.nmem = n_rec.a.y;
                         d.pidx = n_rec.b.x;
                         d.shared = n_rec.b.y;
-                        d.P0 = partitions_of(n_rec.b.z, n_rec.b.y, a.pt);
+                        d.P0 = CAUSAL ? 0 : partitions_of(n_rec.b.z, n_rec.b.y, a.pt);
                         d.canon0 = n_rec.b.w;
                         d.nchunks = nch[c];
                         d.ntok_last = t1[c] - (t0[c] + (nch[c] - 1) * CHUNK);
                         d.bad = bad[c] ? 1 : 0;
                         d.end = 0;
-                        d.pad[0] = d.pad[1] = d.pad[2] = d.pad[3] = d.pad[4] = 0;
+                        d.t0 = t0[c];
+                        d.pad[0] = d.pad[1] = d.pad[2] = d.pad[3] = 0;
                         cs.desc[q] = d;
                     }
                     ++ic[c];
@@ -691,8 +871,10 @@ __device__ void merge_group(const DecodeArgs &a, int seq, int kvh, int P) {
     }
 }
 
-// Consumer warp c: reduces the items its producer hands it.
-template <int D, int NT>
+// Consumer warp c: reduces the items its producer hands it.  CAUSAL: the
+// item's query rows may see different lengths of its token range (several
+// new tokens of one sequence); scores past a row's own position are masked.
+template <int D, int NT, bool CAUSAL>
 __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
     using C = Cfg<D, NT>;
     constexpr int KS = D / 16;     // MMA k-steps of S^T = K Q^T
@@ -775,6 +957,20 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                 }
         }
         const int nchunks = dp->nchunks;
+        // CAUSAL: tokens of the item (from its start) that each column's query
+        // row sees -- at least one, as every member sees the item's first token
+        int lim[NT][2];
+        if constexpr (CAUSAL) {
+            const int len = (nchunks - 1) * CHUNK + dp->ntok_last;
+            const int v0 = dp->seq0, rows = dp->nmem * a.G, it0 = dp->t0;
+#pragma unroll
+            for (int t = 0; t < NT; ++t)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int row = t * 8 + 2 * cq + e;
+                    lim[t][e] = row < rows ? min(len, __ldg(&a.context_lens[v0 + row / a.G]) - it0) : len;
+                }
+        }
 
         // running state per head column (2 * cq, 2 * cq + 1) of each head tile
         float m[NT][2], l[NT][2];
@@ -831,7 +1027,13 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
             for (int t = 0; t < NT; ++t) {
                 float s0 = sa[t][0] + sb[t][0], s1 = sa[t][1] + sb[t][1];   // token r, heads 2cq, 2cq+1
                 float s2 = sa[t][2] + sb[t][2], s3 = sa[t][3] + sb[t][3];   // token r + 8
-                if (tail) {
+                if constexpr (CAUSAL) {
+                    const int tk = ch * CHUNK + r;
+                    s0 = tk < lim[t][0] ? s0 : -INFINITY;
+                    s1 = tk < lim[t][1] ? s1 : -INFINITY;
+                    s2 = tk + 8 < lim[t][0] ? s2 : -INFINITY;
+                    s3 = tk + 8 < lim[t][1] ? s3 : -INFINITY;
+                } else if (tail) {
                     s0 = tok_lo ? s0 : -INFINITY;
                     s1 = tok_lo ? s1 : -INFINITY;
                     s2 = tok_hi ? s2 : -INFINITY;
@@ -956,7 +1158,7 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
     }
 }
 
-template <int D, int NT>
+template <int D, int NT, bool CAUSAL>
 __global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? PA_DECODE_MINB : PA_DECODE_MINB / 2) decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                                              const __grid_constant__ CUtensorMap tmv,
                                                              const DecodeArgs a) {
@@ -977,9 +1179,9 @@ __global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? PA_DECODE_MINB : PA_DEC
     }
     __syncthreads();
     if (warp == 0)
-        producer<D, NT>(smem, &tmk, &tmv, a);
+        producer<D, NT, CAUSAL>(smem, &tmk, &tmv, a);
     else
-        consumer<D, NT>(smem, warp - 1, a);
+        consumer<D, NT, CAUSAL>(smem, warp - 1, a);
 }
 
 // ------------------------------------------------------------ host side
@@ -1034,7 +1236,7 @@ bool cache_tensor_map(CUtensorMap *map, const void *base, long long rows, int D,
     return true;
 }
 
-template <int D, int NT>
+template <int D, int NT, bool CAUSAL>
 int launch_decode(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeArgs &args, long long max_items,
                   cudaStream_t st) {
     using C = Cfg<D, NT>;
@@ -1042,21 +1244,22 @@ int launch_decode(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeAr
     static std::once_flag once;
     static cudaError_t init_err = cudaSuccess;
     std::call_once(once, [] {
-        init_err = cudaFuncSetAttribute(decode_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+        init_err =
+            cudaFuncSetAttribute(decode_kernel<D, NT, CAUSAL>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (init_err != cudaSuccess) return;
         int dev = 0, sms = 0, per_sm = 0;
         init_err = cudaGetDevice(&dev);
         if (init_err == cudaSuccess) init_err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (init_err == cudaSuccess)
-            init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, NT>, NWARPS * 32,
-                                                                     C::SMEM);
+            init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, NT, CAUSAL>,
+                                                                     NWARPS * 32, C::SMEM);
         if (init_err == cudaSuccess) grid = sms * (per_sm > 0 ? per_sm : 1);
     });
     if (init_err != cudaSuccess || grid <= 0) return PA_ERR_CUDA;
     // no more CTAs than there can be items for their consumers
     const long long need = (max_items + NC - 1) / NC;
     const int g = (int)(need < grid ? (need > 0 ? need : 1) : grid);
-    decode_kernel<D, NT><<<g, NWARPS * 32, C::SMEM, st>>>(tmk, tmv, args);
+    decode_kernel<D, NT, CAUSAL><<<g, NWARPS * 32, C::SMEM, st>>>(tmk, tmv, args);
     return cuda_status(cudaGetLastError());
 }
 
@@ -1193,10 +1396,109 @@ int decode_impl(uint16_t *out, const uint16_t *query, const uint16_t *k_cache, c
     args.ws_o = ws_o;
     const long long max_items = L.item_cap * num_kv_heads;
     if (head_dim == 128)
-        return NT == 1 ? launch_decode<128, 1>(tmk, tmv, args, max_items, st)
-                       : launch_decode<128, 2>(tmk, tmv, args, max_items, st);
-    return NT == 1 ? launch_decode<64, 1>(tmk, tmv, args, max_items, st)
-                   : launch_decode<64, 2>(tmk, tmv, args, max_items, st);
+        return NT == 1 ? launch_decode<128, 1, false>(tmk, tmv, args, max_items, st)
+                       : launch_decode<128, 2, false>(tmk, tmv, args, max_items, st);
+    return NT == 1 ? launch_decode<64, 1, false>(tmk, tmv, args, max_items, st)
+                   : launch_decode<64, 2, false>(tmk, tmv, args, max_items, st);
+}
+
+// One multi-token (causal) call.
+int causal_impl(uint16_t *out, const uint16_t *query, const uint16_t *k_cache, const uint16_t *v_cache,
+                const int32_t *block_tables, const int32_t *context_lens, const int32_t *query_start, int num_seqs,
+                int num_query_tokens, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                int64_t num_blocks, int max_blocks_per_seq, int max_context_len, float scale, void *workspace,
+                size_t workspace_bytes, cudaStream_t st) {
+    if (num_seqs < 0 || num_query_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        num_heads % num_kv_heads != 0 || max_context_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 ||
+        !std::isfinite(scale) || !(scale > 0.f))
+        return PA_ERR_INVALID_ARG;
+    const int G = num_heads / num_kv_heads;
+    if ((head_dim != 64 && head_dim != 128) || (block_size != 8 && block_size != 16 && block_size != 32) || G > 16)
+        return PA_ERR_UNSUPPORTED;
+    if (num_query_tokens == 0) return PA_OK;
+    if (num_seqs == 0) return PA_ERR_INVALID_ARG;
+    if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens || !query_start)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    const long long rows = (long long)num_blocks * num_kv_heads * block_size;
+    if (rows >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
+    const WsLayout L = ws_layout_causal(num_seqs, num_query_tokens, num_heads, num_kv_heads, head_dim,
+                                        max_context_len);
+    // item and partial-row indices are 32-bit
+    if (L.item_cap * num_kv_heads >= (1LL << 31) || (long long)num_query_tokens * L.pmax >= (1LL << 31))
+        return PA_ERR_UNSUPPORTED;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total)
+        return PA_ERR_WORKSPACE;
+    if (debug_validate()) {
+        std::vector<int32_t> lens((size_t)num_seqs), tab((size_t)num_seqs * max_blocks_per_seq),
+            qs((size_t)num_seqs + 1);
+        if (cudaMemcpyAsync(lens.data(), context_lens, sizeof(int32_t) * lens.size(), cudaMemcpyDeviceToHost, st) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(tab.data(), block_tables, sizeof(int32_t) * tab.size(), cudaMemcpyDeviceToHost, st) !=
+                cudaSuccess ||
+            cudaMemcpyAsync(qs.data(), query_start, sizeof(int32_t) * qs.size(), cudaMemcpyDeviceToHost, st) !=
+                cudaSuccess ||
+            cudaStreamSynchronize(st) != cudaSuccess)
+            return PA_ERR_CUDA;
+        if (qs[0] != 0 || qs[(size_t)num_seqs] != num_query_tokens) return PA_ERR_INVALID_ARG;
+        for (int i = 0; i < num_seqs; ++i) {
+            const int len = lens[(size_t)i];
+            const int T = qs[(size_t)i + 1] - qs[(size_t)i];
+            if (T < 0 || T > len || len > max_context_len ||
+                (long long)len > (long long)max_blocks_per_seq * block_size)
+                return PA_ERR_INVALID_ARG;
+            for (int b = 0; b < (len + block_size - 1) / block_size; ++b) {
+                const int32_t id = tab[(size_t)i * max_blocks_per_seq + b];
+                if (id < 0 || id >= num_blocks) return PA_ERR_INVALID_ARG;
+            }
+        }
+    }
+    const int box_rows = block_size < CHUNK ? block_size : CHUNK;
+    CUtensorMap tmk, tmv;
+    if (!cache_tensor_map(&tmk, k_cache, rows, head_dim, box_rows) ||
+        !cache_tensor_map(&tmv, v_cache, rows, head_dim, box_rows))
+        return PA_ERR_CUDA;
+    const int ms = 16 / G > 1 ? 16 / G : 1;   // query rows of up to ms new tokens fill two head tiles
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
+    int *part_off = reinterpret_cast<int *>(ws + L.part_off);
+    int *vlen = reinterpret_cast<int *>(ws + L.gsize);
+    int *gstart = reinterpret_cast<int *>(ws + L.gshared);
+    ItemRec *items = reinterpret_cast<ItemRec *>(ws + L.items);
+    int *grp = reinterpret_cast<int *>(ws + L.grp);
+    __half *hout = reinterpret_cast<__half *>(out);
+    causal_prep_kernel<<<1, PREP_THREADS, 0, st>>>(context_lens, query_start, num_seqs, num_query_tokens, num_heads,
+                                                   head_dim, num_kv_heads, max_context_len,
+                                                   (long long)max_blocks_per_seq * block_size, L.pt, ms, hdr,
+                                                   part_off, vlen, gstart, items, grp, hout);
+    if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+
+    DecodeArgs args;
+    args.out = hout;
+    args.query = reinterpret_cast<const __half *>(query);
+    args.block_tables = block_tables;
+    args.context_lens = vlen;   // per query row: the positions it sees
+    args.Hq = num_heads;
+    args.Hkv = num_kv_heads;
+    args.G = G;
+    args.bs = block_size;
+    args.mbps = max_blocks_per_seq;
+    args.pt = L.pt;
+    args.ms = ms;
+    args.num_blocks = num_blocks;
+    args.wait_limit = wait_limit_cycles();
+    args.scale_log2 = scale * 1.4426950408889634f;
+    args.hdr = hdr;
+    args.part_off = part_off;
+    args.items = items;
+    args.grp = grp;
+    args.ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
+    args.ws_o = reinterpret_cast<float *>(ws + L.o);
+    const long long max_items = L.item_cap * num_kv_heads;
+    if (head_dim == 128) return launch_decode<128, 2, true>(tmk, tmv, args, max_items, st);
+    return launch_decode<64, 2, true>(tmk, tmv, args, max_items, st);
 }
 
 }  // namespace
@@ -1245,6 +1547,26 @@ extern "C" int pa_decode_shared_prefix(uint16_t *out, const uint16_t *query, con
     return decode_impl(out, query, k_cache, v_cache, block_tables, context_lens, group_leader, shared_len, num_seqs,
                        num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len,
                        scale, workspace, workspace_bytes, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t pa_attention_causal_workspace_size(int num_seqs, int num_query_tokens, int num_heads,
+                                                     int num_kv_heads, int head_dim, int max_context_len) {
+    if (num_seqs < 0 || num_query_tokens < 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        num_heads % num_kv_heads != 0 || head_dim <= 0 || max_context_len < 0)
+        return 0;
+    return ws_layout_causal(num_seqs, num_query_tokens, num_heads, num_kv_heads, head_dim, max_context_len).total;
+}
+
+extern "C" int pa_attention_causal(uint16_t *out, const uint16_t *query, const uint16_t *k_cache,
+                                   const uint16_t *v_cache, const int32_t *block_tables, const int32_t *context_lens,
+                                   const int32_t *query_start, int num_seqs, int num_query_tokens, int num_heads,
+                                   int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                   int max_blocks_per_seq, int max_context_len, float scale, void *workspace,
+                                   size_t workspace_bytes, void *stream) {
+    return causal_impl(out, query, k_cache, v_cache, block_tables, context_lens, query_start, num_seqs,
+                       num_query_tokens, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                       max_blocks_per_seq, max_context_len, scale, workspace, workspace_bytes,
+                       static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------ failure-detection self-test

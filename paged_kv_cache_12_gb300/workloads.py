@@ -29,6 +29,18 @@ Workloads (shaped like the pages' examples; sizes named by what they are):
   prompt shared by all 8 samples (``prompt_extra`` > 0 adds 1..block-1 tokens
   so the shared tail block is partial), then U{0..512} private tokens per
   sample already generated, plus this step's token.
+* ``spec72b`` -- the gqa72b shapes with 4 new tokens per sequence in the step
+  (speculative candidates, deepsonar page section 2.5): 100 sequences of 8192
+  positions, the last 4 computed together.
+* ``chunked`` -- 64 sequences, 32 / 8 heads, head_dim 128, block 16, in one
+  step (deepsonar page section 2.5: prefill chunks mixed into the decode
+  batch): sequence 0 computes the last 2048-token chunk of a 12000-token
+  prompt, sequence 1 a whole 600-token prompt (the chester-dev.com page's
+  legal-summary and chat sizes), sequences 2..63 one decode token each over
+  log-uniform [64, 32768] contexts.
+
+Steps with several new tokens per sequence also draw ``query_multi``: one
+query row per new token, sequences in order.
 """
 from __future__ import annotations
 
@@ -39,10 +51,10 @@ from dataclasses import dataclass, field
 
 import numpy as np
 
-WORKLOADS = ("tiny", "mha7b", "gqa72b", "mix", "cow16", "cow32")
+WORKLOADS = ("tiny", "mha7b", "gqa72b", "mix", "cow16", "cow32", "spec72b", "chunked")
 
 # child-stream indices, one per drawn array
-_S_LENGTHS, _S_ORDER, _S_QUERY, _S_KPOOL, _S_VPOOL, _S_NEWK, _S_NEWV, _S_EXTRA = range(8)
+_S_LENGTHS, _S_ORDER, _S_QUERY, _S_KPOOL, _S_VPOOL, _S_NEWK, _S_NEWV, _S_EXTRA, _S_QMULTI = range(9)
 
 
 _CHUNK = 1 << 22     # values per independently seeded chunk
@@ -145,6 +157,17 @@ class Workload:
         return self._get("q", _S_QUERY, (self.num_seqs, self.num_heads, self.head_dim))
 
     @property
+    def query_multi(self) -> np.ndarray:
+        """fp16 [num_new_tokens, num_heads, head_dim]: a query row for every
+        token written this step, sequences in order."""
+        return self._get("qm", _S_QMULTI, (self.num_new_tokens, self.num_heads, self.head_dim))
+
+    @property
+    def query_start(self) -> np.ndarray:
+        """int32 [num_seqs + 1]: first query_multi row of every sequence."""
+        return np.concatenate([[0], np.cumsum(self.new_counts)]).astype(np.int32)
+
+    @property
     def k_pool(self) -> np.ndarray:
         """fp16 [num_blocks, num_kv_heads, block_size, head_dim]: initial K content of every
         physical slot (the history already in the cache)."""
@@ -177,9 +200,10 @@ def _spare_pool(context_lens, block_size, spare):
 
 def custom(name="custom", seed=7, num_seqs=4, num_heads=4, num_kv_heads=2, head_dim=64, block_size=16,
            context_lens=None, new_tokens=1, num_blocks=None, spare_blocks=None, permute=True) -> Workload:
-    """A workload with given shapes and lengths (edge cases in tests)."""
+    """A workload with given shapes and lengths (edge cases in tests);
+    new_tokens: tokens written this step, one count or one per sequence."""
     lens = np.asarray(context_lens if context_lens is not None else [1] * num_seqs, dtype=np.int32)
-    hist = np.maximum(lens - new_tokens, 0).astype(np.int32)
+    hist = np.maximum(lens - np.asarray(new_tokens, dtype=np.int32), 0).astype(np.int32)
     spare = num_seqs if spare_blocks is None else spare_blocks
     nb = num_blocks if num_blocks is not None else max(1, _spare_pool(lens, block_size, spare))
     order = _order(seed, nb) if permute else np.arange(nb, dtype=np.int32)
@@ -224,4 +248,16 @@ def make(name: str, prompt_extra: int | None = None) -> Workload:
         w = Workload(name, seed, prompts * samples, 32, 8, 128, bs, nb, lens, hist, _order(seed, nb),
                      num_prompts=prompts, samples_per_prompt=samples, prompt_len=plen, divergent=div)
         return w
+    if name == "spec72b":
+        lens = np.full(100, 8192, dtype=np.int32)
+        nb = _spare_pool(lens, 16, 100)
+        return Workload(name, seed, 100, 64, 8, 128, 16, nb, lens, lens - 4, _order(seed, nb))
+    if name == "chunked":
+        u = rl.uniform(math.log(64), math.log(32768), size=64)
+        lens = np.rint(np.exp(u)).astype(np.int32)
+        lens[:2] = (12000, 600)
+        hist = lens - 1
+        hist[:2] = (12000 - 2048, 0)
+        nb = _spare_pool(lens, 16, 64)
+        return Workload(name, seed, 64, 32, 8, 128, 16, nb, lens, hist.astype(np.int32), _order(seed, nb))
     raise KeyError(name)

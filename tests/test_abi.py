@@ -47,6 +47,10 @@ def test_workspace_size_is_a_host_bound():
     # few sequences: shorter partitions (256 tokens) so that the work still spreads
     assert pa.pa_decode_workspace_size(2, 8, 1, 128, 8192) >= 2 * 32 * 8 * 128 * 4
     assert pa.lib().pa_decode_workspace_size(1, 8, 0, 128, 10) == 0
+    # multi-token form: a partial row per query row and partition (400 rows x 8 partitions of 1024)
+    spec = pa.pa_attention_causal_workspace_size(100, 400, 64, 8, 128, 8192)
+    assert 400 * 8 * 64 * 128 * 4 <= spec < 400 * 9 * 64 * 128 * 4
+    assert pa.lib().pa_attention_causal_workspace_size(1, 4, 6, 4, 128, 10) == 0
 
 
 def test_host_checks_fail_before_any_launch():
@@ -67,3 +71,10 @@ def test_host_checks_fail_before_any_launch():
     assert L.pa_block_copy(nul, nul, nul, 0, 8, 128, 16, 10, nul) == pa.PA_OK
     assert L.pa_decode(nul, nul, nul, nul, nul, nul, 0, 8, 1, 128, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_OK
     assert L.pa_decode(nul, nul, nul, nul, nul, nul, 1, 8, 1, 128, 16, 10, 1, 16, -0.1, nul, 0, nul) == pa.PA_ERR_INVALID_ARG
+    # the multi-token form: same shape rules; no query rows launches nothing; rows need sequences
+    C = L.pa_attention_causal
+    assert C(nul, nul, nul, nul, nul, nul, nul, 1, 4, 8, 1, 96, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_ERR_UNSUPPORTED
+    assert C(nul, nul, nul, nul, nul, nul, nul, 1, 4, 8, 1, 128, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_ERR_INVALID_ARG
+    assert C(nul, nul, nul, nul, nul, nul, nul, 0, 4, 8, 1, 128, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_ERR_INVALID_ARG
+    assert C(nul, nul, nul, nul, nul, nul, nul, 3, 0, 8, 1, 128, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_OK
+    assert C(nul, nul, nul, nul, nul, nul, nul, 1, 4, 8, 3, 128, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_ERR_INVALID_ARG

@@ -36,6 +36,21 @@ def test_shapes_and_ranges():
         assert c.divergent.min() >= 0 and c.divergent.max() <= 512
         c0 = workloads.make(name, prompt_extra=0)
         assert c0.prompt_len == 2048
+    s = workloads.make("spec72b")
+    assert (s.new_counts == 4).all() and (s.context_lens == 8192).all() and s.group == 8
+    assert list(s.query_start[:3]) == [0, 4, 8] and s.query_start[-1] == 400
+    c = workloads.make("chunked")
+    assert list(c.context_lens[:2]) == [12000, 600] and list(c.new_counts[:2]) == [2048, 600]
+    assert (c.new_counts[2:] == 1).all() and c.num_new_tokens == 2048 + 600 + 62
+    assert c.query_start[-1] == c.num_new_tokens and c.query_start[2] == 2648
+
+
+def test_multi_token_query_rows():
+    w = workloads.custom(seed=3, num_seqs=3, num_heads=4, num_kv_heads=2, head_dim=64, context_lens=[10, 5, 7],
+                         new_tokens=[3, 0, 7])
+    assert list(w.history_lens) == [7, 5, 0] and list(w.query_start) == [0, 3, 3, 10]
+    assert w.query_multi.shape == (10, 4, 64) and w.query_multi.dtype == np.float16
+    assert not np.array_equal(w.query_multi[:3], w.query[:3].reshape(3, 4, 64))
 
 
 def test_values_are_rounded_standard_normal():
