@@ -15,6 +15,11 @@ e2e    = the same through the public API with pinned host buffers: every step
          copies its block tables, lengths and slot mapping, and every layer its
          query and new K/V rows, host -> device, and every layer's output back.
 
+Steps that compute several new tokens per sequence (--workload spec72b: 4
+speculative tokens per sequence; chunked: prompt chunks mixed into a decode
+batch) run pa_attention_causal instead of pa_decode; there value counts the
+query tokens computed per second.
+
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Multi-GPU (torchrun): each rank runs its own replica of the workload (weak
 scaling); the time is the maximum over ranks.
@@ -48,7 +53,9 @@ def parse():
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--layers", type=int, default=None, help="default: 80 for gqa72b, 1 for the others")
-    p.add_argument("--workload", default=WORKLOAD, help="gqa72b (the headline), mha7b, mix, cow16, cow32, tiny")
+    p.add_argument("--workload", default=WORKLOAD,
+                   help="gqa72b (the headline), mha7b, mix, cow16, cow32, tiny; several tokens per sequence: "
+                        "spec72b, chunked")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="skip the CUDA Graph replay measurement")
     p.add_argument("--shared-prefix", action="store_true",
@@ -89,6 +96,30 @@ def decode_bytes(w) -> int:
     qo = 2 * w.num_seqs * w.num_heads * w.head_dim * 2
     tables = int((-(-L // w.block_size)).sum()) * 4
     return kv + qo + tables + 4 * w.num_seqs
+
+
+def multi_token(w) -> bool:
+    return bool(w.num_seqs) and not bool((w.new_counts == 1).all())
+
+
+def causal_bytes(w) -> int:
+    """Algorithmic bytes of one multi-token call: every context token's K and
+    V rows once per sequence (its new tokens share them), every query and
+    output row, the block-table entries and the lengths and query offsets."""
+    L = w.context_lens.astype(np.int64)
+    kv = int((L * 2 * w.num_kv_heads * w.head_dim * 2).sum())
+    qo = 2 * w.num_new_tokens * w.num_heads * w.head_dim * 2
+    tables = int((-(-L // w.block_size)).sum()) * 4
+    return kv + qo + tables + 4 * (2 * w.num_seqs + 1)
+
+
+def causal_flops(w) -> int:
+    """Multiply-adds x 2 of Q K^T and P V: new token j of sequence i sees
+    L_i - T_i + j + 1 positions, for every query head."""
+    L = w.context_lens.astype(np.int64)
+    T = w.new_counts.astype(np.int64)
+    seen = (T * (L - T + 1) + T * (T - 1) // 2).sum()       # sum over rows of the positions seen
+    return int(4 * seen * w.num_heads * w.head_dim)
 
 
 def kv_write_bytes(w) -> int:
@@ -180,29 +211,60 @@ class OracleSample:
         import oracle
         self.oracle, self.w, self.tables, self.lens = oracle, w, tables, lens
         self.threads = oracle.default_threads()
-        n = min(self.threads, w.num_seqs)
+        self.multi = multi_token(w)
+        # multi-token steps: sequences in index order, leaving out any one whose
+        # rows alone would take the oracle longer than the whole sample (a long
+        # prompt chunk; the oracle runs one sequence per thread)
+        if self.multi:
+            T = w.new_counts.astype(np.int64)
+            cost = T * w.context_lens.astype(np.int64) * w.num_heads * w.head_dim * 4 / 1e9   # ~s at 1 GFLOP/s
+            self.order = [i for i in range(w.num_seqs) if T[i] > 0 and cost[i] < target_s]
+            self.skipped = w.num_seqs - len(self.order)
+        else:
+            self.order = list(range(w.num_seqs))
+            self.skipped = 0
+        n = min(self.threads, len(self.order))
         t = self.run(n)
-        if t < target_s / 2 and n < w.num_seqs:
-            n = min(w.num_seqs, int(n * target_s / max(t, 1e-3)))
+        if t < target_s / 2 and n < len(self.order):
+            n = min(len(self.order), int(n * target_s / max(t, 1e-3)))
             if n >= self.threads:
                 n = (n // self.threads) * self.threads
         self.n = max(1, n)
 
+    def rows(self, n):
+        qs = self.w.query_start
+        return int(sum(qs[i + 1] - qs[i] for i in self.order[:n]))
+
     def run(self, n):
         w = self.w
         t0 = time.perf_counter()
-        self.oracle.paged_decode(w.query, w.k_pool, w.v_pool, self.tables, self.lens, w.num_kv_heads,
-                                 w.block_size, w.scale, threads=self.threads, seq_range=(0, n))
+        if self.multi:
+            idx = np.asarray(self.order[:n])
+            qs = w.query_start
+            rows = np.concatenate([np.arange(qs[i], qs[i + 1]) for i in idx])
+            sub_qs = np.concatenate([[0], np.cumsum(qs[idx + 1] - qs[idx])]).astype(np.int32)
+            self.oracle.paged_attention_causal(w.query_multi[rows], w.k_pool, w.v_pool, self.tables[idx],
+                                               self.lens[idx], sub_qs, w.num_kv_heads, w.block_size, w.scale,
+                                               threads=self.threads)
+        else:
+            self.oracle.paged_decode(w.query, w.k_pool, w.v_pool, self.tables, self.lens, w.num_kv_heads,
+                                     w.block_size, w.scale, threads=self.threads, seq_range=(0, n))
         return time.perf_counter() - t0
 
-    def rate(self):
-        """(tokens/s for the 80-layer step, seconds of this call)"""
+    def rate(self, layers=LAYERS):
+        """(tokens/s for the `layers`-layer step, seconds of this call)"""
         secs = self.run(self.n)
-        return self.n / (secs * LAYERS), secs
+        units = self.rows(self.n) if self.multi else self.n
+        return units / (secs * layers), secs
 
-    def describe(self, secs):
+    def describe(self, secs, layers=LAYERS):
+        if self.multi:
+            left = f", leaving out {self.skipped} sequence(s) too long for the sample" if self.skipped else ""
+            return (f"{self.n} of {self.w.num_seqs} sequences ({self.rows(self.n)} of {self.w.num_new_tokens} "
+                    f"query rows{left}), 1 of {layers} layer(s) ({secs:.1f} s per call), scaled to the "
+                    f"{layers}-layer step")
         return (f"{self.n} of {self.w.num_seqs} sequences x {int(self.w.context_lens[0])} tokens, "
-                f"1 of {LAYERS} layers ({secs:.1f} s per call), scaled to the {LAYERS}-layer step")
+                f"1 of {layers} layers ({secs:.1f} s per call), scaled to the {layers}-layer step")
 
 
 # ------------------------------------------------------------------ our arm
@@ -214,10 +276,10 @@ def workload(args):
         return w
     if w.num_prompts:
         raise SystemExit("--seqs applies to the single-context workloads only")
+    pick = (lambda a: list(a[: args.seqs]) if args.seqs <= w.num_seqs else [int(a[0])] * args.seqs)
     return workloads.custom(name=f"{w.name}-{args.seqs}seqs", seed=w.seed, num_seqs=args.seqs,
                             num_heads=w.num_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
-                            block_size=w.block_size, context_lens=list(w.context_lens[: args.seqs])
-                            if args.seqs <= w.num_seqs else [int(w.context_lens[0])] * args.seqs)
+                            block_size=w.block_size, context_lens=pick(w.context_lens), new_tokens=pick(w.new_counts))
 
 
 def allocate(w, pa):
@@ -264,6 +326,9 @@ def describe(w, layers):
     ctx = f"{int(L[0])}-token context" if (L == L[0]).all() else f"context {int(L.min())}..{int(L.max())} tokens"
     extra = (f", {w.num_prompts} prompts x {w.samples_per_prompt} samples sharing a {w.prompt_len}-token prompt"
              if w.num_prompts else "")
+    if multi_token(w):
+        T = w.new_counts
+        extra += (f", {w.num_new_tokens} new tokens computed causally (per sequence {int(T.min())}..{int(T.max())})")
     return (f"{w.name}: {w.num_seqs} sequences, {ctx}{extra}, {w.num_heads} query / {w.num_kv_heads} KV heads, "
             f"head_dim {w.head_dim}, block {w.block_size}, {layers} layer(s) per step sharing one layer's cache")
 
@@ -287,9 +352,11 @@ def run_ours(args):
     has_pairs = len(pairs) > 0
 
     # ---- device-resident inputs
+    multi = multi_token(w)
+    q_host = w.query_multi if multi else w.query
     k = torch.from_numpy(w.k_pool).to(dev)
     v = torch.from_numpy(w.v_pool).to(dev)
-    q = torch.from_numpy(w.query).to(dev)
+    q = torch.from_numpy(q_host).to(dev)
     nk = torch.from_numpy(w.new_key).to(dev)
     nv = torch.from_numpy(w.new_value).to(dev)
     d_slots = torch.from_numpy(slots).to(dev)
@@ -298,7 +365,11 @@ def run_ours(args):
     d_lens = torch.from_numpy(lens).to(dev)
     out = torch.empty_like(q)
     shared_mode = bool(args.shared_prefix and w.num_prompts)
-    if shared_mode:
+    if multi:
+        d_qs = torch.from_numpy(w.query_start).to(dev)
+        nws = pa.pa_attention_causal_workspace_size(w.num_seqs, w.num_new_tokens, w.num_heads, w.num_kv_heads,
+                                                    w.head_dim, w.max_context_len)
+    elif shared_mode:
         S = w.samples_per_prompt
         d_lead = torch.from_numpy(np.repeat(np.arange(w.num_prompts) * S, S).astype(np.int32)).to(dev)
         d_shl = torch.full((w.num_seqs,), w.prompt_len, dtype=torch.int32, device=dev)
@@ -315,7 +386,9 @@ def run_ours(args):
         pa.pa_kv_write(nk, nv, d_slots, k, v, st)
 
     def decode_on(st):
-        if shared_mode:
+        if multi:
+            pa.pa_attention_causal(out, q, k, v, d_tables, d_lens, d_qs, w.scale, w.max_context_len, ws, st)
+        elif shared_mode:
             pa.pa_decode_shared_prefix(out, q, k, v, d_tables, d_lens, d_lead, d_shl, w.scale, w.max_context_len, ws,
                                        st)
         else:
@@ -387,7 +460,8 @@ def run_ours(args):
     h_lens = torch.from_numpy(lens).pin_memory()
     h_slots = torch.from_numpy(slots).pin_memory()
     h_pairs = torch.from_numpy(np.ascontiguousarray(pairs)).pin_memory()
-    h_q = torch.from_numpy(np.ascontiguousarray(w.query)).pin_memory()
+    h_q = torch.from_numpy(np.ascontiguousarray(q_host)).pin_memory()
+    h_qs = torch.from_numpy(w.query_start).pin_memory() if multi else None
     h_nk = torch.from_numpy(np.ascontiguousarray(w.new_key)).pin_memory()
     h_nv = torch.from_numpy(np.ascontiguousarray(w.new_value)).pin_memory()
     h_out = torch.empty((layers,) + tuple(out.shape), dtype=out.dtype).pin_memory()
@@ -398,6 +472,8 @@ def run_ours(args):
         d_slots.copy_(h_slots, non_blocking=True)
         if has_pairs:
             d_pairs.copy_(h_pairs, non_blocking=True)
+        if multi:
+            d_qs.copy_(h_qs, non_blocking=True)
         for l in range(layers):
             q.copy_(h_q, non_blocking=True)
             nk.copy_(h_nk, non_blocking=True)
@@ -417,7 +493,7 @@ def run_ours(args):
     barrier()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
     h2d = h_tables.numel() * 4 + h_lens.numel() * 4 + h_slots.numel() * 8 + (h_pairs.numel() * 8 if has_pairs else 0) \
-        + layers * (h_q.numel() * 2 + h_nk.numel() * 2 + h_nv.numel() * 2)
+        + (h_qs.numel() * 4 if multi else 0) + layers * (h_q.numel() * 2 + h_nk.numel() * 2 + h_nv.numel() * 2)
     d2h = layers * out.numel() * 2
 
     if rank != 0:
@@ -427,9 +503,9 @@ def run_ours(args):
         return
 
     # ---- numbers
-    B = w.num_seqs
+    B = w.num_new_tokens if multi else w.num_seqs      # query tokens computed per layer step
     tok_s = job_tokens_per_s(world, B, args.steps, total_ms)
-    dbytes = decode_bytes(w)
+    dbytes = causal_bytes(w) if multi else decode_bytes(w)
     step_bytes = layers * (dbytes + kv_write_bytes(w) + (2 * len(pairs) * w.num_kv_heads * w.block_size *
                                                         w.head_dim * 2 * 2))
     kv_gbs = world * step_bytes * args.steps / (total_ms / 1e3) / 1e9
@@ -437,6 +513,11 @@ def run_ours(args):
     achieved = dbytes / (dec_avg_ms / 1e3) / 1e9
     peaks = measured_peaks()
     peak = peaks["hbm_gbs"] if peaks else 6800.0
+    # multi-token steps: the binding roof is HBM or the tensor cores (fp16 MMA
+    # at the measured bf16 rate), whichever takes longer for the call's work
+    flops = causal_flops(w) if multi else None
+    tpeak = (peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops")) if peaks else 1700.0
+    tensor_bound = bool(multi and flops / (tpeak * 1e12) > dbytes / (peak * 1e9))
     headline = w.name == WORKLOAD and args.seqs is None
     line = {
         "metric": METRIC,
@@ -453,7 +534,7 @@ def run_ours(args):
         "data": "synthetic",
         "config": {
             "workload": describe(w, layers),
-            "num_seqs": B, "context_len_max": int(w.context_lens.max()), "num_heads": w.num_heads,
+            "num_seqs": w.num_seqs, "context_len_max": int(w.context_lens.max()), "num_heads": w.num_heads,
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
             "layers": layers, "parallelism": f"replicas x{world}",
             "l2": f"K/V read per layer {dbytes / 1e9:.2f} GB vs 129 MB L2; no flush",
@@ -462,7 +543,8 @@ def run_ours(args):
         "decode_ms": {"mean": round(dec_avg_ms, 5), "p10": round(float(np.percentile(dec_ms, 10)), 5),
                       "p90": round(float(np.percentile(dec_ms, 90)), 5)},
         "roofline": {
-            "kernel": "pa_decode (prep + persistent partition kernel with fused log-sum-exp merge)",
+            "kernel": ("pa_attention_causal" if multi else "pa_decode") +
+                      " (prep + persistent partition kernel with fused log-sum-exp merge)",
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": kernel_traffic() if headline else None,
@@ -479,6 +561,18 @@ def run_ours(args):
         "alloc_us_per_step": round(alloc_us, 1),
         "clocks": clk.summary(),
     }
+    if multi:
+        tf = flops / (dec_avg_ms / 1e3) / 1e12
+        line["roofline"]["flops_per_launch"] = flops
+        line["roofline"]["achieved_tflops"] = round(tf, 1)
+        line["roofline"]["tensor_peak_tflops"] = tpeak
+        if tensor_bound:
+            line["roofline"].update({"bound": "tensor", "achieved": round(tf, 1), "peak": tpeak, "unit": "TFLOP/s",
+                                     "frac": round(tf / tpeak, 4),
+                                     "peak_source": "MEASURED_PEAKS.json bf16_tflops_sustained (of measured; fp16 "
+                                                    "MMA runs at the bf16 rate)" if peaks else
+                                                    "fallback 1.7 PFLOP/s (of fallback)"})
+        line["query_tokens_per_layer_step"] = int(w.num_new_tokens)
     if w.num_prompts:
         ub = unique_kv_bytes(w, tables, lens)
         line["roofline"]["unique_kv_bytes_per_launch"] = ub
@@ -487,9 +581,9 @@ def run_ours(args):
         line["decode_call"] = "pa_decode_shared_prefix" if shared_mode else "pa_decode"
     if not args.no_cpu_baseline and world == 1 and not w.num_prompts:
         smp = OracleSample(w, tables, lens, target_s=10.0)
-        rate, secs = smp.rate()
+        rate, secs = smp.rate(layers)
         line["cpu_baseline"] = {"value": round(rate, 6), "unit": "tokens/s", "cores": smp.threads, "kind": "oracle",
-                                "sample": smp.describe(secs)}
+                                "sample": smp.describe(secs, layers)}
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.barrier()

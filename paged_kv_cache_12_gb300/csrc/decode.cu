@@ -55,8 +55,20 @@
 #ifndef PA_DECODE_DEPTH
 #define PA_DECODE_DEPTH 2
 #endif
+#ifndef PA_DECODE_MINB_WIDE
+#define PA_DECODE_MINB_WIDE 4
+#endif
+#ifndef PA_DECODE_DEPTH_WIDE
+#define PA_DECODE_DEPTH_WIDE 5
+#endif
 #ifndef PA_DECODE_MINB
 #define PA_DECODE_MINB 8
+#endif
+#ifndef PA_CAUSAL_L2
+#define PA_CAUSAL_L2 0
+#endif
+#ifndef PA_CAUSAL_NT
+#define PA_CAUSAL_NT 2
 #endif
 
 namespace pa {
@@ -66,7 +78,6 @@ constexpr int MAX_PART_TOKENS = 1024;           // largest partition (one work i
 constexpr long long TARGET_ITEMS = 4096;        // work items wanted for load balance
 constexpr int CHUNK = 16;                       // tokens per pipeline stage (one MMA K step of P V)
 constexpr int NC = PA_DECODE_CONSUMERS;         // consumer warps per CTA
-constexpr int DEPTH = PA_DECODE_DEPTH;          // pipeline stages per consumer
 constexpr int NWARPS = NC + 1;                  // + the producer warp
 constexpr long long WAIT_LIMIT = 1LL << 31;     // clock cycles (about a second): default wait bound, drain bound
 constexpr int PREP_THREADS = 1024;
@@ -135,7 +146,7 @@ WsLayout ws_layout(int B, int Hq, int Hkv, int D, int max_ctx, bool grouped) {
 WsLayout ws_layout_causal(int B, int NQ, int Hq, int Hkv, int D, int max_ctx) {
     WsLayout w;
     const int G = Hq / Hkv;
-    const int ms = 16 / G > 1 ? 16 / G : 1;
+    const int ms = 8 * PA_CAUSAL_NT / G > 1 ? 8 * PA_CAUSAL_NT / G : 1;
     w.pt = part_tokens(B, Hkv, max_ctx);
     w.pmax = max_ctx > 0 ? (max_ctx + w.pt - 1) / w.pt : 1;
     w.item_cap = (long long)w.pmax * ((NQ + ms - 1) / ms + B);
@@ -195,6 +206,9 @@ struct ItemDesc {
 
 template <int D, int NT>
 struct Cfg {
+    // pipeline stages per consumer: a two-tile consumer keeps fewer warps on
+    // an SM (registers), so each keeps more bytes in flight
+    static constexpr int DEPTH = NT == 1 ? PA_DECODE_DEPTH : PA_DECODE_DEPTH_WIDE;
     static constexpr int BOXES = D / 64;                   // 64-column (128-byte) boxes per tile row
     static constexpr int TILE = BOXES * CHUNK * 128;       // one 16-token K or V tile
     static constexpr int STAGE = 2 * TILE;                 // K tile then V tile
@@ -571,6 +585,7 @@ struct ConsumerSmem {
 template <int D, int NT>
 __device__ __forceinline__ ConsumerSmem consumer_smem(uint8_t *smem, int c) {
     using C = Cfg<D, NT>;
+    constexpr int DEPTH = C::DEPTH;
     uint8_t *ctrl = smem + NC * C::DATA + c * C::CTRL;
     ConsumerSmem s;
     s.data = smem_u32(smem + c * C::DATA);
@@ -586,9 +601,12 @@ __device__ __forceinline__ ConsumerSmem consumer_smem(uint8_t *smem, int c) {
 template <int D, int NT, bool CAUSAL>
 __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMap *tmv, const DecodeArgs &a) {
     using C = Cfg<D, NT>;
+    constexpr int DEPTH = C::DEPTH;
     const int lane = threadIdx.x & 31;
     const int total = a.hdr->total_items;
-    const uint64_t pol = policy_evict_first();
+    const uint64_t pol = !CAUSAL || PA_CAUSAL_L2 == 0 ? policy_evict_first()
+                         : PA_CAUSAL_L2 == 1               ? policy_evict_normal()
+                                                           : policy_evict_last();
     const int box_rows = a.bs < CHUNK ? a.bs : CHUNK;
 
     // Items are prefetched in three depths so that no latency is waited on
@@ -877,6 +895,7 @@ __device__ void merge_group(const DecodeArgs &a, int seq, int kvh, int P) {
 template <int D, int NT, bool CAUSAL>
 __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
     using C = Cfg<D, NT>;
+    constexpr int DEPTH = C::DEPTH;
     constexpr int KS = D / 16;     // MMA k-steps of S^T = K Q^T
     constexpr int MT = D / 16;     // MMA m-tiles of O^T = V^T P^T
     const int lane = threadIdx.x & 31;
@@ -1159,7 +1178,7 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
 }
 
 template <int D, int NT, bool CAUSAL>
-__global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? PA_DECODE_MINB : PA_DECODE_MINB / 2) decode_kernel(const __grid_constant__ CUtensorMap tmk,
+__global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? PA_DECODE_MINB : PA_DECODE_MINB_WIDE) decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                                              const __grid_constant__ CUtensorMap tmv,
                                                              const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -1168,7 +1187,7 @@ __global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? PA_DECODE_MINB : PA_DEC
     if (threadIdx.x == 0) {
         for (int c = 0; c < NC; ++c) {
             const ConsumerSmem cs = consumer_smem<D, NT>(smem, c);
-            for (int s = 0; s < DEPTH; ++s) {
+            for (int s = 0; s < Cfg<D, NT>::DEPTH; ++s) {
                 mbar_init(smem_u32(&cs.full[s]), 1);
                 mbar_init(smem_u32(&cs.empty[s]), 1);
             }
@@ -1459,7 +1478,9 @@ int causal_impl(uint16_t *out, const uint16_t *query, const uint16_t *k_cache, c
     if (!cache_tensor_map(&tmk, k_cache, rows, head_dim, box_rows) ||
         !cache_tensor_map(&tmv, v_cache, rows, head_dim, box_rows))
         return PA_ERR_CUDA;
-    const int ms = 16 / G > 1 ? 16 / G : 1;   // query rows of up to ms new tokens fill two head tiles
+    // query rows of up to ms new tokens fill the head tiles
+    const int ms = 8 * PA_CAUSAL_NT / G > 1 ? 8 * PA_CAUSAL_NT / G : 1;
+    if (PA_CAUSAL_NT == 1 && G > 8) return PA_ERR_UNSUPPORTED;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
@@ -1497,8 +1518,8 @@ int causal_impl(uint16_t *out, const uint16_t *query, const uint16_t *k_cache, c
     args.ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
     args.ws_o = reinterpret_cast<float *>(ws + L.o);
     const long long max_items = L.item_cap * num_kv_heads;
-    if (head_dim == 128) return launch_decode<128, 2, true>(tmk, tmv, args, max_items, st);
-    return launch_decode<64, 2, true>(tmk, tmv, args, max_items, st);
+    if (head_dim == 128) return launch_decode<128, PA_CAUSAL_NT, true>(tmk, tmv, args, max_items, st);
+    return launch_decode<64, PA_CAUSAL_NT, true>(tmk, tmv, args, max_items, st);
 }
 
 }  // namespace
