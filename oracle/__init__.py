@@ -30,6 +30,11 @@ Contents, each with the passage it follows:
 * ``paged_attention_causal`` -- several new query tokens per sequence, each
   attending causally to the positions up to its own (deepsonar page section
   2.5: chunked prefill and speculative tokens), in C.
+* ``paged_attention_typed`` / ``kv_write_fp8`` / ``e4m3_encode`` -- the same
+  attention over caches of bf16 or fp8 E4M3 codes with one scale for K and one
+  for V, and the quantising write into an fp8 cache.  The pages keep the cache
+  in fp16 (deepsonar page section 2.1, two bytes per element); these follow
+  the formats' definitions, and the quantiser is the reading recorded with it.
 
 Readings where the pages are silent are listed with each function.
 """
@@ -81,6 +86,13 @@ def _load():
             lib.or_paged_attention_causal.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                                       i64, i64, i64, dbl, i32, i32]
             lib.or_paged_attention_causal.restype = i32
+            lib.or_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.or_bf16_to_double.restype = dbl
+            lib.or_e4m3_to_double.argtypes = [ctypes.c_uint8]
+            lib.or_e4m3_to_double.restype = dbl
+            lib.or_paged_attention_typed.argtypes = [vp, vp, i32, vp, vp, i32, dbl, dbl, vp, vp, vp, i32, i32, i32,
+                                                     i32, i32, i32, i64, i64, i64, dbl, i32, i32]
+            lib.or_paged_attention_typed.restype = i32
             _lib = lib
     return _lib
 
@@ -88,6 +100,51 @@ def _load():
 def half_to_double(bits: int) -> float:
     """The C oracle's own binary16 -> double conversion, for pinning it."""
     return _load().or_half_to_double(int(bits) & 0xFFFF)
+
+
+def bf16_to_double(bits: int) -> float:
+    """The C oracle's bfloat16 -> double conversion."""
+    return _load().or_bf16_to_double(int(bits) & 0xFFFF)
+
+
+def e4m3_to_double(code: int) -> float:
+    """The C oracle's FP8 E4M3 code -> double conversion."""
+    return _load().or_e4m3_to_double(int(code) & 0xFF)
+
+
+KV_F16, KV_BF16, KV_FP8_E4M3 = 0, 1, 2
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """float32 values -> FP8 E4M3 codes, rounding to the nearest representable
+    value, ties to the even code, magnitudes beyond the largest finite value
+    (448) saturating to it, NaN to the NaN code; the sign is kept (so -0 and
+    negative values that round to zero give 0x80).  Written as a search over
+    the format's 127 finite non-negative values (``e4m3_to_double`` of codes
+    0x00 .. 0x7E), which is the definition of rounding to nearest."""
+    x = np.asarray(x, dtype=np.float32)
+    values = np.array([e4m3_to_double(c) for c in range(0x7F)])     # increasing
+    a = np.abs(x.astype(np.float64))
+    hi = np.clip(np.searchsorted(values, a, side="left"), 0, 0x7E)  # first value >= a
+    lo = np.clip(hi - 1, 0, 0x7E)
+    d_hi = values[hi] - a
+    d_lo = a - values[lo]
+    take_lo = (d_lo < d_hi) | ((d_lo == d_hi) & (lo % 2 == 0))
+    code = np.where(take_lo, lo, hi)
+    code = np.where(a >= values[0x7E], 0x7E, code)                  # saturate (also +-inf)
+    code = np.where(np.isnan(a), 0x7F, code).astype(np.uint8)
+    sign = np.signbit(x).astype(np.uint8) << 7
+    return code | sign
+
+
+def fp8_quantise(x, scale: float) -> np.ndarray:
+    """Codes of fp16 values x for an fp8 cache with dequantisation scale
+    `scale` (a stored code c stands for e4m3(c) * scale).  Reading (the pages
+    keep fp16): in float32 arithmetic, code = e4m3_encode(fl32(x) * inv) with
+    inv = fl32(1 / fl32(scale)) -- one reciprocal per cache, one product per
+    element, each rounded to float32."""
+    inv = np.float32(1.0) / np.float32(scale)
+    return e4m3_encode(np.asarray(x).astype(np.float32) * inv)
 
 
 # ---------------------------------------------------------------------------
@@ -380,6 +437,13 @@ def kv_write(k_cache, v_cache, key, value, slot_mapping, block_size):
     return kc, vc
 
 
+def kv_write_fp8(k_cache, v_cache, key, value, slot_mapping, block_size, k_scale, v_scale):
+    """kv_write into caches of fp8 codes (uint8 [block, kv_head, offset, dim]):
+    each new fp16 row is quantised with its cache's scale (``fp8_quantise``)."""
+    return kv_write(k_cache, v_cache, fp8_quantise(key, k_scale), fp8_quantise(value, v_scale), slot_mapping,
+                    block_size)
+
+
 def block_copy(k_cache, v_cache, pairs):
     """Return copies of the caches where each dst block holds what its src
     block held before the call (all K and V of every kv head and offset)."""
@@ -494,6 +558,56 @@ def paged_attention_causal(query, k_cache, v_cache, block_tables, context_lens, 
                                            block_size, tab.shape[1], sb, sh, st, float(scale), a, b)
         if rc != 0:
             raise RuntimeError("oracle causal attention failed")
+
+    bounds = np.linspace(0, B, threads + 1).astype(int)
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        list(ex.map(lambda ab: run(*ab), zip(bounds[:-1], bounds[1:])))
+    return out
+
+
+def paged_attention_typed(query, k_cache, v_cache, block_tables, context_lens, query_start, num_kv_heads, block_size,
+                          scale, kv_dtype, k_scale=1.0, v_scale=1.0, threads=None):
+    """fp64 attention over caches of element type kv_dtype (KV_F16, KV_BF16
+    with bf16 query rows, KV_FP8_E4M3 with fp16 query rows): element e of the
+    K cache stands for value(e) * k_scale, of the V cache for value(e) *
+    v_scale.  query_start None: one query row per sequence (the decode, a zero
+    row for an empty context); else the causal multi-token form.  query and
+    the caches are arrays of 16-bit patterns (uint16/float16) or, for fp8,
+    uint8 codes; the caches are 4-d [block, kv_head, offset, dim] views."""
+    lib = _load()
+    q = np.ascontiguousarray(query)
+    q_dtype = KV_BF16 if kv_dtype == KV_BF16 else KV_F16
+    nq, num_heads, head_dim = q.shape
+    kc = np.asarray(k_cache)
+    vc = np.asarray(v_cache)
+    esz = 1 if kv_dtype == KV_FP8_E4M3 else 2
+    if kc.ndim != 4 or kc.strides != vc.strides or kc.strides[3] != esz or kc.itemsize != esz:
+        raise ValueError("caches must be 4-d [block, kv_head, offset, dim] views with a unit-stride dim")
+    sb, sh, st = (s // esz for s in kc.strides[:3])
+    tab = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    B = len(lens)
+    if query_start is None:
+        qs, qs_ptr = None, None
+        if nq != B:
+            raise ValueError("one query row per sequence")
+    else:
+        qs = np.ascontiguousarray(query_start, dtype=np.int32)
+        if len(qs) != B + 1 or qs[-1] != nq:
+            raise ValueError("query_start must have num_seqs + 1 entries ending at the query row count")
+        qs_ptr = qs.ctypes.data
+    out = np.zeros((nq, num_heads, head_dim), dtype=np.float64)
+    kptr = kc.__array_interface__["data"][0]
+    vptr = vc.__array_interface__["data"][0]
+    threads = max(1, min(threads or default_threads(), B))
+
+    def run(a, b):
+        rc = lib.or_paged_attention_typed(out.ctypes.data, q.ctypes.data, q_dtype, kptr, vptr, int(kv_dtype),
+                                          float(k_scale), float(v_scale), tab.ctypes.data, lens.ctypes.data, qs_ptr,
+                                          B, num_heads, num_kv_heads, head_dim, block_size, tab.shape[1], sb, sh, st,
+                                          float(scale), a, b)
+        if rc != 0:
+            raise RuntimeError("oracle typed attention failed")
 
     bounds = np.linspace(0, B, threads + 1).astype(int)
     with ThreadPoolExecutor(max_workers=threads) as ex:

@@ -352,3 +352,154 @@ int or_paged_attention_causal(double *out, const uint16_t *query,
     }
     return 0;
 }
+
+/* ------------------------------------------------ other cache element types
+ *
+ * The pages store K and V in fp16 (deepsonar page, section 2.1: two bytes per
+ * element in the cache-size count).  The same attention is also computed over
+ * caches of bf16 or of one-byte fp8 codes (a cache element of half the size
+ * halves the bytes per token in that count).  These readers turn each stored
+ * element into its exact value, from the formats' definitions. */
+
+/* bfloat16 -> double: 1 sign bit, 8 exponent bits (bias 127), 7 fraction bits.
+ *   exponent 0       : subnormal, fraction * 2^-133
+ *   exponent 1..254  : (128 + fraction) * 2^(exponent-134)
+ *   exponent 255     : infinity (fraction 0) or NaN. */
+double or_bf16_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 7) & 0xff;
+    int frac = h & 0x7f;
+    double v;
+    if (expo == 0)
+        v = ldexp((double)frac, -133);
+    else if (expo == 255)
+        v = frac ? NAN : INFINITY;
+    else
+        v = ldexp((double)(128 + frac), expo - 134);
+    return sign ? -v : v;
+}
+
+/* FP8 E4M3 code -> double (the OCP 8-bit floating point E4M3 format): 1 sign
+ * bit, 4 exponent bits (bias 7), 3 fraction bits; no infinities.
+ *   exponent 0       : subnormal, fraction * 2^-9
+ *   exponent 1..15   : (8 + fraction) * 2^(exponent-10), except
+ *   exponent 15 with fraction 7: NaN.   Largest finite value 448. */
+double or_e4m3_to_double(uint8_t c)
+{
+    int sign = (c >> 7) & 1;
+    int expo = (c >> 3) & 0xf;
+    int frac = c & 0x7;
+    double v;
+    if (expo == 15 && frac == 7)
+        v = NAN;
+    else if (expo == 0)
+        v = ldexp((double)frac, -9);
+    else
+        v = ldexp((double)(8 + frac), expo - 10);
+    return sign ? -v : v;
+}
+
+enum { OR_F16 = 0, OR_BF16 = 1, OR_E4M3 = 2 };
+
+static double elem_value(const void *base, int64_t idx, int dtype)
+{
+    if (dtype == OR_E4M3)
+        return or_e4m3_to_double(((const uint8_t *)base)[idx]);
+    if (dtype == OR_BF16)
+        return or_bf16_to_double(((const uint16_t *)base)[idx]);
+    return or_half_to_double(((const uint16_t *)base)[idx]);
+}
+
+/* or_paged_attention_causal over caches of element type kv_dtype (0 fp16,
+ * 1 bf16, 2 fp8 E4M3) with query rows of type q_dtype (0 fp16, 1 bf16):
+ * cache element e stands for value(e) * k_scale in K and value(e) * v_scale
+ * in V.  query_start = NULL means one query row per sequence (the decode).
+ * Strides count elements.  Returns 0, or -1 on a bad argument. */
+int or_paged_attention_typed(double *out, const void *query, int q_dtype,
+                             const void *k_cache, const void *v_cache, int kv_dtype,
+                             double k_scale, double v_scale,
+                             const int32_t *block_tables, const int32_t *context_lens,
+                             const int32_t *query_start,
+                             int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                             int block_size, int max_blocks_per_seq,
+                             int64_t stride_block, int64_t stride_head, int64_t stride_token,
+                             double scale, int seq_begin, int seq_end)
+{
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        block_size <= 0 || seq_begin < 0 || seq_end > num_seqs)
+        return -1;
+    int group = num_heads / num_kv_heads;
+    for (int i = seq_begin; i < seq_end; ++i) {
+        int L = context_lens[i];
+        int64_t r0 = query_start ? query_start[i] : i;
+        int T = query_start ? query_start[i + 1] - query_start[i] : 1;
+        if (T <= 0)
+            continue;
+        if (L <= 0 && !query_start) {   /* decode of an empty context: zero row */
+            memset(out + r0 * num_heads * head_dim, 0, sizeof(double) * (size_t)num_heads * head_dim);
+            continue;
+        }
+        if (T > L)
+            return -1;
+        size_t n = (size_t)L * num_kv_heads * head_dim;
+        double *K = (double *)malloc(n * sizeof(double));
+        double *V = (double *)malloc(n * sizeof(double));
+        double *s = (double *)malloc((size_t)L * sizeof(double));
+        double *q = (double *)malloc((size_t)head_dim * sizeof(double));
+        if (!K || !V || !s || !q) {
+            free(K); free(V); free(s); free(q);
+            return -1;
+        }
+        /* gather positions 0 .. L-1 through the block table, as values */
+        const int32_t *table = block_tables + (int64_t)i * max_blocks_per_seq;
+        for (int t = 0; t < L; ++t) {
+            int64_t phys = table[t / block_size];
+            int64_t off = t % block_size;
+            for (int h = 0; h < num_kv_heads; ++h) {
+                int64_t base = phys * stride_block + h * stride_head + off * stride_token;
+                double *krow = K + ((int64_t)t * num_kv_heads + h) * head_dim;
+                double *vrow = V + ((int64_t)t * num_kv_heads + h) * head_dim;
+                for (int d = 0; d < head_dim; ++d) {
+                    krow[d] = elem_value(k_cache, base + d, kv_dtype) * k_scale;
+                    vrow[d] = elem_value(v_cache, base + d, kv_dtype) * v_scale;
+                }
+            }
+        }
+        for (int j = 0; j < T; ++j) {
+            int visible = L - T + j + 1;
+            int64_t row = r0 + j;
+            for (int h = 0; h < num_heads; ++h) {
+                int g = h / group;
+                for (int d = 0; d < head_dim; ++d)
+                    q[d] = elem_value(query, (row * num_heads + h) * head_dim + d, q_dtype);
+                double m = -INFINITY;
+                for (int t = 0; t < visible; ++t) {
+                    const double *k = K + ((int64_t)t * num_kv_heads + g) * head_dim;
+                    double dot = 0.0;
+                    for (int d = 0; d < head_dim; ++d)
+                        dot += q[d] * k[d];
+                    s[t] = scale * dot;
+                    if (s[t] > m)
+                        m = s[t];
+                }
+                double z = 0.0;
+                for (int t = 0; t < visible; ++t) {
+                    s[t] = exp(s[t] - m);
+                    z += s[t];
+                }
+                double *o = out + (row * num_heads + h) * head_dim;
+                for (int d = 0; d < head_dim; ++d)
+                    o[d] = 0.0;
+                for (int t = 0; t < visible; ++t) {
+                    double p = s[t] / z;
+                    const double *v = V + ((int64_t)t * num_kv_heads + g) * head_dim;
+                    for (int d = 0; d < head_dim; ++d)
+                        o[d] += p * v[d];
+                }
+            }
+        }
+        free(K); free(V); free(s); free(q);
+    }
+    return 0;
+}

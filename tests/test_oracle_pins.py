@@ -12,7 +12,12 @@ the oracle's own code.  CPU only.
   the mean of V; a score boosted by 64 selects its V row; zero length gives 0;
 * the split-context form with the log-sum-exp merge equals the unsplit form;
 * the multi-token causal form equals a masked brute force and, with one token
-  per sequence, the decode.
+  per sequence, the decode;
+* bf16 and fp8 E4M3 elements decode to the values their formats define
+  (every bf16 pattern through float32, the E4M3 values of the OCP definition),
+  E4M3 rounding takes ties to the even code and saturates at 448, and the
+  typed attention equals a brute force over the decoded values, with the K
+  scale on the scores and the V scale on the output.
 """
 import json
 import math
@@ -291,3 +296,152 @@ def test_causal_attention_pins():
     a = oracle.paged_attention_causal(q1, kc, vc, tab, ln, qs1, Hkv, bs, scale)
     b = oracle.paged_decode(q1, kc, vc, tab, ln, Hkv, bs, scale)
     assert np.array_equal(a, b)
+
+
+# ------------------------------------------------- bf16 and fp8 E4M3 caches
+
+def test_bf16_every_bit_pattern():
+    # bfloat16 is the top half of an IEEE binary32: reinterpret through float32
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    with np.errstate(invalid="ignore"):          # signalling NaN patterns
+        ref = (bits << 16).view(np.float32).astype(np.float64)
+    got = np.array([oracle.bf16_to_double(int(b)) for b in bits])
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan) and np.array_equal(got[~nan], ref[~nan])
+    assert oracle.bf16_to_double(0x3F80) == 1.0 and oracle.bf16_to_double(0xC000) == -2.0
+    assert oracle.bf16_to_double(0x0001) == 2.0 ** -133 and oracle.bf16_to_double(0x7F80) == math.inf
+    assert oracle.bf16_to_double(0x7F7F) == (2 - 2 ** -7) * 2.0 ** 127
+
+
+def test_e4m3_values_of_the_format():
+    v = oracle.e4m3_to_double
+    # values the OCP FP8 E4M3 definition fixes (S.EEEE.MMM, bias 7, no infinities)
+    assert v(0x38) == 1.0 and v(0xB8) == -1.0 and v(0x40) == 2.0 and v(0x3C) == 1.5
+    assert v(0x7E) == 448.0 and v(0xFE) == -448.0                   # largest finite: S.1111.110
+    assert v(0x08) == 2.0 ** -6 and v(0x07) == 0.875 * 2.0 ** -6    # smallest normal, largest subnormal
+    assert v(0x01) == 2.0 ** -9 and v(0x00) == 0.0                  # smallest subnormal
+    assert math.copysign(1.0, v(0x80)) == -1.0 and v(0x80) == 0.0
+    assert v(0x77) == 240.0 and v(0x78) == 256.0 and v(0x7D) == 416.0
+    assert math.isnan(v(0x7F)) and math.isnan(v(0xFF))
+    vals = [v(c) for c in range(0x7F)]
+    assert all(b > a for a, b in zip(vals, vals[1:]))                # codes 0 .. 0x7E increase
+    assert all(v(0x80 | c) == -v(c) for c in range(1, 0x7F))
+
+
+def test_e4m3_rounding_ties_and_saturation():
+    enc = lambda x: int(oracle.e4m3_encode(np.float32(x)))
+    assert enc(1.0) == 0x38 and enc(-1.0) == 0xB8 and enc(448.0) == 0x7E and enc(-448.0) == 0xFE
+    for big in (449.0, 464.0, 500.0, 1e6, np.inf):
+        assert enc(big) == 0x7E and enc(-big) == 0xFE
+    assert enc(np.nan) == 0x7F
+    assert enc(0.0) == 0x00 and enc(-0.0) == 0x80
+    # ties go to the even code
+    assert enc(2.0 ** -10) == 0x00            # halfway between 0 and 2^-9
+    assert enc(3 * 2.0 ** -10) == 0x02        # halfway between 2^-9 (0x01) and 2^-8 (0x02)
+    assert enc(1.0625) == 0x38 and enc(1.1875) == 0x3A
+    assert enc(1.0624) == 0x38 and enc(1.0626) == 0x39
+    assert enc(2.0 ** -11) == 0x00 and enc(-(2.0 ** -11)) == 0x80
+    # every finite code survives a round trip
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    vals = np.array([oracle.e4m3_to_double(int(c)) for c in codes], dtype=np.float32)
+    assert np.array_equal(oracle.e4m3_encode(vals), codes)
+    # random values land on the nearest representable value (brute force)
+    x = RNG.uniform(-460, 460, size=4000).astype(np.float32)
+    c = oracle.e4m3_encode(x)
+    table = np.array([oracle.e4m3_to_double(k) for k in range(0x7F)])
+    got = np.array([oracle.e4m3_to_double(int(k)) for k in c])
+    best = np.min(np.abs(np.abs(x.astype(np.float64))[:, None] - table[None, :]), axis=1)
+    assert np.all(np.abs(np.abs(got) - np.minimum(np.abs(x), 448.0)) <= best + 1e-12)
+
+
+def test_fp8_quantise_is_exact_on_representable_values():
+    codes = np.array([c for c in range(256) if (c & 0x7F) != 0x7F], dtype=np.uint8)
+    vals = np.array([oracle.e4m3_to_double(int(c)) for c in codes])
+    for scale in (1.0, 0.25, 8.0):                     # powers of two: x = value * scale is exact in fp16/fp32
+        x = (vals * scale).astype(np.float32)
+        ok = np.abs(x) <= 65504                         # fp16 inputs
+        assert np.array_equal(oracle.fp8_quantise(x[ok].astype(np.float16), scale), codes[ok])
+
+
+def _typed_case(kv_dtype, lens, T, H, Hkv, D, bs, rng):
+    """Contiguous per-sequence K/V values and the same data paged in a cache of
+    the given element type; returns (query, caches, tables, lens, qs, Kv, Vv)."""
+    q_bits = rand_fp16(sum(T), H, D, rng=rng)
+    if kv_dtype == oracle.KV_BF16:
+        q_bits = (q_bits.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        q_val = (q_bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    else:
+        q_val = q_bits.astype(np.float64)
+    Kraw, Vraw, Kv, Vv = [], [], [], []
+    for L in lens:
+        if kv_dtype == oracle.KV_FP8_E4M3:
+            k = rng.integers(0, 256, size=(L, Hkv, D)).astype(np.uint8)
+            v = rng.integers(0, 256, size=(L, Hkv, D)).astype(np.uint8)
+            k[(k & 0x7F) == 0x7F] = 0x30          # no NaN codes in real data
+            v[(v & 0x7F) == 0x7F] = 0x30
+            # values decoded by hand from the format: sign, 4-bit exponent (bias 7), 3-bit fraction
+            dec = lambda c: np.where((c >> 3) & 15, (8 + (c & 7)) * 2.0 ** (((c >> 3) & 15).astype(np.int64) - 10),
+                                     (c & 7) * 2.0 ** -9) * np.where(c >> 7, -1.0, 1.0)
+            Kv.append(dec(k)), Vv.append(dec(v))
+        elif kv_dtype == oracle.KV_BF16:
+            k = (rng.standard_normal((L, Hkv, D)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+            v = (rng.standard_normal((L, Hkv, D)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+            Kv.append((k.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+            Vv.append((v.astype(np.uint32) << 16).view(np.float32).astype(np.float64))
+        else:
+            k, v = rand_fp16(L, Hkv, D, rng=rng), rand_fp16(L, Hkv, D, rng=rng)
+            Kv.append(k.astype(np.float64)), Vv.append(v.astype(np.float64))
+        Kraw.append(k), Vraw.append(v)
+    # page with a fill pattern that is NaN in every format (unused slots)
+    fill = {oracle.KV_F16: np.float16(np.nan), oracle.KV_BF16: np.uint16(0x7FC0), oracle.KV_FP8_E4M3: np.uint8(0x7F)}
+    need = sum(-(-L // bs) for L in lens)
+    nb = need + 2
+    phys = rng.permutation(nb)[:need]
+    kc = np.full((nb, Hkv, bs, D), fill[kv_dtype], dtype=Kraw[0].dtype)
+    vc = np.full_like(kc, fill[kv_dtype])
+    tab = np.full((len(lens), max(1, max(-(-L // bs) for L in lens))), -1, dtype=np.int32)
+    j = 0
+    for i, L in enumerate(lens):
+        for lb in range(-(-L // bs)):
+            tab[i, lb] = phys[j]
+            t0, t1 = lb * bs, min(L, (lb + 1) * bs)
+            kc[phys[j], :, : t1 - t0] = Kraw[i][t0:t1].transpose(1, 0, 2)
+            vc[phys[j], :, : t1 - t0] = Vraw[i][t0:t1].transpose(1, 0, 2)
+            j += 1
+    qs = np.concatenate([[0], np.cumsum(T)]).astype(np.int32)
+    return q_bits, q_val, kc, vc, tab, np.array(lens, dtype=np.int32), qs, Kv, Vv
+
+
+@pytest.mark.parametrize("kv_dtype", [0, 1, 2])
+def test_typed_attention_equals_masked_bruteforce(kv_dtype):
+    H, Hkv, D, bs = 8, 2, 32, 8
+    lens, T = [1, 9, 30, 17], [1, 3, 5, 0]
+    rng = np.random.default_rng(77 + kv_dtype)
+    q_bits, q_val, kc, vc, tab, ln, qs, Kv, Vv = _typed_case(kv_dtype, lens, T, H, Hkv, D, bs, rng)
+    ks, vs = (0.02, 0.5) if kv_dtype == oracle.KV_FP8_E4M3 else (1.0, 1.0)
+    scale = 0.2
+    got = oracle.paged_attention_typed(q_bits, kc, vc, tab, ln, qs, Hkv, bs, scale, kv_dtype, ks, vs, threads=2)
+    for i, (L, t) in enumerate(zip(lens, T)):
+        for j in range(t):
+            vis = L - t + j + 1
+            for h in range(H):
+                s = scale * (Kv[i][:vis, h // 4, :] * ks) @ q_val[qs[i] + j, h]
+                p = np.exp(s - s.max())
+                p /= p.sum()
+                assert np.max(np.abs(got[qs[i] + j, h] - p @ (Vv[i][:vis, h // 4, :] * vs))) < 1e-12
+
+
+def test_typed_attention_reduces_to_fp16_forms_and_scales():
+    lens = [40, 7, 100]
+    q, Ks, Vs = make_case(lens, 8, 2, 64)
+    kc, vc, tab, ln = page_sequences(Ks, Vs, 16, RNG)
+    a = oracle.paged_attention_typed(q, kc, vc, tab, ln, None, 2, 16, 0.125, oracle.KV_F16)
+    assert np.array_equal(a, oracle.paged_decode(q, kc, vc, tab, ln, 2, 16, 0.125))
+    qm = rand_fp16(6, 8, 64)
+    qs = np.array([0, 2, 3, 6], dtype=np.int32)
+    b = oracle.paged_attention_typed(qm, kc, vc, tab, ln, qs, 2, 16, 0.125, oracle.KV_F16)
+    assert np.array_equal(b, oracle.paged_attention_causal(qm, kc, vc, tab, ln, qs, 2, 16, 0.125))
+    # k_scale multiplies every score, v_scale the output (closed forms)
+    c = oracle.paged_attention_typed(q, kc, vc, tab, ln, None, 2, 16, 0.125, oracle.KV_F16, 2.0, 3.0)
+    d = oracle.paged_attention_typed(q, kc, vc, tab, ln, None, 2, 16, 0.25, oracle.KV_F16)
+    assert np.max(np.abs(c - 3.0 * d)) < 1e-12
