@@ -66,6 +66,20 @@ enum {
     PA_ERR_TIMEOUT = -7        /* a kernel gave up waiting on its own copies (see pa_workspace_status) */
 };
 
+/* Element type of the K and V caches (the "typed" calls below).  The pages
+ * keep the cache in fp16 (deepsonar page section 2.1: two bytes per element
+ * in the cache-size count); bf16 keeps two bytes, fp8 E4M3 halves them.
+ *   PA_KV_F16       fp16 cache; fp16 query and output
+ *   PA_KV_BF16      bf16 cache; bf16 query and output
+ *   PA_KV_FP8_E4M3  one-byte FP8 E4M3 codes (OCP format); fp16 query and
+ *                   output; a K code c stands for e4m3(c) * k_scale, a V code
+ *                   for e4m3(c) * v_scale (one scale per cache, host floats) */
+enum {
+    PA_KV_F16 = 0,
+    PA_KV_BF16 = 1,
+    PA_KV_FP8_E4M3 = 2
+};
+
 /* Static text for a status code (never NULL). */
 PA_API const char *pa_status_string(int status);
 
@@ -233,6 +247,50 @@ PA_API int pa_attention_causal(uint16_t *out, const uint16_t *query, const uint1
                                int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
                                int max_blocks_per_seq, int max_context_len, float scale, void *workspace,
                                size_t workspace_bytes, void *stream);
+
+/* ----------------------------------------- bf16 and fp8 E4M3 caches (typed) */
+
+/* Quantising KV write into caches of one-byte FP8 E4M3 codes
+ * (uint8 [num_blocks][num_kv_heads][block_size][head_dim]).  Each fp16
+ * element x of key[t] / value[t] is stored at slot slot_mapping[t] as the
+ * code of fl32(x * fl32(1 / scale)) (scale = k_scale or v_scale, the
+ * reciprocal taken once in float on the host), rounded to the nearest E4M3
+ * value with ties to the even code and saturated at +-448 (NaN stays NaN).
+ * Slots as in pa_kv_write.  head_dim a multiple of 8, scales positive and
+ * finite.  (A bf16 cache takes bf16 rows through pa_kv_write, which copies
+ * 16-bit elements whatever their type.) */
+PA_API int pa_kv_write_fp8(const uint16_t *key, const uint16_t *value, const int64_t *slot_mapping,
+                           uint8_t *k_cache, uint8_t *v_cache, int num_tokens, int num_kv_heads, int head_dim,
+                           int block_size, int64_t num_blocks, float k_scale, float v_scale, void *stream);
+
+/* pa_block_copy for a cache of element type kv_dtype (PA_KV_*); for fp8
+ * head_dim must be a multiple of 16. */
+PA_API int pa_block_copy_typed(void *k_cache, void *v_cache, const int64_t *pairs, int num_pairs,
+                               int num_kv_heads, int head_dim, int block_size, int64_t num_blocks, int kv_dtype,
+                               void *stream);
+
+/* pa_decode over a cache of element type kv_dtype (PA_KV_*): out and query
+ * are bf16 for PA_KV_BF16, fp16 otherwise.  For PA_KV_FP8_E4M3 a K code c
+ * stands for e4m3(c) * k_scale and a V code for e4m3(c) * v_scale (both
+ * positive and finite; head_dim 128); the scales are ignored for the 16-bit
+ * types.  MMA operands are fp16 (fp8 codes are turned into their exact fp16
+ * values) or bf16, accumulation fp32.  Workspace: pa_decode_workspace_size.
+ * PA_ERR_UNSUPPORTED for an fp8 cache with head_dim 64. */
+PA_API int pa_decode_typed(void *out, const void *query, const void *k_cache, const void *v_cache,
+                           const int32_t *block_tables, const int32_t *context_lens, int num_seqs, int num_heads,
+                           int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                           int max_blocks_per_seq, int max_context_len, float scale, int kv_dtype, float k_scale,
+                           float v_scale, void *workspace, size_t workspace_bytes, void *stream);
+
+/* pa_attention_causal over a cache of element type kv_dtype, as
+ * pa_decode_typed.  Workspace: pa_attention_causal_workspace_size. */
+PA_API int pa_attention_causal_typed(void *out, const void *query, const void *k_cache, const void *v_cache,
+                                     const int32_t *block_tables, const int32_t *context_lens,
+                                     const int32_t *query_start, int num_seqs, int num_query_tokens, int num_heads,
+                                     int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                                     int max_blocks_per_seq, int max_context_len, float scale, int kv_dtype,
+                                     float k_scale, float v_scale, void *workspace, size_t workspace_bytes,
+                                     void *stream);
 
 /* Read the error word a pa_decode call left in its workspace: PA_OK, or
  * PA_ERR_TIMEOUT if a kernel gave up waiting for its own copies into shared

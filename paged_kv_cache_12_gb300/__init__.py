@@ -40,8 +40,12 @@ EXPORTS = (
     "pa_alloc_stats", "pa_decode_static_ws", "pa_alloc_free_queue", "pa_alloc_enable_prefix_cache",
     "pa_alloc_match_prefix", "pa_alloc_append_ids", "pa_alloc_block_hash", "pa_alloc_prefix_stats", "pa_sha256",
     "pa_decode_shared_prefix_workspace_size", "pa_decode_shared_prefix", "pa_selftest_wait_timeout",
-    "pa_attention_causal_workspace_size", "pa_attention_causal",
+    "pa_attention_causal_workspace_size", "pa_attention_causal", "pa_kv_write_fp8", "pa_block_copy_typed",
+    "pa_decode_typed", "pa_attention_causal_typed",
 )
+
+# cache element types (PA_KV_* in pa.h)
+PA_KV_F16, PA_KV_BF16, PA_KV_FP8_E4M3 = 0, 1, 2
 
 # bytes of the library's built-in scratch array used by pa_decode_static_ws
 PA_DECODE_STATIC_WS_BYTES = 64 << 20
@@ -101,6 +105,13 @@ def lib():
             "pa_decode_shared_prefix": ([vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, i32, i32,
                                          ctypes.c_float, vp, sz, vp], i32),
             "pa_attention_causal_workspace_size": ([i32, i32, i32, i32, i32, i32], sz),
+            "pa_kv_write_fp8": ([vp, vp, vp, vp, vp, i32, i32, i32, i32, i64, ctypes.c_float, ctypes.c_float, vp],
+                                i32),
+            "pa_block_copy_typed": ([vp, vp, vp, i32, i32, i32, i32, i64, i32, vp], i32),
+            "pa_decode_typed": ([vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, i32, i32, ctypes.c_float, i32,
+                                 ctypes.c_float, ctypes.c_float, vp, sz, vp], i32),
+            "pa_attention_causal_typed": ([vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i64, i32, i32,
+                                           ctypes.c_float, i32, ctypes.c_float, ctypes.c_float, vp, sz, vp], i32),
             "pa_attention_causal": ([vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i64, i32, i32,
                                      ctypes.c_float, vp, sz, vp], i32),
         }
@@ -148,12 +159,15 @@ def _need(t, dtype, ndim, name):
 
 
 def pa_kv_write(key, value, slot_mapping, k_cache, v_cache, stream=None):
-    """Store key[t], value[t] at slot slot_mapping[t] of the caches (slot < 0: skipped)."""
+    """Store key[t], value[t] at slot slot_mapping[t] of the caches (slot < 0:
+    skipped); fp16 rows into fp16 caches or bf16 rows into bf16 caches (a copy
+    of 16-bit elements either way)."""
     import torch
-    _need(k_cache, torch.float16, 4, "k_cache")
-    _need(v_cache, torch.float16, 4, "v_cache")
-    _need(key, torch.float16, 3, "key")
-    _need(value, torch.float16, 3, "value")
+    dt = torch.bfloat16 if k_cache.dtype == torch.bfloat16 else torch.float16
+    _need(k_cache, dt, 4, "k_cache")
+    _need(v_cache, dt, 4, "v_cache")
+    _need(key, dt, 3, "key")
+    _need(value, dt, 3, "value")
     _need(slot_mapping, torch.int64, 1, "slot_mapping")
     nb, hkv, bs, d = k_cache.shape
     if v_cache.shape != k_cache.shape or key.shape != value.shape or key.shape[1:] != (hkv, d) \
@@ -163,17 +177,116 @@ def pa_kv_write(key, value, slot_mapping, k_cache, v_cache, stream=None):
                              v_cache.data_ptr(), key.shape[0], hkv, d, bs, nb, _stream(stream)), "pa_kv_write")
 
 
-def pa_block_copy(k_cache, v_cache, pairs, stream=None):
-    """Copy every (src, dst) block pair of int64 ``pairs`` [n, 2], K and V."""
+def kv_dtype_of(cache) -> int:
+    """PA_KV_* of a cache tensor: float16, bfloat16, or one-byte E4M3 codes
+    (uint8 or torch.float8_e4m3fn)."""
     import torch
-    _need(k_cache, torch.float16, 4, "k_cache")
-    _need(v_cache, torch.float16, 4, "v_cache")
+    if cache.dtype == torch.float16:
+        return PA_KV_F16
+    if cache.dtype == torch.bfloat16:
+        return PA_KV_BF16
+    if cache.dtype == torch.uint8 or cache.dtype == getattr(torch, "float8_e4m3fn", None):
+        return PA_KV_FP8_E4M3
+    raise ValueError(f"unsupported cache dtype {cache.dtype}")
+
+
+def _need_cache(t, name, kv):
+    import torch
+    want = {PA_KV_F16: (torch.float16,), PA_KV_BF16: (torch.bfloat16,),
+            PA_KV_FP8_E4M3: (torch.uint8, getattr(torch, "float8_e4m3fn", torch.uint8))}[kv]
+    if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype not in want or t.dim() != 4 \
+            or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous 4-d CUDA cache tensor of {want[0]}")
+
+
+def pa_block_copy(k_cache, v_cache, pairs, stream=None):
+    """Copy every (src, dst) block pair of int64 ``pairs`` [n, 2], K and V
+    (caches of fp16, bf16 or fp8 codes)."""
+    import torch
+    kv = kv_dtype_of(k_cache)
+    _need_cache(k_cache, "k_cache", kv)
+    _need_cache(v_cache, "v_cache", kv)
     _need(pairs, torch.int64, 2, "pairs")
     nb, hkv, bs, d = k_cache.shape
     if v_cache.shape != k_cache.shape or pairs.shape[1] != 2:
         raise ValueError("pa_block_copy: shape mismatch")
-    _check(lib().pa_block_copy(k_cache.data_ptr(), v_cache.data_ptr(), pairs.data_ptr(), pairs.shape[0], hkv, d, bs,
-                               nb, _stream(stream)), "pa_block_copy")
+    if kv == PA_KV_F16:
+        _check(lib().pa_block_copy(k_cache.data_ptr(), v_cache.data_ptr(), pairs.data_ptr(), pairs.shape[0], hkv, d,
+                                   bs, nb, _stream(stream)), "pa_block_copy")
+    else:
+        _check(lib().pa_block_copy_typed(k_cache.data_ptr(), v_cache.data_ptr(), pairs.data_ptr(), pairs.shape[0],
+                                         hkv, d, bs, nb, kv, _stream(stream)), "pa_block_copy_typed")
+
+
+def pa_kv_write_fp8(key, value, slot_mapping, k_cache, v_cache, k_scale, v_scale, stream=None):
+    """Quantise fp16 key/value rows into caches of FP8 E4M3 codes (uint8 or
+    float8_e4m3fn tensors): code = E4M3(fl32(x * fl32(1 / scale))), nearest
+    value, ties to even, saturating at 448."""
+    import torch
+    _need_cache(k_cache, "k_cache", PA_KV_FP8_E4M3)
+    _need_cache(v_cache, "v_cache", PA_KV_FP8_E4M3)
+    _need(key, torch.float16, 3, "key")
+    _need(value, torch.float16, 3, "value")
+    _need(slot_mapping, torch.int64, 1, "slot_mapping")
+    nb, hkv, bs, d = k_cache.shape
+    if v_cache.shape != k_cache.shape or key.shape != value.shape or key.shape[1:] != (hkv, d) \
+            or slot_mapping.shape[0] != key.shape[0]:
+        raise ValueError("pa_kv_write_fp8: shape mismatch")
+    _check(lib().pa_kv_write_fp8(key.data_ptr(), value.data_ptr(), slot_mapping.data_ptr(), k_cache.data_ptr(),
+                                 v_cache.data_ptr(), key.shape[0], hkv, d, bs, nb, float(k_scale), float(v_scale),
+                                 _stream(stream)), "pa_kv_write_fp8")
+
+
+def pa_decode_typed(out, query, k_cache, v_cache, block_tables, context_lens, scale, max_context_len, workspace,
+                    k_scale=1.0, v_scale=1.0, stream=None):
+    """pa_decode over a cache of fp16, bf16 (bf16 query/out) or fp8 E4M3 codes
+    (fp16 query/out; a code stands for its value times k_scale or v_scale).
+    Workspace: pa_decode_workspace_size."""
+    import torch
+    kv = kv_dtype_of(k_cache)
+    qdt = torch.bfloat16 if kv == PA_KV_BF16 else torch.float16
+    _need_cache(k_cache, "k_cache", kv)
+    _need_cache(v_cache, "v_cache", kv)
+    for t, dt, nd, nm in ((out, qdt, 3, "out"), (query, qdt, 3, "query"),
+                          (block_tables, torch.int32, 2, "block_tables"), (context_lens, torch.int32, 1, "context_lens"),
+                          (workspace, torch.uint8, 1, "workspace")):
+        _need(t, dt, nd, nm)
+    nb, hkv, bs, d = k_cache.shape
+    B, hq, d2 = query.shape
+    if out.shape != query.shape or d2 != d or v_cache.shape != k_cache.shape or block_tables.shape[0] != B \
+            or context_lens.shape[0] != B:
+        raise ValueError("pa_decode_typed: shape mismatch")
+    _check(lib().pa_decode_typed(out.data_ptr(), query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                 block_tables.data_ptr(), context_lens.data_ptr(), B, hq, hkv, d, bs, nb,
+                                 block_tables.shape[1], int(max_context_len), float(scale), kv, float(k_scale),
+                                 float(v_scale), workspace.data_ptr(), workspace.numel(), _stream(stream)),
+           "pa_decode_typed")
+
+
+def pa_attention_causal_typed(out, query, k_cache, v_cache, block_tables, context_lens, query_start, scale,
+                              max_context_len, workspace, k_scale=1.0, v_scale=1.0, stream=None):
+    """pa_attention_causal over a cache of fp16, bf16 or fp8 E4M3 codes (as
+    pa_decode_typed).  Workspace: pa_attention_causal_workspace_size."""
+    import torch
+    kv = kv_dtype_of(k_cache)
+    qdt = torch.bfloat16 if kv == PA_KV_BF16 else torch.float16
+    _need_cache(k_cache, "k_cache", kv)
+    _need_cache(v_cache, "v_cache", kv)
+    for t, dt, nd, nm in ((out, qdt, 3, "out"), (query, qdt, 3, "query"),
+                          (block_tables, torch.int32, 2, "block_tables"), (context_lens, torch.int32, 1, "context_lens"),
+                          (query_start, torch.int32, 1, "query_start"), (workspace, torch.uint8, 1, "workspace")):
+        _need(t, dt, nd, nm)
+    nb, hkv, bs, d = k_cache.shape
+    nq, hq, d2 = query.shape
+    B = context_lens.shape[0]
+    if out.shape != query.shape or d2 != d or v_cache.shape != k_cache.shape or block_tables.shape[0] != B \
+            or query_start.shape[0] != B + 1:
+        raise ValueError("pa_attention_causal_typed: shape mismatch")
+    _check(lib().pa_attention_causal_typed(out.data_ptr(), query.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                           block_tables.data_ptr(), context_lens.data_ptr(), query_start.data_ptr(),
+                                           B, nq, hq, hkv, d, bs, nb, block_tables.shape[1], int(max_context_len),
+                                           float(scale), kv, float(k_scale), float(v_scale), workspace.data_ptr(),
+                                           workspace.numel(), _stream(stream)), "pa_attention_causal_typed")
 
 
 def pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len) -> int:
