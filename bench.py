@@ -56,6 +56,8 @@ def parse():
     p.add_argument("--workload", default=WORKLOAD,
                    help="gqa72b (the headline), mha7b, mix, cow16, cow32, tiny; several tokens per sequence: "
                         "spec72b, chunked")
+    p.add_argument("--kv-dtype", choices=["f16", "bf16", "fp8"], default="f16",
+                   help="cache element type: fp16 (the pages'), bf16, or fp8 E4M3 codes with one scale per cache")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="skip the CUDA Graph replay measurement")
     p.add_argument("--shared-prefix", action="store_true",
@@ -87,12 +89,40 @@ def job_tokens_per_s(world: int, seqs: int, steps: int, max_ms: float) -> float:
     return world * seqs * steps / (max_ms / 1e3)
 
 
-def decode_bytes(w) -> int:
+KV_CODES = {"f16": 0, "bf16": 1, "fp8": 2}
+FP8_SCALES = (1.0 / 64, 1.0 / 32)      # K and V scales of the fp8 caches (N(0, 1) data spans about +-5)
+
+
+def inputs(w, kv_dtype):
+    """Host arrays of the step in the cache's element type: (k_pool, v_pool,
+    query, query_multi, new_key, new_value).  bf16: the fp16 draws truncated to
+    bf16 patterns; fp8: seeded random finite E4M3 codes for the pools (any codes
+    serve as cache content) and fp16 queries and new rows (quantised by the
+    write)."""
+    if kv_dtype == "f16":
+        return w.k_pool, w.v_pool, w.query, w.query_multi, w.new_key, w.new_value
+    if kv_dtype == "bf16":
+        bf = lambda x: (np.asarray(x, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        return (bf(w.k_pool), bf(w.v_pool), bf(w.query), bf(w.query_multi), bf(w.new_key), bf(w.new_value))
+    shape = (w.num_blocks, w.num_kv_heads, w.block_size, w.head_dim)
+    pools = []
+    for stream in (1, 2):
+        c = np.random.default_rng([w.seed, stream]).integers(0, 256, size=shape, dtype=np.uint8)
+        c[(c & 0x7F) == 0x7F] = 0x38
+        pools.append(c)
+    return pools[0], pools[1], w.query, w.query_multi, w.new_key, w.new_value
+
+
+def elem_bytes(kv_dtype) -> int:
+    return 1 if kv_dtype == "fp8" else 2
+
+
+def decode_bytes(w, esz=2) -> int:
     """Algorithmic bytes of one decode over the workload: every context token's
     K and V rows, the query, the output, the block-table entries the contexts
     need and the lengths."""
     L = w.context_lens.astype(np.int64)
-    kv = int((L * 2 * w.num_kv_heads * w.head_dim * 2).sum())
+    kv = int((L * 2 * w.num_kv_heads * w.head_dim * esz).sum())
     qo = 2 * w.num_seqs * w.num_heads * w.head_dim * 2
     tables = int((-(-L // w.block_size)).sum()) * 4
     return kv + qo + tables + 4 * w.num_seqs
@@ -102,12 +132,12 @@ def multi_token(w) -> bool:
     return bool(w.num_seqs) and not bool((w.new_counts == 1).all())
 
 
-def causal_bytes(w) -> int:
+def causal_bytes(w, esz=2) -> int:
     """Algorithmic bytes of one multi-token call: every context token's K and
     V rows once per sequence (its new tokens share them), every query and
     output row, the block-table entries and the lengths and query offsets."""
     L = w.context_lens.astype(np.int64)
-    kv = int((L * 2 * w.num_kv_heads * w.head_dim * 2).sum())
+    kv = int((L * 2 * w.num_kv_heads * w.head_dim * esz).sum())
     qo = 2 * w.num_new_tokens * w.num_heads * w.head_dim * 2
     tables = int((-(-L // w.block_size)).sum()) * 4
     return kv + qo + tables + 4 * (2 * w.num_seqs + 1)
@@ -122,9 +152,13 @@ def causal_flops(w) -> int:
     return int(4 * seen * w.num_heads * w.head_dim)
 
 
-def kv_write_bytes(w) -> int:
+def kv_write_bytes(w, esz=2) -> int:
+    """fp16/bf16 rows read, cache elements written, slots read."""
     T = w.num_new_tokens
-    return 2 * (2 * T * w.num_kv_heads * w.head_dim * 2) + 8 * T
+    return 2 * (T * w.num_kv_heads * w.head_dim * (2 + esz)) + 8 * T
+
+
+KERNEL_SOURCES = ("decode_common.cuh", "decode.cu", "common.cuh")   # what the fp16 decode kernel is built from
 
 
 def kernel_traffic():
@@ -134,7 +168,7 @@ def kernel_traffic():
     try:
         rec = json.load(open(os.path.join(ROOT, "profiles", "decode_kernel_traffic.json")))
         src = b"".join(open(os.path.join(ROOT, "paged_kv_cache_12_gb300", "csrc", f), "rb").read()
-                       for f in ("decode.cu", "common.cuh"))
+                       for f in KERNEL_SOURCES)
         if hashlib.sha256(src).hexdigest() == rec["source_sha256"]:
             return int(rec["dram_bytes_per_launch"])
     except Exception:
@@ -207,9 +241,11 @@ class OracleSample:
     workload: the first n of its sequences, one layer, on all host cores.
     n is calibrated once so that one timed call takes about `target_s`."""
 
-    def __init__(self, w, tables, lens, target_s):
+    def __init__(self, w, tables, lens, target_s, kv_dtype="f16"):
         import oracle
         self.oracle, self.w, self.tables, self.lens = oracle, w, tables, lens
+        self.kv_dtype = kv_dtype
+        self.kpool, self.vpool, self.q, self.qm, _, _ = inputs(w, kv_dtype)
         self.threads = oracle.default_threads()
         self.multi = multi_token(w)
         # multi-token steps: sequences in index order, leaving out any one whose
@@ -238,17 +274,23 @@ class OracleSample:
     def run(self, n):
         w = self.w
         t0 = time.perf_counter()
+        kv = KV_CODES[self.kv_dtype]
+        ks, vs = FP8_SCALES if self.kv_dtype == "fp8" else (1.0, 1.0)
         if self.multi:
             idx = np.asarray(self.order[:n])
             qs = w.query_start
             rows = np.concatenate([np.arange(qs[i], qs[i + 1]) for i in idx])
             sub_qs = np.concatenate([[0], np.cumsum(qs[idx + 1] - qs[idx])]).astype(np.int32)
-            self.oracle.paged_attention_causal(w.query_multi[rows], w.k_pool, w.v_pool, self.tables[idx],
-                                               self.lens[idx], sub_qs, w.num_kv_heads, w.block_size, w.scale,
-                                               threads=self.threads)
-        else:
+            self.oracle.paged_attention_typed(self.qm[rows], self.kpool, self.vpool, self.tables[idx],
+                                              self.lens[idx], sub_qs, w.num_kv_heads, w.block_size, w.scale, kv,
+                                              ks, vs, threads=self.threads)
+        elif self.kv_dtype == "f16":
             self.oracle.paged_decode(w.query, w.k_pool, w.v_pool, self.tables, self.lens, w.num_kv_heads,
                                      w.block_size, w.scale, threads=self.threads, seq_range=(0, n))
+        else:
+            self.oracle.paged_attention_typed(self.q[:n], self.kpool, self.vpool, self.tables[:n], self.lens[:n],
+                                              None, w.num_kv_heads, w.block_size, w.scale, kv, ks, vs,
+                                              threads=self.threads)
         return time.perf_counter() - t0
 
     def rate(self, layers=LAYERS):
@@ -353,12 +395,19 @@ def run_ours(args):
 
     # ---- device-resident inputs
     multi = multi_token(w)
-    q_host = w.query_multi if multi else w.query
-    k = torch.from_numpy(w.k_pool).to(dev)
-    v = torch.from_numpy(w.v_pool).to(dev)
-    q = torch.from_numpy(q_host).to(dev)
-    nk = torch.from_numpy(w.new_key).to(dev)
-    nv = torch.from_numpy(w.new_value).to(dev)
+    kvd = args.kv_dtype
+    kpool, vpool, q1, qmulti, nk_host, nv_host = inputs(w, kvd)
+    q_host = qmulti if multi else q1
+    cache_dt = {"f16": torch.float16, "bf16": torch.bfloat16, "fp8": torch.uint8}[kvd]
+    row_dt = torch.bfloat16 if kvd == "bf16" else torch.float16
+    dv = lambda a, dt: torch.from_numpy(np.ascontiguousarray(a)).to(dev).view(dt)
+    k = dv(kpool, cache_dt)
+    v = dv(vpool, cache_dt)
+    q = dv(q_host, row_dt)
+    nk = dv(nk_host, row_dt)
+    nv = dv(nv_host, row_dt)
+    ks, vs = FP8_SCALES if kvd == "fp8" else (1.0, 1.0)
+    typed = kvd != "f16"
     d_slots = torch.from_numpy(slots).to(dev)
     d_pairs = torch.from_numpy(np.ascontiguousarray(pairs)).to(dev)
     d_tables = torch.from_numpy(tables).to(dev)
@@ -383,11 +432,19 @@ def run_ours(args):
     def writes_on(st):
         if has_pairs:
             pa.pa_block_copy(k, v, d_pairs, st)
-        pa.pa_kv_write(nk, nv, d_slots, k, v, st)
+        if kvd == "fp8":
+            pa.pa_kv_write_fp8(nk, nv, d_slots, k, v, ks, vs, st)
+        else:
+            pa.pa_kv_write(nk, nv, d_slots, k, v, st)
 
     def decode_on(st):
-        if multi:
+        if multi and typed:
+            pa.pa_attention_causal_typed(out, q, k, v, d_tables, d_lens, d_qs, w.scale, w.max_context_len, ws, ks, vs,
+                                         st)
+        elif multi:
             pa.pa_attention_causal(out, q, k, v, d_tables, d_lens, d_qs, w.scale, w.max_context_len, ws, st)
+        elif typed:
+            pa.pa_decode_typed(out, q, k, v, d_tables, d_lens, w.scale, w.max_context_len, ws, ks, vs, st)
         elif shared_mode:
             pa.pa_decode_shared_prefix(out, q, k, v, d_tables, d_lens, d_lead, d_shl, w.scale, w.max_context_len, ws,
                                        st)
@@ -460,10 +517,10 @@ def run_ours(args):
     h_lens = torch.from_numpy(lens).pin_memory()
     h_slots = torch.from_numpy(slots).pin_memory()
     h_pairs = torch.from_numpy(np.ascontiguousarray(pairs)).pin_memory()
-    h_q = torch.from_numpy(np.ascontiguousarray(q_host)).pin_memory()
+    h_q = torch.from_numpy(np.ascontiguousarray(q_host)).pin_memory().view(row_dt)
     h_qs = torch.from_numpy(w.query_start).pin_memory() if multi else None
-    h_nk = torch.from_numpy(np.ascontiguousarray(w.new_key)).pin_memory()
-    h_nv = torch.from_numpy(np.ascontiguousarray(w.new_value)).pin_memory()
+    h_nk = torch.from_numpy(np.ascontiguousarray(nk_host)).pin_memory().view(row_dt)
+    h_nv = torch.from_numpy(np.ascontiguousarray(nv_host)).pin_memory().view(row_dt)
     h_out = torch.empty((layers,) + tuple(out.shape), dtype=out.dtype).pin_memory()
 
     def e2e_step():
@@ -505,9 +562,10 @@ def run_ours(args):
     # ---- numbers
     B = w.num_new_tokens if multi else w.num_seqs      # query tokens computed per layer step
     tok_s = job_tokens_per_s(world, B, args.steps, total_ms)
-    dbytes = causal_bytes(w) if multi else decode_bytes(w)
-    step_bytes = layers * (dbytes + kv_write_bytes(w) + (2 * len(pairs) * w.num_kv_heads * w.block_size *
-                                                        w.head_dim * 2 * 2))
+    esz = elem_bytes(kvd)
+    dbytes = causal_bytes(w, esz) if multi else decode_bytes(w, esz)
+    step_bytes = layers * (dbytes + kv_write_bytes(w, esz) + (2 * len(pairs) * w.num_kv_heads * w.block_size *
+                                                        w.head_dim * esz * 2))
     kv_gbs = world * step_bytes * args.steps / (total_ms / 1e3) / 1e9
     dec_avg_ms = statistics.mean(dec_ms)
     achieved = dbytes / (dec_avg_ms / 1e3) / 1e9
@@ -530,13 +588,13 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16",
+        "dtype": {"f16": "f16", "bf16": "bf16", "fp8": "fp8_e4m3 cache, f16 MMA"}[kvd],
         "data": "synthetic",
         "config": {
             "workload": describe(w, layers),
             "num_seqs": w.num_seqs, "context_len_max": int(w.context_lens.max()), "num_heads": w.num_heads,
             "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-            "layers": layers, "parallelism": f"replicas x{world}",
+            "layers": layers, "parallelism": f"replicas x{world}", "kv_dtype": kvd,
             "l2": f"K/V read per layer {dbytes / 1e9:.2f} GB vs 129 MB L2; no flush",
         },
         "kv_gbs": round(kv_gbs, 1),
@@ -580,7 +638,7 @@ def run_ours(args):
         line["copy_pairs"] = int(len(pairs))
         line["decode_call"] = "pa_decode_shared_prefix" if shared_mode else "pa_decode"
     if not args.no_cpu_baseline and world == 1 and not w.num_prompts:
-        smp = OracleSample(w, tables, lens, target_s=10.0)
+        smp = OracleSample(w, tables, lens, target_s=10.0, kv_dtype=kvd)
         rate, secs = smp.rate(layers)
         line["cpu_baseline"] = {"value": round(rate, 6), "unit": "tokens/s", "cores": smp.threads, "kind": "oracle",
                                 "sample": smp.describe(secs, layers)}

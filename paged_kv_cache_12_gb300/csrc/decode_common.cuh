@@ -18,6 +18,12 @@
 #ifndef PA_DECODE_DEPTH
 #define PA_DECODE_DEPTH 2
 #endif
+#ifndef PA_DECODE_MINB_FP8
+#define PA_DECODE_MINB_FP8 6
+#endif
+#ifndef PA_FP8_LATE_V
+#define PA_FP8_LATE_V 0
+#endif
 #ifndef PA_DECODE_MINB_WIDE
 #define PA_DECODE_MINB_WIDE 4
 #endif
@@ -730,7 +736,9 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
             }
             // V^T fragments, loaded ahead of the softmax
             uint32_t va[MT][4];
-            if constexpr (C::FP8) {
+            if constexpr (C::FP8 && PA_FP8_LATE_V) {
+                // converted just before their MMAs (below)
+            } else if constexpr (C::FP8) {
                 // transposed 8 x 8 loads of 16-bit pairs: per thread, tokens
                 // 2 cq and 2 cq + 1, dims 2 r and 2 r + 1 of a 16-byte chunk; the
                 // byte permutation regroups them by dim, so m-tile i holds
@@ -808,24 +816,51 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                 pb[t][0] = movmatrix_trans(pack_p<KV>(p0, p1));
                 pb[t][1] = movmatrix_trans(pack_p<KV>(p2, p3));
             }
-            if (tail) {   // stale or poisoned slots past the context must not reach O
-                const uint32_t lo = (2 * cq < ntok ? 0x0000ffffu : 0u) | (2 * cq + 1 < ntok ? 0xffff0000u : 0u);
-                const uint32_t hi = (2 * cq + 8 < ntok ? 0x0000ffffu : 0u) | (2 * cq + 9 < ntok ? 0xffff0000u : 0u);
+            const uint32_t vlo = (2 * cq < ntok ? 0x0000ffffu : 0u) | (2 * cq + 1 < ntok ? 0xffff0000u : 0u);
+            const uint32_t vhi = (2 * cq + 8 < ntok ? 0x0000ffffu : 0u) | (2 * cq + 9 < ntok ? 0xffff0000u : 0u);
+            if constexpr (C::FP8 && PA_FP8_LATE_V) {
+                // V^T fragments of an fp8 tile (layout as in the early path),
+                // converted just before their MMAs to keep few registers live
 #pragma unroll
-                for (int i = 0; i < MT; ++i) {
-                    va[i][0] &= lo;
-                    va[i][1] &= lo;
-                    va[i][2] &= hi;
-                    va[i][3] &= hi;
+                for (int u = 0; u < MT / 2; ++u) {
+                    uint32_t r4[4];
+                    ldmatrix_x4_trans(vt + koff[u], r4[0], r4[1], r4[2], r4[3]);
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t lo = __byte_perm(r4[2 * h], 0, 0x3120);
+                        const uint32_t hi = __byte_perm(r4[2 * h + 1], 0, 0x3120);
+                        uint32_t f[4] = {e4m3x2_to_f16x2(lo), e4m3x2_to_f16x2(lo >> 16), e4m3x2_to_f16x2(hi),
+                                         e4m3x2_to_f16x2(hi >> 16)};
+                        if (tail) {
+                            f[0] &= vlo;
+                            f[1] &= vlo;
+                            f[2] &= vhi;
+                            f[3] &= vhi;
+                        }
+#pragma unroll
+                        for (int t = 0; t < NT; ++t)
+                            mma_kv<KV>(acc[2 * u + h][t][0], acc[2 * u + h][t][1], acc[2 * u + h][t][2],
+                                       acc[2 * u + h][t][3], f[0], f[1], f[2], f[3], pb[t][0], pb[t][1]);
+                    }
                 }
+            } else {
+                if (tail) {   // stale or poisoned slots past the context must not reach O
+#pragma unroll
+                    for (int i = 0; i < MT; ++i) {
+                        va[i][0] &= vlo;
+                        va[i][1] &= vlo;
+                        va[i][2] &= vhi;
+                        va[i][3] &= vhi;
+                    }
+                }
+                // O^T += V^T P^T
+#pragma unroll
+                for (int i = 0; i < MT; ++i)
+#pragma unroll
+                    for (int t = 0; t < NT; ++t)
+                        mma_kv<KV>(acc[i][t][0], acc[i][t][1], acc[i][t][2], acc[i][t][3], va[i][0], va[i][1],
+                                   va[i][2], va[i][3], pb[t][0], pb[t][1]);
             }
-            // O^T += V^T P^T
-#pragma unroll
-            for (int i = 0; i < MT; ++i)
-#pragma unroll
-                for (int t = 0; t < NT; ++t)
-                    mma_kv<KV>(acc[i][t][0], acc[i][t][1], acc[i][t][2], acc[i][t][3], va[i][0], va[i][1], va[i][2],
-                               va[i][3], pb[t][0], pb[t][1]);
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&cs.empty[s]));   // stage free for the next copy
             ++stage;
@@ -902,7 +937,8 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
 }
 
 template <int D, int NT, bool CAUSAL, int KV>
-__global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? PA_DECODE_MINB : PA_DECODE_MINB_WIDE) decode_kernel(const __grid_constant__ CUtensorMap tmk,
+__global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? (KV == PA_KV_FP8_E4M3 ? PA_DECODE_MINB_FP8 : PA_DECODE_MINB)
+                                                       : PA_DECODE_MINB_WIDE) decode_kernel(const __grid_constant__ CUtensorMap tmk,
                                                              const __grid_constant__ CUtensorMap tmv,
                                                              const DecodeArgs a) {
     extern __shared__ uint8_t smem_raw[];
