@@ -129,7 +129,8 @@ def decode_bytes(w, esz=2) -> int:
 
 
 def multi_token(w) -> bool:
-    return bool(w.num_seqs) and not bool((w.new_counts == 1).all())
+    """Several new tokens per sequence are query rows of this step."""
+    return bool(w.multi)
 
 
 def causal_bytes(w, esz=2) -> int:
@@ -321,7 +322,8 @@ def workload(args):
     pick = (lambda a: list(a[: args.seqs]) if args.seqs <= w.num_seqs else [int(a[0])] * args.seqs)
     return workloads.custom(name=f"{w.name}-{args.seqs}seqs", seed=w.seed, num_seqs=args.seqs,
                             num_heads=w.num_heads, num_kv_heads=w.num_kv_heads, head_dim=w.head_dim,
-                            block_size=w.block_size, context_lens=pick(w.context_lens), new_tokens=pick(w.new_counts))
+                            block_size=w.block_size, context_lens=pick(w.context_lens), new_tokens=pick(w.new_counts),
+                            multi=w.multi)
 
 
 def allocate(w, pa):

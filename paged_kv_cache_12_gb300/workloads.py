@@ -119,6 +119,9 @@ class Workload:
     samples_per_prompt: int = 0
     prompt_len: int = 0
     divergent: np.ndarray | None = None   # int32 [num_seqs]: private tokens generated before this step
+    # several new tokens per sequence are computed in this step (each written
+    # token is a query row); otherwise one query per sequence (the decode)
+    multi: bool = False
     _cache: dict = field(default_factory=dict, repr=False)
 
     @property
@@ -199,15 +202,19 @@ def _spare_pool(context_lens, block_size, spare):
 
 
 def custom(name="custom", seed=7, num_seqs=4, num_heads=4, num_kv_heads=2, head_dim=64, block_size=16,
-           context_lens=None, new_tokens=1, num_blocks=None, spare_blocks=None, permute=True) -> Workload:
+           context_lens=None, new_tokens=1, num_blocks=None, spare_blocks=None, permute=True, multi=None) -> Workload:
     """A workload with given shapes and lengths (edge cases in tests);
-    new_tokens: tokens written this step, one count or one per sequence."""
+    new_tokens: tokens written this step, one count or one per sequence;
+    multi: each of them is a query row (default: when any count is not 1)."""
     lens = np.asarray(context_lens if context_lens is not None else [1] * num_seqs, dtype=np.int32)
     hist = np.maximum(lens - np.asarray(new_tokens, dtype=np.int32), 0).astype(np.int32)
     spare = num_seqs if spare_blocks is None else spare_blocks
     nb = num_blocks if num_blocks is not None else max(1, _spare_pool(lens, block_size, spare))
     order = _order(seed, nb) if permute else np.arange(nb, dtype=np.int32)
-    return Workload(name, seed, len(lens), num_heads, num_kv_heads, head_dim, block_size, nb, lens, hist, order)
+    if multi is None:
+        multi = bool(np.any(np.asarray(new_tokens) != 1))
+    return Workload(name, seed, len(lens), num_heads, num_kv_heads, head_dim, block_size, nb, lens, hist, order,
+                    multi=bool(multi))
 
 
 def make(name: str, prompt_extra: int | None = None) -> Workload:
@@ -251,7 +258,7 @@ def make(name: str, prompt_extra: int | None = None) -> Workload:
     if name == "spec72b":
         lens = np.full(100, 8192, dtype=np.int32)
         nb = _spare_pool(lens, 16, 100)
-        return Workload(name, seed, 100, 64, 8, 128, 16, nb, lens, lens - 4, _order(seed, nb))
+        return Workload(name, seed, 100, 64, 8, 128, 16, nb, lens, lens - 4, _order(seed, nb), multi=True)
     if name == "chunked":
         u = rl.uniform(math.log(64), math.log(32768), size=64)
         lens = np.rint(np.exp(u)).astype(np.int32)
@@ -259,5 +266,6 @@ def make(name: str, prompt_extra: int | None = None) -> Workload:
         hist = lens - 1
         hist[:2] = (12000 - 2048, 0)
         nb = _spare_pool(lens, 16, 64)
-        return Workload(name, seed, 64, 32, 8, 128, 16, nb, lens, hist.astype(np.int32), _order(seed, nb))
+        return Workload(name, seed, 64, 32, 8, 128, 16, nb, lens, hist.astype(np.int32), _order(seed, nb),
+                        multi=True)
     raise KeyError(name)

@@ -37,12 +37,14 @@ def test_shapes_and_ranges():
         c0 = workloads.make(name, prompt_extra=0)
         assert c0.prompt_len == 2048
     s = workloads.make("spec72b")
-    assert (s.new_counts == 4).all() and (s.context_lens == 8192).all() and s.group == 8
+    assert (s.new_counts == 4).all() and (s.context_lens == 8192).all() and s.group == 8 and s.multi
     assert list(s.query_start[:3]) == [0, 4, 8] and s.query_start[-1] == 400
     c = workloads.make("chunked")
     assert list(c.context_lens[:2]) == [12000, 600] and list(c.new_counts[:2]) == [2048, 600]
     assert (c.new_counts[2:] == 1).all() and c.num_new_tokens == 2048 + 600 + 62
-    assert c.query_start[-1] == c.num_new_tokens and c.query_start[2] == 2648
+    assert c.query_start[-1] == c.num_new_tokens and c.query_start[2] == 2648 and c.multi
+    # the parallel-sampling steps append private tokens but decode one query per sequence
+    assert not workloads.make("cow16").multi and not workloads.make("gqa72b").multi
 
 
 def test_multi_token_query_rows():
