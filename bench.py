@@ -153,6 +153,15 @@ def causal_flops(w) -> int:
     return int(4 * seen * w.num_heads * w.head_dim)
 
 
+def prefill_launch(w, kv_dtype) -> bool:
+    """Whether a multi-token call also launches the tensor-core kernel for long
+    runs of new tokens (the library's rule: head_dim 128, fp16/bf16 cache, G
+    dividing 128, at least 64 query rows in the call; PA_PREFILL=0 disables)."""
+    G = w.num_heads // w.num_kv_heads
+    return (multi_token(w) and os.environ.get("PA_PREFILL", "1")[:1] != "0" and w.head_dim == 128
+            and kv_dtype != "fp8" and 128 % G == 0 and w.num_new_tokens * G >= 64)
+
+
 def kv_write_bytes(w, esz=2) -> int:
     """fp16/bf16 rows read, cache elements written, slots read."""
     T = w.num_new_tokens
@@ -617,7 +626,7 @@ def run_ours(args):
             "value": round(job_tokens_per_s(world, B, args.steps, graph_ms), 2), "unit": "tokens/s",
             "ms_per_step": round(graph_ms / args.steps, 4),
             "note": "the whole step captured once in a CUDA Graph and replayed"},
-        "gpu_launches": args.steps * layers * (3 + (1 if has_pairs else 0)),
+        "gpu_launches": args.steps * layers * (3 + (1 if has_pairs else 0) + (1 if prefill_launch(w, kvd) else 0)),
         "alloc_us_per_step": round(alloc_us, 1),
         "clocks": clk.summary(),
     }

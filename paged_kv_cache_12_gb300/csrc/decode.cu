@@ -46,6 +46,7 @@
 #include <vector>
 
 #include "decode_common.cuh"
+#include "prefill.h"
 
 namespace pa {
 namespace {
@@ -268,10 +269,13 @@ __device__ __forceinline__ int last_le(const int32_t *a, int n, int x) {
 // in the single-token form.  A sequence whose lengths are inconsistent gets
 // NaN rows; a query_start that is not a non-decreasing cover of [0, NQ) makes
 // every row NaN.
+// A sequence with at least pf_min_rows query rows (new tokens x G; 0: none)
+// goes to the tensor-core prefill kernel instead: it gets no items here, and
+// its ceil(T G / 128) row tiles are listed in ptiles, last rows first.
 __global__ void __launch_bounds__(PREP_THREADS) causal_prep_kernel(
     const int32_t *__restrict__ context_lens, const int32_t *__restrict__ qs, int B, int NQ, int Hq, int D, int Hkv,
     int max_ctx, long long max_table_tokens, int pt, int ms, WsHeader *hdr, int *part_off, int *vlen, int *gstart,
-    ItemRec *items, int *grp, uint16_t *out, uint32_t nan2) {
+    ItemRec *items, int *grp, uint16_t *out, uint32_t nan2, int pf_min_rows, int4 *ptiles) {
     constexpr int NBK = MAX_PART_TOKENS / CHUNK;
     __shared__ int warp_sums[PREP_THREADS / 32];
     __shared__ int hist[NBK], cursor[NBK];
@@ -288,6 +292,8 @@ __global__ void __launch_bounds__(PREP_THREADS) causal_prep_kernel(
         T = qs[i + 1] - qs[i];
         return L >= 0 && L <= max_ctx && (long long)L <= max_table_tokens && T <= L;
     };
+    const int G = Hq / Hkv;
+    auto prefill = [&](int T) { return pf_min_rows > 0 && (long long)T * G >= pf_min_rows; };
     // pass 1: visible length and partial-row offset of every query row
     int run = 0;
     for (int base = 0; base < NQ; base += PREP_THREADS) {
@@ -296,7 +302,7 @@ __global__ void __launch_bounds__(PREP_THREADS) causal_prep_kernel(
         if (v < NQ && qs_ok) {
             const int i = last_le(qs, B, v);
             int L, T;
-            if (seq_ok(i, L, T)) vl = L - T + (v - qs[i]) + 1;
+            if (seq_ok(i, L, T)) vl = prefill(T) ? 0 : L - T + (v - qs[i]) + 1;   // 0: the prefill kernel's row
         }
         int tot;
         const int e = run + block_exclusive_scan(vl > 0 ? (vl + pt - 1) / pt : 0, warp_sums, &tot);
@@ -316,15 +322,27 @@ __global__ void __launch_bounds__(PREP_THREADS) causal_prep_kernel(
     for (int base = 0; base < B; base += PREP_THREADS) {
         const int i = base + threadIdx.x;
         int n = 0, L, T;
-        if (i < B && qs_ok && seq_ok(i, L, T)) n = (T + ms - 1) / ms;
+        if (i < B && qs_ok && seq_ok(i, L, T) && !prefill(T)) n = (T + ms - 1) / ms;
         int tot;
         const int e = run_g + block_exclusive_scan(n, warp_sums, &tot);
         if (i < B) gstart[i] = e;
         run_g += tot;
     }
+    // pass 2b: row tiles of the prefill kernel
+    int run_t = 0;
+    for (int base = 0; base < B; base += PREP_THREADS) {
+        const int i = base + threadIdx.x;
+        int n = 0, L, T;
+        if (i < B && qs_ok && seq_ok(i, L, T) && prefill(T)) n = (int)(((long long)T * G + 127) / 128);
+        int tot;
+        const int e = run_t + block_exclusive_scan(n, warp_sums, &tot);
+        for (int k = 0; k < n; ++k) ptiles[e + k] = make_int4(i, n - 1 - k, 0, 0);
+        run_t += tot;
+    }
     if (threadIdx.x == 0) {
         gstart[B] = run_g;
         part_off[NQ] = run;
+        hdr->pf_items = run_t * Hkv;
     }
     __syncthreads();
     const int NG = run_g;
@@ -468,6 +486,16 @@ long long wait_limit_cycles() {
         return x > 0 ? x : WAIT_LIMIT;
     }();
     return v;
+}
+
+// The tensor-core kernel for long runs of new tokens is used unless
+// PA_PREFILL=0 (read once; then every sequence takes the decode pipeline).
+bool prefill_enabled() {
+    static const bool on = [] {
+        const char *e = std::getenv("PA_PREFILL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
 }
 
 // Checks of the cache element type and its scales; 0 when valid.
@@ -679,10 +707,16 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     ItemRec *items = reinterpret_cast<ItemRec *>(ws + L.items);
     int *grp = reinterpret_cast<int *>(ws + L.grp);
     uint16_t *hout = out;
+    // sequences with many new tokens go to the tensor-core prefill kernel
+    // (fp16 / bf16 caches, head_dim 128, G dividing the 128-row tile)
+    const bool pf = prefill_enabled() && head_dim == 128 && kv != PA_KV_FP8_E4M3 && PF_ROWS % G == 0 &&
+                    (long long)num_query_tokens * G >= PF_MIN_ROWS;
+    int4 *ptiles = reinterpret_cast<int4 *>(ws + L.ptiles);
     causal_prep_kernel<<<1, PREP_THREADS, 0, st>>>(context_lens, query_start, num_seqs, num_query_tokens, num_heads,
                                                    head_dim, num_kv_heads, max_context_len,
                                                    (long long)max_blocks_per_seq * block_size, L.pt, ms, hdr,
-                                                   part_off, vlen, gstart, items, grp, hout, nan_pair(kv));
+                                                   part_off, vlen, gstart, items, grp, hout, nan_pair(kv),
+                                                   pf ? PF_MIN_ROWS : 0, ptiles);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
 
     DecodeArgs args;
@@ -708,7 +742,25 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     args.ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
     args.ws_o = reinterpret_cast<float *>(ws + L.o);
     const long long max_items = L.item_cap * num_kv_heads;
-    return launch_kv_any(kv, head_dim, PA_CAUSAL_NT, true, tmk, tmv, args, max_items, st);
+    const int rc = launch_kv_any(kv, head_dim, PA_CAUSAL_NT, true, tmk, tmv, args, max_items, st);
+    if (rc != PA_OK || !pf) return rc;
+    PrefillArgs pa_;
+    pa_.out = hout;
+    pa_.query = query;
+    pa_.block_tables = block_tables;
+    pa_.context_lens = context_lens;
+    pa_.query_start = query_start;
+    pa_.tiles = ptiles;
+    pa_.hdr = hdr;
+    pa_.Hq = num_heads;
+    pa_.Hkv = num_kv_heads;
+    pa_.G = G;
+    pa_.bs = block_size;
+    pa_.mbps = max_blocks_per_seq;
+    pa_.num_blocks = num_blocks;
+    pa_.scale_log2 = scale * 1.4426950408889634f;
+    pa_.wait_limit = wait_limit_cycles();
+    return launch_prefill(kv, tmk, tmv, pa_, L.ptile_cap * num_kv_heads, st);
 }
 
 }  // namespace

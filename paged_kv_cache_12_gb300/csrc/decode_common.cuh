@@ -68,14 +68,15 @@ struct WsHeader {
     int error;
     int total_items;
     int counter;
-    int pad[61];
+    int pf_items;    // multi-token form: work items of the tensor-core prefill kernel
+    int pad[60];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
 struct WsLayout {
-    size_t part_off, gsize, gshared, items, grp, ml, o, total;
+    size_t part_off, gsize, gshared, items, grp, ml, o, ptiles, total;
     int pmax, pt;
-    long long item_cap;
+    long long item_cap, ptile_cap;
 };
 
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -135,6 +136,10 @@ inline WsLayout ws_layout_causal(int B, int NQ, int Hq, int Hkv, int D, int max_
     off += up256(sizeof(float2) * (size_t)parts * Hq);
     w.o = off;
     off += up256(sizeof(float) * (size_t)parts * Hq * D);
+    // prefill tiles: 128 query rows (new tokens x G) of one sequence each
+    w.ptile_cap = ((long long)NQ * G + 127) / 128 + B;
+    w.ptiles = off;
+    off += up256(sizeof(int4) * (size_t)w.ptile_cap);
     w.total = off;
     return w;
 }

@@ -1,0 +1,485 @@
+// Paged causal attention for long runs of new tokens (a prompt chunk) on the
+// 5th-generation tensor cores.
+//
+// What is computed is the multi-token form of decode.cu (deepsonar page,
+// section 2.5: a request may compute a chunk of its prompt in one step): new
+// token j of sequence i (query row query_start[i] + j) attends to positions
+// t <= L_i - T_i + j through the block table.  When a sequence brings many new
+// tokens the work is a dense contraction -- 128 query rows against every KV
+// tile -- so it runs here on tcgen05 rather than on the decode pipeline.
+//
+// A work tile is (sequence, kv head, 128 query rows): 128 / G consecutive new
+// tokens times the G query heads of the kv head (rows token-major), so a K/V
+// tile read from HBM serves all of them.  One CTA per SM, persistent over a
+// static list of tiles ordered longest first; six warps:
+//   warps 0-1  producers of K and of V: per 64-token KV tile, TMA copies of
+//              the block rows (gathered through the block table, one lane per
+//              block) into 4-stage rings;
+//   warp 2     MMA issuer (one thread): S = Q K^T into one of two tensor
+//              memory buffers (M 128, N 64, K 128), then O += P V (M 128,
+//              N 128, K 64) into a tensor-memory accumulator; completions are
+//              committed to mbarriers;
+//   warps 3-6  softmax (one query row per thread): read the row of S from
+//              tensor memory, mask past the row's position, online softmax in
+//              fp32 with the running maximum rescaled only when it grows by
+//              more than 2^8 (then O is rescaled in tensor memory), write P
+//              (fp16/bf16) to shared memory for the PV product, and at the
+//              end divide O by the row sum and store the output row.
+// S for the next KV tile is computed while the softmax works on this one.
+// Every wait is bounded; tensor memory is released on every path.
+
+#include <cmath>
+#include <mutex>
+
+#include "decode_common.cuh"
+#include "prefill.h"
+#include "umma.cuh"
+
+namespace pa {
+namespace {
+
+constexpr int PM = 128;                    // query rows per work tile
+constexpr int PN = 64;                     // KV tokens per tile
+constexpr int PD = 128;                    // head dim
+constexpr int PST = 4;                     // K and V ring stages
+constexpr int Q_BYTES = PM * PD * 2;       // 2 K-blocks (64 dims) x 128 rows x 128 B
+constexpr int KV_BYTES = PN * PD * 2;      // 2 blocks (64 dims) x 64 tokens x 128 B
+constexpr int P_BYTES = PM * PN * 2;       // 128 rows x 128 B; two buffers
+constexpr int OFF_Q = 0;
+constexpr int OFF_K = OFF_Q + Q_BYTES;
+constexpr int OFF_V = OFF_K + PST * KV_BYTES;
+constexpr int OFF_P = OFF_V + PST * KV_BYTES;
+constexpr int OFF_CTRL = OFF_P + 2 * P_BYTES;
+constexpr int CTRL_BYTES = 256;
+constexpr int CTRL_BAD = 224;              // int: 1 + the work item that met an out-of-range block id
+constexpr int CTRL_ABORT = 228;            // int: a role gave up waiting
+constexpr int PF_SMEM = OFF_CTRL + CTRL_BYTES + 1024;   // + alignment slack
+constexpr int PF_THREADS = 7 * 32;         // K producer, V producer, MMA, 4 softmax warps
+constexpr int TMEM_COLS = 256;             // S0 [0, 64), S1 [64, 128), O [128, 256)
+constexpr int TM_O = 128;
+static_assert(8 * (4 * PST + 11) + 8 <= CTRL_BAD && CTRL_ABORT + 4 <= CTRL_BYTES, "control block layout");
+
+struct PfBars {
+    // pfull / pvdone: one per P buffer, so that a softmax warp a step ahead of
+    // another never adds its arrival to the other step's phase
+    uint32_t kfull[PST], kempty[PST], vfull[PST], vempty[PST], sfull[2], sfree[2], pfull[2], pvdone[2], qfull;
+    uint32_t tmem_slot, flags;   // shared addresses
+};
+
+__device__ __forceinline__ PfBars pf_bars(uint8_t *smem) {
+    const uint32_t c = smem_u32(smem + OFF_CTRL);
+    PfBars b;
+    uint32_t a = c;
+    for (int s = 0; s < PST; ++s) b.kfull[s] = a, a += 8;
+    for (int s = 0; s < PST; ++s) b.kempty[s] = a, a += 8;
+    for (int s = 0; s < PST; ++s) b.vfull[s] = a, a += 8;
+    for (int s = 0; s < PST; ++s) b.vempty[s] = a, a += 8;
+    b.sfull[0] = a, a += 8;
+    b.sfull[1] = a, a += 8;
+    b.sfree[0] = a, a += 8;
+    b.sfree[1] = a, a += 8;
+    b.pfull[0] = a, a += 8;
+    b.pfull[1] = a, a += 8;
+    b.pvdone[0] = a, a += 8;
+    b.pvdone[1] = a, a += 8;
+    b.qfull = a, a += 8;
+    b.tmem_slot = a, a += 8;
+    b.flags = a;   // barriers and slots end at byte 8 (4 PST + 11) + 8 = 216 <= CTRL_BAD
+    return b;
+}
+
+// Geometry of one work tile, the same in every warp.
+struct PfTile {
+    int seq, kvh, row0, ntok, C, nkv, L, q0;
+};
+
+__device__ __forceinline__ PfTile pf_tile(const PrefillArgs &a, int item) {
+    const int4 rec = a.tiles[item / a.Hkv];
+    PfTile t;
+    t.seq = rec.x;
+    t.kvh = item % a.Hkv;
+    const int tpt = PM / a.G;               // new tokens per tile
+    t.L = a.context_lens[t.seq];
+    t.q0 = a.query_start[t.seq];
+    const int T = a.query_start[t.seq + 1] - t.q0;
+    t.row0 = rec.y * tpt;                   // first new token of the tile
+    t.ntok = min(tpt, T - t.row0);
+    t.C = t.L - T + 1;                      // positions the first new token sees
+    t.nkv = (t.C + t.row0 + t.ntok - 1 + PN - 1) / PN;
+    return t;
+}
+
+__device__ __forceinline__ void pf_error(const PrefillArgs &a) { atomicExch(&a.hdr->error, PA_ERR_TIMEOUT); }
+
+// ----------------------------------------------------------- producer
+
+__device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const PrefillArgs &a, const PfBars &bb,
+                            volatile int *abort_flag, int total, int kv) {
+    const int lane = threadIdx.x & 31;
+    const uint64_t pol = policy_evict_normal();
+    const int box_rows = a.bs < 16 ? a.bs : 16;    // rows per TMA box: one box per block or 16-row group
+    const uint32_t base = smem_u32(smem) + (kv ? OFF_V : OFF_K);
+    const uint32_t *full = kv ? bb.vfull : bb.kfull;
+    const uint32_t *empty = kv ? bb.vempty : bb.kempty;
+    int cnt = 0;
+    // Before leaving, the last copy into every stage has landed (bounded).
+    auto drain = [&]() {
+        for (int s = 0; s < PST; ++s)
+            if (cnt > s) mbar_wait_bounded(full[s], (uint32_t)(((s + (cnt - 1 - s) / PST * PST) / PST) & 1), WAIT_LIMIT);
+    };
+    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+        const PfTile t = pf_tile(a, item);
+        const int32_t *row = a.block_tables + (long long)t.seq * a.mbps;
+        for (int n = 0; n < t.nkv; ++n) {
+            // lane j owns box j of the tile (tokens t0 + j box_rows ..): its block id,
+            // loaded before the wait so that the load's latency overlaps it
+            const int t0 = n * PN;
+            const int tok = t0 + lane * box_rows;
+            const bool mine = lane < PN / box_rows && tok < t.L;
+            const int32_t blk = mine ? __ldg(row + tok / a.bs) : 0;
+            const int s = cnt % PST;
+            // the warp decides together (no lane may leave alone)
+            const bool got = !*abort_flag && mbar_wait_bounded(empty[s], ((cnt / PST) & 1) ^ 1, a.wait_limit);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (lane == 0) pf_error(a);
+                *abort_flag = 1;
+                drain();
+                return;
+            }
+            const unsigned boxes = __ballot_sync(0xffffffffu, mine);
+            const bool bad = __any_sync(0xffffffffu, mine && (blk < 0 || blk >= a.num_blocks));
+            if (lane == 0) {
+                if (bad) *reinterpret_cast<volatile int *>(smem + OFF_CTRL + CTRL_BAD) = item + 1;
+                mbar_arrive_expect_tx(full[s], bad ? 0u : (uint32_t)(__popc(boxes) * 2 * box_rows * 128));
+            }
+            __syncwarp();
+            if (!bad && mine) {
+                const uint32_t dst = base + s * KV_BYTES + lane * box_rows * 128;
+                const int y = (int)(((long long)blk * a.Hkv + t.kvh) * a.bs) + tok % a.bs;
+                tma_load_2d(dst, map, 0, y, full[s], pol);
+                tma_load_2d(dst + PN * 128, map, 64, y, full[s], pol);
+            }
+            __syncwarp();
+            ++cnt;
+        }
+    }
+    drain();
+}
+
+// ----------------------------------------------------------- MMA issuer
+
+__device__ void pf_mma(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, uint32_t tmem, bool bf16,
+                       volatile int *abort_flag, int total) {
+    const uint32_t base = smem_u32(smem);
+    const uint32_t id_s = idesc_f16(PM, PN, bf16, false);
+    const uint32_t id_o = idesc_f16(PM, PD, bf16, true);
+    int kc = 0, vc = 0, sc = 0, pc = 0, qc = 0;
+    bool ok = true;
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (!ok) return false;
+        if (*abort_flag || !mbar_wait_bounded(bar, parity, a.wait_limit)) {
+            pf_error(a);
+            *abort_flag = 1;
+            ok = false;
+        }
+        return ok;
+    };
+    // S(next) = Q K^T into tensor-memory buffer sc & 1
+    auto issue_s = [&]() {
+        const int ks = kc % PST;
+        const int b = sc & 1;
+        if (!wait(bb.kfull[ks], (kc / PST) & 1)) return;
+        if (sc >= 2 && !wait(bb.sfree[b], ((sc >> 1) - 1) & 1)) return;
+        tc_fence_after_sync();
+        const uint32_t qa = base + OFF_Q, ka = base + OFF_K + ks * KV_BYTES;
+#pragma unroll
+        for (int k = 0; k < PD / 16; ++k) {
+            // K-step k: 16 dims at byte 32 (k % 4) of the 64-dim block k / 4
+            const uint64_t da = sw128_desc(qa + (k >> 2) * (PM * 128) + (k & 3) * 32, 16, 1024);
+            const uint64_t db = sw128_desc(ka + (k >> 2) * (PN * 128) + (k & 3) * 32, 16, 1024);
+            umma_f16(tmem + b * PN, da, db, id_s, k > 0 ? 1u : 0u);
+        }
+        umma_commit(bb.sfull[b]);
+        umma_commit(bb.kempty[ks]);
+        ++kc;
+        ++sc;
+    };
+    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const PfTile t = pf_tile(a, item);
+        if (!wait(bb.qfull, qc & 1)) break;
+        ++qc;
+        issue_s();
+        for (int n = 0; n < t.nkv && ok; ++n) {
+            if (n + 1 < t.nkv) issue_s();
+            const int pb = pc & 1;   // PV number pc reads P buffer pc & 1
+            if (!wait(bb.pfull[pb], (pc >> 1) & 1)) break;
+            ++pc;
+            const int vs = vc % PST;
+            if (!wait(bb.vfull[vs], (vc / PST) & 1)) break;
+            tc_fence_after_sync();
+            const uint32_t pa_ = base + OFF_P + pb * P_BYTES, va = base + OFF_V + vs * KV_BYTES;
+#pragma unroll
+            for (int k = 0; k < PN / 16; ++k) {
+                const uint64_t da = sw128_desc(pa_ + k * 32, 16, 1024);
+                // V tile, B operand with N (dims) contiguous: 128-byte rows of
+                // 64 dims, one row per token (K); the next 64 dims are the
+                // next block of PN rows; K-step k starts 16 tokens further
+                const uint64_t db = sw128_desc(va + k * 16 * 128, PN * 128, 1024);
+                umma_f16(tmem + TM_O, da, db, id_o, (n > 0 || k > 0) ? 1u : 0u);
+            }
+            umma_commit(bb.pvdone[pb]);
+            umma_commit(bb.vempty[vs]);
+            ++vc;
+        }
+    }
+}
+
+// ------------------------------------------------------------- softmax
+
+template <int KV>
+__device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, uint32_t tmem,
+                           volatile int *abort_flag, int total) {
+    const int tid = threadIdx.x - 96;             // 0 .. 127
+    const int lane = threadIdx.x & 31;
+    const int quarter = (threadIdx.x >> 5) & 3;    // tensor-memory lanes 32 quarter .. + 31
+    const int m = quarter * 32 + lane;             // this thread's query row in the tile
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t base = smem_u32(smem);
+    const float sl2 = a.scale_log2;
+    // g: P tiles written so far (P tile g feeds PV number g, buffer g & 1);
+    // pvdone[b] completes for PV numbers b, b + 2, ... in order
+    int sc = 0, g = 0, vcount = 0;
+    bool ok = true;
+    // every thread of the warp takes the same decision, so warp-collective
+    // tensor-memory loads and stores are never reached by part of a warp
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (!ok) return false;
+        const bool got = !*abort_flag && mbar_wait_bounded(bar, parity, a.wait_limit);
+        if (!__all_sync(0xffffffffu, got)) {
+            if (lane == 0) pf_error(a);
+            *abort_flag = 1;
+            ok = false;
+        }
+        return ok;
+    };
+    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const PfTile t = pf_tile(a, item);
+        const int tok = m / a.G, hh = m - tok * a.G;
+        const bool valid = tok < t.ntok;
+        const long long qrow = ((long long)(t.q0 + t.row0 + tok) * a.Hq + t.kvh * a.G + hh) * PD;
+        // ---- Q row into the swizzled A tile (zeros past the new tokens)
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.query + qrow);
+#pragma unroll
+            for (int c = 0; c < PD / 8; ++c) {
+                const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                const int kb = c >> 3, cc = c & 7;
+                *reinterpret_cast<uint4 *>(smem + OFF_Q + kb * (PM * 128) + m * 128 + ((cc ^ (m & 7)) << 4)) = v;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bb.qfull);
+        }
+        const int vis = valid ? t.C + t.row0 + tok : 1;   // positions this row sees
+        float mrun = -INFINITY, l = 0.f;
+        for (int n = 0; n < t.nkv && ok; ++n) {
+            // ---- S row of this KV tile
+            const int b = sc & 1;
+            if (!wait(bb.sfull[b], (sc >> 1) & 1)) break;
+            ++sc;
+            tc_fence_after_sync();
+            uint32_t r0[32], r1[32];
+            tmem_ld32(trow + b * PN, r0);
+            tmem_ld32(trow + b * PN + 32, r1);
+            tmem_wait_ld();
+            tc_fence_before_sync();
+            mbar_arrive(bb.sfree[b]);
+            float s[PN];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                s[c] = __uint_as_float(r0[c]);
+                s[c + 32] = __uint_as_float(r1[c]);
+            }
+            const int t0 = n * PN;
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < PN; ++c) {
+                s[c] = t0 + c < vis ? s[c] * sl2 : -INFINITY;
+                mx = fmaxf(mx, s[c]);
+            }
+            if (mx > mrun + RESCALE_THRESHOLD) {
+                const float nm = fmaxf(mrun, mx);
+                const float alpha = fast_exp2(mrun - nm);
+                if (n > 0) {   // O holds PV up to number g - 1: rescale it in tensor memory
+                    if (!wait(bb.pvdone[(g - 1) & 1], ((g - 1) >> 1) & 1)) break;
+                    tc_fence_after_sync();
+#pragma unroll 1
+                    for (int c4 = 0; c4 < PD / 32; ++c4) {
+                        uint32_t o[32];
+                        tmem_ld32(trow + TM_O + c4 * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tmem_st32(trow + TM_O + c4 * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+                l *= alpha;
+                mrun = nm;
+            }
+            float p[PN];
+#pragma unroll
+            for (int c = 0; c < PN; ++c) {
+                p[c] = fast_exp2(s[c] - mrun);
+                l += p[c];
+            }
+            if (g >= 2 && !wait(bb.pvdone[g & 1], ((g >> 1) - 1) & 1)) break;   // buffer g & 1 free: PV g - 2 done
+            // ---- the last KV tile: V rows past the context are zeroed (P is 0 there)
+            const int vs = vcount % PST;
+            const int vphase = (vcount / PST) & 1;
+            ++vcount;
+            if (t0 + PN > t.L) {
+                if (!wait(bb.vfull[vs], vphase)) break;
+                const int first = t.L - t0;    // rows first .. PN-1 of both 64-dim blocks
+                uint8_t *vt = smem + OFF_V + vs * KV_BYTES;
+                for (int k = tid; k < 2 * PN * 8; k += 128) {
+                    const int h = k / (PN * 8), rr = (k / 8) % PN, cc = k % 8;
+                    if (rr >= first)
+                        *reinterpret_cast<uint4 *>(vt + h * (PN * 128) + rr * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
+                }
+            }
+            // ---- P row into the swizzled A tile of the PV product
+#pragma unroll
+            for (int c = 0; c < PN / 8; ++c) {
+                uint4 v;
+                v.x = pack_p<KV>(p[8 * c + 0], p[8 * c + 1]);
+                v.y = pack_p<KV>(p[8 * c + 2], p[8 * c + 3]);
+                v.z = pack_p<KV>(p[8 * c + 4], p[8 * c + 5]);
+                v.w = pack_p<KV>(p[8 * c + 6], p[8 * c + 7]);
+                *reinterpret_cast<uint4 *>(smem + OFF_P + (g & 1) * P_BYTES + m * 128 + ((c ^ (m & 7)) << 4)) = v;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            mbar_arrive(bb.pfull[g & 1]);
+            ++g;
+        }
+        if (!ok) break;
+        // ---- epilogue: O / l once the tile's last PV (number g - 1) is done
+        if (!wait(bb.pvdone[(g - 1) & 1], ((g - 1) >> 1) & 1)) break;
+        tc_fence_after_sync();
+        const bool bad = *reinterpret_cast<volatile int *>(smem + OFF_CTRL + CTRL_BAD) == item + 1;
+        const float inv = bad ? __int_as_float(0x7fc00000) : 1.f / l;
+        uint16_t *orow = a.out + qrow;
+#pragma unroll 1
+        for (int c4 = 0; c4 < PD / 32; ++c4) {
+            uint32_t o[32];
+            tmem_ld32(trow + TM_O + c4 * 32, o);
+            tmem_wait_ld();
+            if (valid) {
+#pragma unroll
+                for (int c = 0; c < 32; c += 8) {
+                    uint4 v;
+                    v.x = (uint32_t)out_bits<KV>(__uint_as_float(o[c]) * inv) |
+                          ((uint32_t)out_bits<KV>(__uint_as_float(o[c + 1]) * inv) << 16);
+                    v.y = (uint32_t)out_bits<KV>(__uint_as_float(o[c + 2]) * inv) |
+                          ((uint32_t)out_bits<KV>(__uint_as_float(o[c + 3]) * inv) << 16);
+                    v.z = (uint32_t)out_bits<KV>(__uint_as_float(o[c + 4]) * inv) |
+                          ((uint32_t)out_bits<KV>(__uint_as_float(o[c + 5]) * inv) << 16);
+                    v.w = (uint32_t)out_bits<KV>(__uint_as_float(o[c + 6]) * inv) |
+                          ((uint32_t)out_bits<KV>(__uint_as_float(o[c + 7]) * inv) << 16);
+                    *reinterpret_cast<uint4 *>(orow + c4 * 32 + c) = v;
+                }
+            }
+        }
+        tc_fence_before_sync();
+    }
+}
+
+template <int KV>
+__global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmk,
+                                                                 const __grid_constant__ CUtensorMap tmv,
+                                                                 const PrefillArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const PfBars bb = pf_bars(smem);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_CTRL + CTRL_ABORT);
+    const int warp = threadIdx.x >> 5;
+    const int total = *reinterpret_cast<volatile int *>(&a.hdr->pf_items);   // written by the prep kernel
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PST; ++s) {
+            mbar_init(bb.kfull[s], 1);
+            mbar_init(bb.kempty[s], 1);
+            mbar_init(bb.vfull[s], 1);
+            mbar_init(bb.vempty[s], 1);
+        }
+        mbar_init(bb.sfull[0], 1);
+        mbar_init(bb.sfull[1], 1);
+        mbar_init(bb.sfree[0], 128);
+        mbar_init(bb.sfree[1], 128);
+        mbar_init(bb.pfull[0], 128);
+        mbar_init(bb.pfull[1], 128);
+        mbar_init(bb.pvdone[0], 1);
+        mbar_init(bb.pvdone[1], 1);
+        mbar_init(bb.qfull, 128);
+        mbar_init(bb.flags, 1);            // all MMAs completed (before tensor memory is freed)
+        *reinterpret_cast<volatile int *>(smem + OFF_CTRL + CTRL_BAD) = 0;
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {   // this warp owns the tensor memory
+        tmem_alloc(bb.tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + (bb.tmem_slot - smem_u32(smem)));
+    if (warp < 2) {
+        pf_producer(smem, warp ? &tmv : &tmk, a, bb, abort_flag, total, warp);
+    } else if (warp == 2) {
+        if ((threadIdx.x & 31) == 0) {
+            pf_mma(smem, a, bb, tmem, KV == PA_KV_BF16, abort_flag, total);
+            // every MMA issued has completed before tensor memory is released
+            umma_commit(bb.flags);
+            mbar_wait_bounded(bb.flags, 0, WAIT_LIMIT);
+        }
+        __syncwarp();
+    } else {
+        pf_softmax<KV>(smem, a, bb, tmem, abort_flag, total);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+template <int KV>
+int launch_prefill_kv(const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args, long long max_items,
+                      cudaStream_t st) {
+    static int grid = 0;
+    static cudaError_t init_err = cudaSuccess;
+    static std::once_flag once;
+    std::call_once(once, [] {   // one CTA per SM
+        init_err = cudaFuncSetAttribute(prefill_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
+        int dev = 0, sms = 0;
+        if (init_err == cudaSuccess) init_err = cudaGetDevice(&dev);
+        if (init_err == cudaSuccess) init_err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        grid = sms;
+    });
+    if (init_err != cudaSuccess || grid <= 0) return PA_ERR_CUDA;
+    const int g = (int)(max_items < grid ? (max_items > 0 ? max_items : 1) : grid);
+    prefill_kernel<KV><<<g, PF_THREADS, PF_SMEM, st>>>(tmk, tmv, args);
+    return cuda_status(cudaGetLastError());
+}
+
+}  // namespace
+
+int launch_prefill(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
+                   long long max_items, cudaStream_t st) {
+    if (kv == PA_KV_BF16) return launch_prefill_kv<PA_KV_BF16>(tmk, tmv, args, max_items, st);
+    if (kv == PA_KV_F16) return launch_prefill_kv<PA_KV_F16>(tmk, tmv, args, max_items, st);
+    return PA_ERR_UNSUPPORTED;
+}
+
+}  // namespace pa

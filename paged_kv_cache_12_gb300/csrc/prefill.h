@@ -1,0 +1,37 @@
+// Paged causal attention for long runs of new tokens on tcgen05 (prefill.cu):
+// arguments and launch, used by the multi-token entry points in decode.cu.
+#pragma once
+
+#include <cudaTypedefs.h>
+#include <stdint.h>
+
+#include "decode_common.cuh"
+
+namespace pa {
+
+struct PrefillArgs {
+    uint16_t *out;                    // fp16 / bf16 [num_query_tokens][Hq][128]
+    const uint16_t *query;            // same layout
+    const int32_t *block_tables;
+    const int32_t *context_lens;
+    const int32_t *query_start;
+    const int4 *tiles;                // {sequence, row tile, 0, 0}, longest first
+    WsHeader *hdr;                    // error word; pf_items = work items (tiles x Hkv)
+    int Hq, Hkv, G, bs, mbps;
+    long long num_blocks;
+    float scale_log2;
+    long long wait_limit;
+};
+
+// Query rows per work tile, and the smallest number of query rows
+// (new tokens x G) for which a sequence goes to the tensor-core kernel.
+constexpr int PF_ROWS = 128;
+constexpr int PF_MIN_ROWS = 64;
+
+// Launch the prefill kernel on `st` (fp16 or bf16 caches, head_dim 128);
+// it reads its item count from the workspace header; max_items is a host
+// bound that trims the grid.  tmk / tmv: the caches' tensor maps.
+int launch_prefill(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
+                   long long max_items, cudaStream_t st);
+
+}  // namespace pa

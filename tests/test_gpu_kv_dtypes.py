@@ -90,7 +90,7 @@ class TypedStep:
             k0, v0 = w.k_pool.view(np.uint16).copy(), w.v_pool.view(np.uint16).copy()
             nanc = NAN16
             self.q, self.qm = w.query, w.query_multi
-            self.nk, self.nv = w.new_key, w.new_value
+            self.nk, self.nv = w.new_key.view(np.uint16), w.new_value.view(np.uint16)   # bit patterns, as the caches
         k0.transpose(0, 2, 1, 3)[unused] = nanc
         v0.transpose(0, 2, 1, 3)[unused] = nanc
         self.k0, self.v0 = k0, v0

@@ -1,0 +1,84 @@
+"""The tensor-core kernel for long runs of new tokens (prompt chunks; deepsonar
+page section 2.5): a sequence whose new tokens x G reach 64 query rows is
+computed in 128-row tiles with tcgen05 MMAs.  Results must be the oracle's
+causal attention within the decode tolerance, for every G that divides the
+tile, every block size, fp16 and bf16 caches, chunks after long histories
+(many KV tiles, running-maximum rescales), whole prompts, partial row tiles and
+contexts that end inside a KV tile (the V rows past them are poisoned NaN)."""
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import oracle
+import paged_kv_cache_12_gb300 as pa
+from paged_kv_cache_12_gb300 import workloads
+from test_gpu_kv_dtypes import TypedStep, compare, as_f64
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():  # pragma: no cover
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def run_case(H, Hkv, bs, kv, lens, T, seed):
+    w = workloads.custom(seed=seed, num_seqs=len(lens), num_heads=H, num_kv_heads=Hkv, head_dim=128, block_size=bs,
+                         context_lens=lens, new_tokens=T, multi=True)
+    st = TypedStep(w, kv)
+    st.run_gpu()
+    kc, vc = st.oracle_caches()
+    out = st.causal()
+    ref = oracle.paged_attention_typed(st.qm, kc, vc, st.tables, st.lens, w.query_start, Hkv, bs, w.scale, kv,
+                                       *st.scales())
+    return w, st, out, ref
+
+
+@pytest.mark.parametrize("kv", [pa.PA_KV_F16, pa.PA_KV_BF16])
+@pytest.mark.parametrize("H,Hkv", [(8, 8), (16, 8), (32, 8), (64, 8), (16, 1)])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_prompt_chunks_against_oracle(kv, H, Hkv, bs):
+    G = H // Hkv
+    # a whole prompt, chunks after a history (ending inside a KV tile), a
+    # chunk of exactly one row tile, one with a partial last tile, and short
+    # requests that stay on the decode pipeline in the same call
+    tpt = 128 // G
+    lens = [300, 1000 + 37, 700, 2 * tpt + 513, 5, 4000]
+    T = [300, 200, tpt, 2 * tpt + 3, 2, 129]
+    w, st, out, ref = run_case(H, Hkv, bs, kv, lens, T, seed=11 * H + bs + kv)
+    compare(as_f64(out, kv), ref, kv)
+
+
+def test_long_history_many_kv_tiles():
+    # 16k positions before a 256-token chunk: 260 KV tiles per row tile,
+    # scores drawn large enough that the running maximum moves often
+    w, st, out, ref = run_case(32, 8, 16, pa.PA_KV_F16, [16384 + 256], [256], seed=5)
+    compare(as_f64(out, pa.PA_KV_F16), ref, pa.PA_KV_F16)
+
+
+def test_deterministic_and_equal_to_the_decode_pipeline(tmp_path):
+    H, Hkv, bs = 32, 8, 16
+    lens, T = [900, 2500, 64], [300, 500, 16]
+    w, st, out, ref = run_case(H, Hkv, bs, pa.PA_KV_F16, lens, T, seed=3)
+    again = st.causal()
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+    # the same call with the tensor-core kernel switched off (PA_PREFILL=0, read
+    # once per process): the decode pipeline's result, also within the bar
+    np.save(tmp_path / "tc.npy", out.cpu().numpy())
+    code = f"""
+import sys, numpy as np
+sys.path.insert(0, {ROOT!r}); sys.path.insert(0, {os.path.join(ROOT, 'tests')!r})
+import test_gpu_prefill as t
+import paged_kv_cache_12_gb300 as pa
+w, st, out, ref = t.run_case({H}, {Hkv}, {bs}, pa.PA_KV_F16, {lens}, {T}, seed=3)
+t.compare(t.as_f64(out, pa.PA_KV_F16), ref, pa.PA_KV_F16)
+tc = np.load({str(tmp_path / 'tc.npy')!r}).astype(np.float64)
+assert np.max(np.abs(tc - out.cpu().numpy().astype(np.float64))) <= 2e-3
+"""
+    env = dict(os.environ, PA_PREFILL="0")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout + r.stderr
