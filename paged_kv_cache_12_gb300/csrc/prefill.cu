@@ -39,12 +39,18 @@ namespace pa {
 namespace {
 
 constexpr int PM = 128;                    // query rows per work tile
-constexpr int PN = 64;                     // KV tokens per tile
+#ifndef PA_PF_PN
+#define PA_PF_PN 128
+#endif
+#ifndef PA_PF_STAGES
+#define PA_PF_STAGES 2
+#endif
+constexpr int PN = PA_PF_PN;               // KV tokens per tile (64 or 128)
 constexpr int PD = 128;                    // head dim
-constexpr int PST = 4;                     // K and V ring stages
+constexpr int PST = PA_PF_STAGES;          // K and V ring stages
 constexpr int Q_BYTES = PM * PD * 2;       // 2 K-blocks (64 dims) x 128 rows x 128 B
-constexpr int KV_BYTES = PN * PD * 2;      // 2 blocks (64 dims) x 64 tokens x 128 B
-constexpr int P_BYTES = PM * PN * 2;       // 128 rows x 128 B; two buffers
+constexpr int KV_BYTES = PN * PD * 2;      // 2 blocks (64 dims) x PN tokens x 128 B
+constexpr int P_BYTES = PM * PN * 2;       // PN / 64 blocks (64 tokens) x 128 rows x 128 B; two buffers
 constexpr int OFF_Q = 0;
 constexpr int OFF_K = OFF_Q + Q_BYTES;
 constexpr int OFF_V = OFF_K + PST * KV_BYTES;
@@ -55,8 +61,10 @@ constexpr int CTRL_BAD = 224;              // int: 1 + the work item that met an
 constexpr int CTRL_ABORT = 228;            // int: a role gave up waiting
 constexpr int PF_SMEM = OFF_CTRL + CTRL_BYTES + 1024;   // + alignment slack
 constexpr int PF_THREADS = 7 * 32;         // K producer, V producer, MMA, 4 softmax warps
-constexpr int TMEM_COLS = 256;             // S0 [0, 64), S1 [64, 128), O [128, 256)
-constexpr int TM_O = 128;
+constexpr int TMEM_COLS = PN == 64 ? 256 : 512;   // S0 [0, PN), S1 [PN, 2 PN), O [2 PN, 2 PN + 128)
+constexpr int TM_O = 2 * PN;
+static_assert(PN == 64 || PN == 128, "KV tile of 64 or 128 tokens");
+static_assert(OFF_CTRL + CTRL_BYTES + 1024 <= 227 * 1024, "shared memory of one CTA");
 static_assert(8 * (4 * PST + 11) + 8 <= CTRL_BAD && CTRL_ABORT + 4 <= CTRL_BYTES, "control block layout");
 
 struct PfBars {
@@ -173,6 +181,14 @@ __device__ void pf_mma(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, ui
     const uint32_t base = smem_u32(smem);
     const uint32_t id_s = idesc_f16(PM, PN, bf16, false);
     const uint32_t id_o = idesc_f16(PM, PD, bf16, true);
+    // descriptors of the operand tiles; a byte offset o inside shared memory
+    // is o / 16 added to the descriptor (its low field is the address / 16)
+    const uint64_t dq = sw128_desc(base + OFF_Q, 16, 1024);
+    const uint64_t dk0 = sw128_desc(base + OFF_K, 16, 1024);
+    const uint64_t dp0 = sw128_desc(base + OFF_P, 16, 1024);
+    // V: B operand with N (dims) contiguous: 128-byte rows of 64 dims, one row
+    // per token (K); the next 64 dims are the next block of PN rows
+    const uint64_t dv0 = sw128_desc(base + OFF_V, PN * 128, 1024);
     int kc = 0, vc = 0, sc = 0, pc = 0, qc = 0;
     bool ok = true;
     auto wait = [&](uint32_t bar, uint32_t parity) {
@@ -191,13 +207,13 @@ __device__ void pf_mma(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, ui
         if (!wait(bb.kfull[ks], (kc / PST) & 1)) return;
         if (sc >= 2 && !wait(bb.sfree[b], ((sc >> 1) - 1) & 1)) return;
         tc_fence_after_sync();
-        const uint32_t qa = base + OFF_Q, ka = base + OFF_K + ks * KV_BYTES;
+        const uint64_t dk = dk0 + (uint64_t)(ks * (KV_BYTES >> 4));
+        const uint32_t dst = tmem + b * PN;
 #pragma unroll
         for (int k = 0; k < PD / 16; ++k) {
             // K-step k: 16 dims at byte 32 (k % 4) of the 64-dim block k / 4
-            const uint64_t da = sw128_desc(qa + (k >> 2) * (PM * 128) + (k & 3) * 32, 16, 1024);
-            const uint64_t db = sw128_desc(ka + (k >> 2) * (PN * 128) + (k & 3) * 32, 16, 1024);
-            umma_f16(tmem + b * PN, da, db, id_s, k > 0 ? 1u : 0u);
+            umma_f16(dst, dq + (uint64_t)(((k >> 2) * (PM * 128) + (k & 3) * 32) >> 4),
+                     dk + (uint64_t)(((k >> 2) * (PN * 128) + (k & 3) * 32) >> 4), id_s, k > 0 ? 1u : 0u);
         }
         umma_commit(bb.sfull[b]);
         umma_commit(bb.kempty[ks]);
@@ -217,16 +233,12 @@ __device__ void pf_mma(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, ui
             const int vs = vc % PST;
             if (!wait(bb.vfull[vs], (vc / PST) & 1)) break;
             tc_fence_after_sync();
-            const uint32_t pa_ = base + OFF_P + pb * P_BYTES, va = base + OFF_V + vs * KV_BYTES;
+            const uint64_t dp = dp0 + (uint64_t)(pb * (P_BYTES >> 4));
+            const uint64_t dv = dv0 + (uint64_t)(vs * (KV_BYTES >> 4));
 #pragma unroll
-            for (int k = 0; k < PN / 16; ++k) {
-                const uint64_t da = sw128_desc(pa_ + k * 32, 16, 1024);
-                // V tile, B operand with N (dims) contiguous: 128-byte rows of
-                // 64 dims, one row per token (K); the next 64 dims are the
-                // next block of PN rows; K-step k starts 16 tokens further
-                const uint64_t db = sw128_desc(va + k * 16 * 128, PN * 128, 1024);
-                umma_f16(tmem + TM_O, da, db, id_o, (n > 0 || k > 0) ? 1u : 0u);
-            }
+            for (int k = 0; k < PN / 16; ++k)   // K-step k: 16 tokens: P block k / 4 at byte 32 (k % 4), V row 16 k
+                umma_f16(tmem + TM_O, dp + (uint64_t)(((k >> 2) * (PM * 128) + (k & 3) * 32) >> 4),
+                         dv + (uint64_t)((k * 16 * 128) >> 4), id_o, (n > 0 || k > 0) ? 1u : 0u);
             umma_commit(bb.pvdone[pb]);
             umma_commit(bb.vempty[vs]);
             ++vc;
@@ -287,25 +299,30 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
             if (!wait(bb.sfull[b], (sc >> 1) & 1)) break;
             ++sc;
             tc_fence_after_sync();
-            uint32_t r0[32], r1[32];
-            tmem_ld32(trow + b * PN, r0);
-            tmem_ld32(trow + b * PN + 32, r1);
+            float s[PN];
+#pragma unroll
+            for (int q = 0; q < PN / 32; ++q) {
+                uint32_t r[32];
+                tmem_ld32(trow + b * PN + 32 * q, r);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) s[32 * q + c] = __uint_as_float(r[c]);
+            }
             tmem_wait_ld();
             tc_fence_before_sync();
             mbar_arrive(bb.sfree[b]);
-            float s[PN];
-#pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                s[c] = __uint_as_float(r0[c]);
-                s[c + 32] = __uint_as_float(r1[c]);
-            }
             const int t0 = n * PN;
-            float mx = -INFINITY;
+            if (t0 + PN > vis) {   // the tile reaches past this row's position
 #pragma unroll
-            for (int c = 0; c < PN; ++c) {
-                s[c] = t0 + c < vis ? s[c] * sl2 : -INFINITY;
-                mx = fmaxf(mx, s[c]);
+                for (int c = 0; c < PN; ++c) s[c] = t0 + c < vis ? s[c] : -INFINITY;
             }
+            // row maximum of the raw scores (scale > 0), eight partial maxima
+            float mp[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mp[j] = s[j];
+#pragma unroll
+            for (int c = 8; c < PN; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
+            const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                   fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl2;
             if (mx > mrun + RESCALE_THRESHOLD) {
                 const float nm = fmaxf(mrun, mx);
                 const float alpha = fast_exp2(mrun - nm);
@@ -326,12 +343,6 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
                 l *= alpha;
                 mrun = nm;
             }
-            float p[PN];
-#pragma unroll
-            for (int c = 0; c < PN; ++c) {
-                p[c] = fast_exp2(s[c] - mrun);
-                l += p[c];
-            }
             if (g >= 2 && !wait(bb.pvdone[g & 1], ((g >> 1) - 1) & 1)) break;   // buffer g & 1 free: PV g - 2 done
             // ---- the last KV tile: V rows past the context are zeroed (P is 0 there)
             const int vs = vcount % PST;
@@ -347,16 +358,30 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
                         *reinterpret_cast<uint4 *>(vt + h * (PN * 128) + rr * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
-            // ---- P row into the swizzled A tile of the PV product
+            // ---- p = 2^(s scale log2(e) - m) into the swizzled A tile of the PV
+            // product (chunk c of 8 tokens: block c / 8, 16-byte column c % 8),
+            // and the row sum in eight partial sums
+            float lp[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) lp[j] = 0.f;
 #pragma unroll
             for (int c = 0; c < PN / 8; ++c) {
+                float p[8];
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    p[j] = fast_exp2(fmaf(s[8 * c + j], sl2, -mrun));
+                    lp[j] += p[j];
+                }
                 uint4 v;
-                v.x = pack_p<KV>(p[8 * c + 0], p[8 * c + 1]);
-                v.y = pack_p<KV>(p[8 * c + 2], p[8 * c + 3]);
-                v.z = pack_p<KV>(p[8 * c + 4], p[8 * c + 5]);
-                v.w = pack_p<KV>(p[8 * c + 6], p[8 * c + 7]);
-                *reinterpret_cast<uint4 *>(smem + OFF_P + (g & 1) * P_BYTES + m * 128 + ((c ^ (m & 7)) << 4)) = v;
+                v.x = pack_p<KV>(p[0], p[1]);
+                v.y = pack_p<KV>(p[2], p[3]);
+                v.z = pack_p<KV>(p[4], p[5]);
+                v.w = pack_p<KV>(p[6], p[7]);
+                const int cc = c & 7;
+                *reinterpret_cast<uint4 *>(smem + OFF_P + (g & 1) * P_BYTES + (c >> 3) * (PM * 128) + m * 128 +
+                                           ((cc ^ (m & 7)) << 4)) = v;
             }
+            l += ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
             fence_proxy_async_smem();
             tc_fence_before_sync();
             mbar_arrive(bb.pfull[g & 1]);
