@@ -156,10 +156,10 @@ def causal_flops(w) -> int:
 def prefill_launch(w, kv_dtype) -> bool:
     """Whether a multi-token call also launches the tensor-core kernel for long
     runs of new tokens (the library's rule: head_dim 128, fp16/bf16 cache, G
-    dividing 128, at least 64 query rows in the call; PA_PREFILL=0 disables)."""
+    dividing 128, at least 32 query rows in the call; PA_PREFILL=0 disables)."""
     G = w.num_heads // w.num_kv_heads
     return (multi_token(w) and os.environ.get("PA_PREFILL", "1")[:1] != "0" and w.head_dim == 128
-            and kv_dtype != "fp8" and 128 % G == 0 and w.num_new_tokens * G >= 64)
+            and kv_dtype != "fp8" and 128 % G == 0 and w.num_new_tokens * G >= 32)
 
 
 def kv_write_bytes(w, esz=2) -> int:

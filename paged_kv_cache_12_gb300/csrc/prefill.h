@@ -25,8 +25,11 @@ struct PrefillArgs {
 
 // Query rows per work tile, and the smallest number of query rows
 // (new tokens x G) for which a sequence goes to the tensor-core kernel.
+#ifndef PA_PF_MIN_ROWS
+#define PA_PF_MIN_ROWS 32
+#endif
 constexpr int PF_ROWS = 128;
-constexpr int PF_MIN_ROWS = 64;
+constexpr int PF_MIN_ROWS = PA_PF_MIN_ROWS;
 
 // Launch the prefill kernel on `st` (fp16 or bf16 caches, head_dim 128);
 // it reads its item count from the workspace header; max_items is a host
