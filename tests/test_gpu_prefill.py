@@ -82,3 +82,63 @@ assert np.max(np.abs(tc - out.cpu().numpy().astype(np.float64))) <= 2e-3
     env = dict(os.environ, PA_PREFILL="0")
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+def test_out_of_range_block_id_gives_nan_rows_of_that_sequence_only():
+    H, Hkv, bs = 32, 8, 16
+    lens, T = [900, 1200, 700], [300, 256, 40]
+    w, st, out, ref = run_case(H, Hkv, bs, pa.PA_KV_F16, lens, T, seed=21)
+    compare(as_f64(out, pa.PA_KV_F16), ref, pa.PA_KV_F16)
+    bad = st.d["tables"].clone()
+    bad[1, 0] = w.num_blocks + 5          # never read: the tiles that meet it write NaN
+    st.d["tables"] = bad
+    out2 = st.causal().cpu().numpy()
+    qs = w.query_start
+    assert np.isnan(out2[qs[1]:qs[2]]).all()
+    keep = np.r_[qs[0]:qs[1], qs[2]:qs[3]]
+    compare(out2[keep].astype(np.float64), ref[keep], pa.PA_KV_F16)
+
+
+def test_graph_capture_of_a_mixed_call():
+    # a prompt chunk (tensor-core kernel) and decode rows (decode pipeline) in one
+    # call, captured once in a CUDA Graph: replays give the eager bits, also after
+    # new query rows are copied into the captured buffer
+    H, Hkv, bs = 32, 8, 16
+    lens, T = [1500, 300, 64, 2000], [500, 1, 1, 3]
+    w = workloads.custom(seed=8, num_seqs=len(lens), num_heads=H, num_kv_heads=Hkv, head_dim=128, block_size=bs,
+                         context_lens=lens, new_tokens=T, multi=True)
+    st = TypedStep(w, pa.PA_KV_F16)
+    st.run_gpu()
+    d = st.d
+    qs = torch.from_numpy(w.query_start).cuda()
+    out = torch.empty_like(d["qm"])
+    ws = torch.zeros(pa.pa_attention_causal_workspace_size(w.num_seqs, w.num_new_tokens, H, Hkv, 128,
+                                                           w.max_context_len), dtype=torch.uint8, device="cuda")
+
+    def call(stream=None):
+        pa.pa_attention_causal(out, d["qm"], d["k"], d["v"], d["tables"], d["lens"], qs, w.scale, w.max_context_len,
+                               ws, stream)
+
+    call()                                     # first call: one-time set-up outside the capture
+    torch.cuda.synchronize()
+    eager = out.clone()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            call(s)
+    torch.cuda.current_stream().wait_stream(s)
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager.view(torch.int16))
+    d["qm"].copy_(torch.flip(d["qm"], dims=[0]))
+    call()
+    torch.cuda.synchronize()
+    eager2 = out.clone()
+    out.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), eager2.view(torch.int16))
+    assert not torch.equal(eager2.view(torch.int16), eager.view(torch.int16))
