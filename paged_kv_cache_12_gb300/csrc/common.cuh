@@ -155,11 +155,20 @@ __device__ __forceinline__ uint32_t pack_bf162(float lo, float hi) {
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
-// Two FP8 E4M3 codes (low byte first) -> their exact values as fp16x2 (low
-// half from the low byte).  Every E4M3 value is an fp16 value.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// Two FP8 E4M3 codes -> their exact values as fp16x2 (every E4M3 value is an
+// fp16 value): the codes in bytes 0 and 1 (lo) or 2 and 3 (hi) of a register,
+// the lower byte going to the lower half.  One conversion instruction each:
+// the 16-bit operand is a half of the 32-bit register and the result is the
+// fp16x2 register itself, with no masking, shifting or repacking around it.
+__device__ __forceinline__ uint32_t e4m3x2_lo_to_f16x2(uint32_t codes) {
+    uint32_t r;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.rn.f16x2.e4m3x2 %0, l; }" : "=r"(r) : "r"(codes));
+    return r;
+}
+__device__ __forceinline__ uint32_t e4m3x2_hi_to_f16x2(uint32_t codes) {
+    uint32_t r;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; cvt.rn.f16x2.e4m3x2 %0, h; }" : "=r"(r) : "r"(codes));
+    return r;
 }
 
 }  // namespace pa

@@ -710,14 +710,14 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                     uint32_t r0, r1, r2, r3;
                     ldmatrix_x4(kt + koff[u], r0, r1, r2, r3);
                     uint32_t af[2][4];
-                    af[0][0] = e4m3x2_to_f16x2(r0);
-                    af[0][2] = e4m3x2_to_f16x2(r0 >> 16);
-                    af[0][1] = e4m3x2_to_f16x2(r1);
-                    af[0][3] = e4m3x2_to_f16x2(r1 >> 16);
-                    af[1][0] = e4m3x2_to_f16x2(r2);
-                    af[1][2] = e4m3x2_to_f16x2(r2 >> 16);
-                    af[1][1] = e4m3x2_to_f16x2(r3);
-                    af[1][3] = e4m3x2_to_f16x2(r3 >> 16);
+                    af[0][0] = e4m3x2_lo_to_f16x2(r0);
+                    af[0][2] = e4m3x2_hi_to_f16x2(r0);
+                    af[0][1] = e4m3x2_lo_to_f16x2(r1);
+                    af[0][3] = e4m3x2_hi_to_f16x2(r1);
+                    af[1][0] = e4m3x2_lo_to_f16x2(r2);
+                    af[1][2] = e4m3x2_hi_to_f16x2(r2);
+                    af[1][1] = e4m3x2_lo_to_f16x2(r3);
+                    af[1][3] = e4m3x2_hi_to_f16x2(r3);
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
@@ -756,10 +756,10 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t lo = __byte_perm(r4[2 * h], 0, 0x3120);       // tokens 2cq, 2cq+1
                         const uint32_t hi = __byte_perm(r4[2 * h + 1], 0, 0x3120);   // tokens 2cq+8, 2cq+9
-                        va[2 * u + h][0] = e4m3x2_to_f16x2(lo);
-                        va[2 * u + h][1] = e4m3x2_to_f16x2(lo >> 16);
-                        va[2 * u + h][2] = e4m3x2_to_f16x2(hi);
-                        va[2 * u + h][3] = e4m3x2_to_f16x2(hi >> 16);
+                        va[2 * u + h][0] = e4m3x2_lo_to_f16x2(lo);
+                        va[2 * u + h][1] = e4m3x2_hi_to_f16x2(lo);
+                        va[2 * u + h][2] = e4m3x2_lo_to_f16x2(hi);
+                        va[2 * u + h][3] = e4m3x2_hi_to_f16x2(hi);
                     }
                 }
             } else {
@@ -834,8 +834,8 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t lo = __byte_perm(r4[2 * h], 0, 0x3120);
                         const uint32_t hi = __byte_perm(r4[2 * h + 1], 0, 0x3120);
-                        uint32_t f[4] = {e4m3x2_to_f16x2(lo), e4m3x2_to_f16x2(lo >> 16), e4m3x2_to_f16x2(hi),
-                                         e4m3x2_to_f16x2(hi >> 16)};
+                        uint32_t f[4] = {e4m3x2_lo_to_f16x2(lo), e4m3x2_hi_to_f16x2(lo), e4m3x2_lo_to_f16x2(hi),
+                                         e4m3x2_hi_to_f16x2(hi)};
                         if (tail) {
                             f[0] &= vlo;
                             f[1] &= vlo;
