@@ -634,11 +634,17 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
         }
 
         // the group's query rows as MMA B fragments: B = Q^T (k = dim, n = head)
+        // Columns past the item's query rows get zeros, not what an earlier
+        // item left in the slot: a thread's two columns share one rescale
+        // decision, so stale values there could move a real column's
+        // running maximum and with it the rounding of the result.
         uint32_t qb[NT][KS][2];
         {
             const __half *qs = reinterpret_cast<const __half *>(smem + c * C::DATA + DEPTH * C::STAGE + q * C::QSLOT);
+            const int rows = dp->nmem * a.G;
 #pragma unroll
-            for (int t = 0; t < NT; ++t)
+            for (int t = 0; t < NT; ++t) {
+                const bool live = t * 8 + r < rows;
 #pragma unroll
                 for (int k = 0; k < KS; ++k) {
                     if constexpr (C::FP8) {
@@ -647,14 +653,15 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                         // pair u = k / 2 uses dims 32u + 16 (k % 2) + 4 cq .. + 3
                         const __half *row = qs + (t * 8 + r) * D + 16 * k + 4 * cq;
                         const uint2 v = *reinterpret_cast<const uint2 *>(row);
-                        qb[t][k][0] = v.x;
-                        qb[t][k][1] = v.y;
+                        qb[t][k][0] = live ? v.x : 0u;
+                        qb[t][k][1] = live ? v.y : 0u;
                     } else {
                         const __half *row = qs + (t * 8 + r) * D + 16 * k + 2 * cq;
-                        qb[t][k][0] = *reinterpret_cast<const uint32_t *>(row);
-                        qb[t][k][1] = *reinterpret_cast<const uint32_t *>(row + 8);
+                        qb[t][k][0] = live ? *reinterpret_cast<const uint32_t *>(row) : 0u;
+                        qb[t][k][1] = live ? *reinterpret_cast<const uint32_t *>(row + 8) : 0u;
                     }
                 }
+            }
         }
         const int nchunks = dp->nchunks;
         // CAUSAL: tokens of the item (from its start) that each column's query

@@ -195,7 +195,7 @@ CASES = [(8, 8, 128, 16), (64, 8, 128, 16), (32, 4, 128, 32), (16, 2, 128, 8), (
 def test_decode_typed_against_oracle(kv, H, Hkv, D, bs):
     if kv == pa.PA_KV_FP8_E4M3 and D != 128:
         pytest.skip("fp8 caches are built for head_dim 128")
-    lens = [1, 2, 15, 16, 17, 100, 511, 512, 513, 1025, 2100, 3000]
+    lens = [1, 2, 15, 16, 17, 31, 32, 33, 47, 100, 511, 512, 513, 1025, 2100, 3000]
     w = workloads.custom(seed=H + bs + D + kv, num_seqs=len(lens), num_heads=H, num_kv_heads=Hkv, head_dim=D,
                          block_size=bs, context_lens=lens)
     st = TypedStep(w, kv)
