@@ -12,19 +12,25 @@
 // tokens times the G query heads of the kv head (rows token-major), so a K/V
 // tile read from HBM serves all of them.  One CTA per SM, persistent over a
 // static list of tiles ordered longest first; six warps:
-//   warps 0-1  producers of K and of V: per 64-token KV tile, TMA copies of
+//   warps 0-1  producers of K and of V: per 128-token KV tile, TMA copies of
 //              the block rows (gathered through the block table, one lane per
-//              block) into 4-stage rings;
+//              block) into 3-stage rings;
 //   warp 2     MMA issuer (one thread): S = Q K^T into one of two tensor
-//              memory buffers (M 128, N 64, K 128), then O += P V (M 128,
-//              N 128, K 64) into a tensor-memory accumulator; completions are
-//              committed to mbarriers;
-//   warps 3-6  softmax (one query row per thread): read the row of S from
-//              tensor memory, mask past the row's position, online softmax in
-//              fp32 with the running maximum rescaled only when it grows by
-//              more than 2^8 (then O is rescaled in tensor memory), write P
-//              (fp16/bf16) to shared memory for the PV product, and at the
-//              end divide O by the row sum and store the output row.
+//              memory buffers (M 128, N 128, K 128), then O += P V (M 128,
+//              N 128, K 128) into a tensor-memory accumulator, both with the
+//              A operand (Q, P) in tensor memory and B (K, V) in shared
+//              memory; completions are committed to mbarriers;
+//   warps 3-6  softmax (one query row per thread, the row's tensor-memory
+//              lane): store the Q row into tensor memory, read the row of S,
+//              mask past the row's position, online softmax in fp32 with the
+//              running maximum rescaled only when it grows by more than 2^8
+//              (then O is rescaled in tensor memory), store P (fp16/bf16) into
+//              tensor memory for the PV product, and at the end divide O by
+//              the row sum and store the output row.
+// Q and P live in tensor memory so that shared memory holds only K/V rings,
+// three stages deep: a 32 KB K or V tile takes about 2 us to arrive from L2,
+// and with two stages that latency, not the tensor or exponential work, set
+// the time per KV tile.
 // S for the next KV tile is computed while the softmax works on this one.
 // Every wait is bounded; tensor memory is released on every path.
 
@@ -43,33 +49,34 @@ constexpr int PM = 128;                    // query rows per work tile
 #define PA_PF_PN 128
 #endif
 #ifndef PA_PF_STAGES
-#define PA_PF_STAGES 2
+#define PA_PF_STAGES 3
 #endif
 constexpr int PN = PA_PF_PN;               // KV tokens per tile (64 or 128)
 constexpr int PD = 128;                    // head dim
 constexpr int PST = PA_PF_STAGES;          // K and V ring stages
-constexpr int Q_BYTES = PM * PD * 2;       // 2 K-blocks (64 dims) x 128 rows x 128 B
 constexpr int KV_BYTES = PN * PD * 2;      // 2 blocks (64 dims) x PN tokens x 128 B
-constexpr int P_BYTES = PM * PN * 2;       // PN / 64 blocks (64 tokens) x 128 rows x 128 B; two buffers
-constexpr int OFF_Q = 0;
-constexpr int OFF_K = OFF_Q + Q_BYTES;
+constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + PST * KV_BYTES;
-constexpr int OFF_P = OFF_V + PST * KV_BYTES;
-constexpr int OFF_CTRL = OFF_P + 2 * P_BYTES;
+constexpr int OFF_CTRL = OFF_V + PST * KV_BYTES;
 constexpr int CTRL_BYTES = 256;
 constexpr int CTRL_BAD = 224;              // int: 1 + the work item that met an out-of-range block id
 constexpr int CTRL_ABORT = 228;            // int: a role gave up waiting
 constexpr int PF_SMEM = OFF_CTRL + CTRL_BYTES + 1024;   // + alignment slack
 constexpr int PF_THREADS = 7 * 32;         // K producer, V producer, MMA, 4 softmax warps
-constexpr int TMEM_COLS = PN == 64 ? 256 : 512;   // S0 [0, PN), S1 [PN, 2 PN), O [2 PN, 2 PN + 128)
+// tensor memory: S0 [0, PN), S1 [PN, 2 PN), O (128 fp32 columns), Q (128 dims,
+// two fp16/bf16 per column), P (PN tokens, two per column)
+constexpr int TMEM_COLS = 512;
 constexpr int TM_O = 2 * PN;
+constexpr int TM_Q = TM_O + PD;
+constexpr int TM_P = TM_Q + PD / 2;
+static_assert(TM_P + PN / 2 <= TMEM_COLS, "tensor-memory columns");
 static_assert(PN == 64 || PN == 128, "KV tile of 64 or 128 tokens");
 static_assert(OFF_CTRL + CTRL_BYTES + 1024 <= 227 * 1024, "shared memory of one CTA");
 static_assert(8 * (4 * PST + 11) + 8 <= CTRL_BAD && CTRL_ABORT + 4 <= CTRL_BYTES, "control block layout");
 
 struct PfBars {
-    // pfull / pvdone: one per P buffer, so that a softmax warp a step ahead of
-    // another never adds its arrival to the other step's phase
+    // pfull / pvdone: one per PV-number parity, so that a softmax warp a step
+    // ahead of another never adds its arrival to the other step's phase
     uint32_t kfull[PST], kempty[PST], vfull[PST], vempty[PST], sfull[2], sfree[2], pfull[2], pvdone[2], qfull;
     uint32_t tmem_slot, flags;   // shared addresses
 };
@@ -181,11 +188,9 @@ __device__ void pf_mma(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, ui
     const uint32_t base = smem_u32(smem);
     const uint32_t id_s = idesc_f16(PM, PN, bf16, false);
     const uint32_t id_o = idesc_f16(PM, PD, bf16, true);
-    // descriptors of the operand tiles; a byte offset o inside shared memory
-    // is o / 16 added to the descriptor (its low field is the address / 16)
-    const uint64_t dq = sw128_desc(base + OFF_Q, 16, 1024);
+    // descriptors of the shared-memory B tiles; a byte offset o inside shared
+    // memory is o / 16 added to the descriptor (its low field is the address / 16)
     const uint64_t dk0 = sw128_desc(base + OFF_K, 16, 1024);
-    const uint64_t dp0 = sw128_desc(base + OFF_P, 16, 1024);
     // V: B operand with N (dims) contiguous: 128-byte rows of 64 dims, one row
     // per token (K); the next 64 dims are the next block of PN rows
     const uint64_t dv0 = sw128_desc(base + OFF_V, PN * 128, 1024);
@@ -211,9 +216,9 @@ __device__ void pf_mma(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, ui
         const uint32_t dst = tmem + b * PN;
 #pragma unroll
         for (int k = 0; k < PD / 16; ++k) {
-            // K-step k: 16 dims at byte 32 (k % 4) of the 64-dim block k / 4
-            umma_f16(dst, dq + (uint64_t)(((k >> 2) * (PM * 128) + (k & 3) * 32) >> 4),
-                     dk + (uint64_t)(((k >> 2) * (PN * 128) + (k & 3) * 32) >> 4), id_s, k > 0 ? 1u : 0u);
+            // K-step k: 16 dims = Q columns 8k .. 8k + 7; K at byte 32 (k % 4) of the 64-dim block k / 4
+            umma_f16_ts(dst, tmem + TM_Q + 8 * k, dk + (uint64_t)(((k >> 2) * (PN * 128) + (k & 3) * 32) >> 4), id_s,
+                        k > 0 ? 1u : 0u);
         }
         umma_commit(bb.sfull[b]);
         umma_commit(bb.kempty[ks]);
@@ -227,18 +232,17 @@ __device__ void pf_mma(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, ui
         issue_s();
         for (int n = 0; n < t.nkv && ok; ++n) {
             if (n + 1 < t.nkv) issue_s();
-            const int pb = pc & 1;   // PV number pc reads P buffer pc & 1
+            const int pb = pc & 1;   // barrier parity of PV number pc
             if (!wait(bb.pfull[pb], (pc >> 1) & 1)) break;
             ++pc;
             const int vs = vc % PST;
             if (!wait(bb.vfull[vs], (vc / PST) & 1)) break;
             tc_fence_after_sync();
-            const uint64_t dp = dp0 + (uint64_t)(pb * (P_BYTES >> 4));
             const uint64_t dv = dv0 + (uint64_t)(vs * (KV_BYTES >> 4));
 #pragma unroll
-            for (int k = 0; k < PN / 16; ++k)   // K-step k: 16 tokens: P block k / 4 at byte 32 (k % 4), V row 16 k
-                umma_f16(tmem + TM_O, dp + (uint64_t)(((k >> 2) * (PM * 128) + (k & 3) * 32) >> 4),
-                         dv + (uint64_t)((k * 16 * 128) >> 4), id_o, (n > 0 || k > 0) ? 1u : 0u);
+            for (int k = 0; k < PN / 16; ++k)   // K-step k: 16 tokens = P columns 8k .. 8k + 7, V row 16 k
+                umma_f16_ts(tmem + TM_O, tmem + TM_P + 8 * k, dv + (uint64_t)((k * 16 * 128) >> 4), id_o,
+                            (n > 0 || k > 0) ? 1u : 0u);
             umma_commit(bb.pvdone[pb]);
             umma_commit(bb.vempty[vs]);
             ++vc;
@@ -256,10 +260,10 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
     const int quarter = (threadIdx.x >> 5) & 3;    // tensor-memory lanes 32 quarter .. + 31
     const int m = quarter * 32 + lane;             // this thread's query row in the tile
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t base = smem_u32(smem);
     const float sl2 = a.scale_log2;
-    // g: P tiles written so far (P tile g feeds PV number g, buffer g & 1);
-    // pvdone[b] completes for PV numbers b, b + 2, ... in order
+    // g: P tiles written so far (P tile g feeds PV number g; one P buffer, so
+    // P tile g is stored once PV number g - 1 is done); pvdone[b] completes
+    // for PV numbers b, b + 2, ... in order
     int sc = 0, g = 0, vcount = 0;
     bool ok = true;
     // every thread of the warp takes the same decision, so warp-collective
@@ -279,16 +283,26 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
         const int tok = m / a.G, hh = m - tok * a.G;
         const bool valid = tok < t.ntok;
         const long long qrow = ((long long)(t.q0 + t.row0 + tok) * a.Hq + t.kvh * a.G + hh) * PD;
-        // ---- Q row into the swizzled A tile (zeros past the new tokens)
+        // ---- Q row into this thread's lane of the tensor-memory A tile, two
+        // dims per column (zeros past the new tokens); the previous tile's
+        // products, which read Q, are done (its last PV was waited for)
         {
             const uint4 *src = reinterpret_cast<const uint4 *>(a.query + qrow);
 #pragma unroll
-            for (int c = 0; c < PD / 8; ++c) {
-                const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-                const int kb = c >> 3, cc = c & 7;
-                *reinterpret_cast<uint4 *>(smem + OFF_Q + kb * (PM * 128) + m * 128 + ((cc ^ (m & 7)) << 4)) = v;
+            for (int h = 0; h < 2; ++h) {
+                uint32_t r[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint4 v = valid ? __ldg(src + 8 * h + c) : make_uint4(0, 0, 0, 0);
+                    r[4 * c] = v.x;
+                    r[4 * c + 1] = v.y;
+                    r[4 * c + 2] = v.z;
+                    r[4 * c + 3] = v.w;
+                }
+                tmem_st32(trow + TM_Q + 32 * h, r);
             }
-            fence_proxy_async_smem();
+            tmem_wait_st();
+            tc_fence_before_sync();
             mbar_arrive(bb.qfull);
         }
         const int vis = valid ? t.C + t.row0 + tok : 1;   // positions this row sees
@@ -343,12 +357,12 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
                 l *= alpha;
                 mrun = nm;
             }
-            if (g >= 2 && !wait(bb.pvdone[g & 1], ((g >> 1) - 1) & 1)) break;   // buffer g & 1 free: PV g - 2 done
             // ---- the last KV tile: V rows past the context are zeroed (P is 0 there)
             const int vs = vcount % PST;
             const int vphase = (vcount / PST) & 1;
             ++vcount;
-            if (t0 + PN > t.L) {
+            const bool zero_v = t0 + PN > t.L;
+            if (zero_v) {
                 if (!wait(bb.vfull[vs], vphase)) break;
                 const int first = t.L - t0;    // rows first .. PN-1 of both 64-dim blocks
                 uint8_t *vt = smem + OFF_V + vs * KV_BYTES;
@@ -358,31 +372,42 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
                         *reinterpret_cast<uint4 *>(vt + h * (PN * 128) + rr * 128 + cc * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
-            // ---- p = 2^(s scale log2(e) - m) into the swizzled A tile of the PV
-            // product (chunk c of 8 tokens: block c / 8, 16-byte column c % 8),
+            // ---- p = 2^(s scale log2(e) - m), packed two per column into this
+            // thread's lane of the tensor-memory P tile (64 tokens per store),
             // and the row sum in eight partial sums
             float lp[8];
 #pragma unroll
             for (int j = 0; j < 8; ++j) lp[j] = 0.f;
+            auto pack64 = [&](int h, uint32_t (&r)[32]) {
 #pragma unroll
-            for (int c = 0; c < PN / 8; ++c) {
-                float p[8];
+                for (int c = 0; c < 8; ++c) {   // tokens 64 h + 8 c .. + 7
+                    float p[8];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    p[j] = fast_exp2(fmaf(s[8 * c + j], sl2, -mrun));
-                    lp[j] += p[j];
+                    for (int j = 0; j < 8; ++j) {
+                        p[j] = fast_exp2(fmaf(s[64 * h + 8 * c + j], sl2, -mrun));
+                        lp[j] += p[j];
+                    }
+                    r[4 * c] = pack_p<KV>(p[0], p[1]);
+                    r[4 * c + 1] = pack_p<KV>(p[2], p[3]);
+                    r[4 * c + 2] = pack_p<KV>(p[4], p[5]);
+                    r[4 * c + 3] = pack_p<KV>(p[6], p[7]);
                 }
-                uint4 v;
-                v.x = pack_p<KV>(p[0], p[1]);
-                v.y = pack_p<KV>(p[2], p[3]);
-                v.z = pack_p<KV>(p[4], p[5]);
-                v.w = pack_p<KV>(p[6], p[7]);
-                const int cc = c & 7;
-                *reinterpret_cast<uint4 *>(smem + OFF_P + (g & 1) * P_BYTES + (c >> 3) * (PM * 128) + m * 128 +
-                                           ((cc ^ (m & 7)) << 4)) = v;
+            };
+            {
+                uint32_t r[32];
+                pack64(0, r);
+                // one P buffer: PV g - 1 (which reads P tile g - 1) is done first
+                if (g >= 1 && !wait(bb.pvdone[(g - 1) & 1], ((g - 1) >> 1) & 1)) break;
+                tmem_st32(trow + TM_P, r);
+            }
+            if constexpr (PN == 128) {
+                uint32_t r[32];
+                pack64(1, r);
+                tmem_st32(trow + TM_P + 32, r);
             }
             l += ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
-            fence_proxy_async_smem();
+            tmem_wait_st();
+            if (zero_v) fence_proxy_async_smem();   // the zeroed V rows, for the tensor cores
             tc_fence_before_sync();
             mbar_arrive(bb.pfull[g & 1]);
             ++g;
