@@ -210,7 +210,7 @@ def test_streams_are_respected():
     compare(to_np(d["out"]), st.oracle_out(kc, vc))
 
 
-@pytest.mark.parametrize("B,H,Hkv,max_ctx,pt", [(4, 8, 2, 3000, 256), (32, 16, 16, 4000, 512), (25, 16, 8, 21000, 1024)])
+@pytest.mark.parametrize("B,H,Hkv,max_ctx,pt", [(4, 8, 2, 3000, 256), (64, 32, 8, 8000, 512), (25, 64, 8, 21000, 1024)])
 def test_partition_sizes(B, H, Hkv, max_ctx, pt):
     """The partition size follows the shapes (256, 512 or 1024 tokens); each is
     checked against the oracle on ragged lengths."""
@@ -219,8 +219,11 @@ def test_partition_sizes(B, H, Hkv, max_ctx, pt):
     lens[0] = max_ctx
     w = workloads.custom(seed=B + H, num_seqs=B, num_heads=H, num_kv_heads=Hkv, head_dim=128, block_size=16,
                          context_lens=lens)
-    # the size the library picks: largest of 1024/512/256 reaching 4096 estimated items
-    picked = next((p for p in (1024, 512) if B * Hkv * -(-max_ctx // p) >= 4096), 256)
+    # the size the library picks: largest of 1024/512/256 reaching 4096 estimated
+    # items, times 8 / G for GQA groups G smaller than 8
+    G = H // Hkv
+    target = 4096 * (8 // G if G < 8 else 1)
+    picked = next((p for p in (1024, 512) if B * Hkv * -(-max_ctx // p) >= target), 256)
     assert picked == pt
     run_step(w)
 

@@ -54,8 +54,8 @@ def test_prompt_chunks_against_oracle(kv, H, Hkv, bs):
 
 
 def test_long_history_many_kv_tiles():
-    # 16k positions before a 256-token chunk: 260 KV tiles per row tile,
-    # scores drawn large enough that the running maximum moves often
+    # 16k positions before a 256-token chunk: 130 KV tiles of 128 tokens per
+    # row tile, scores drawn large enough that the running maximum moves often
     w, st, out, ref = run_case(32, 8, 16, pa.PA_KV_F16, [16384 + 256], [256], seed=5)
     compare(as_f64(out, pa.PA_KV_F16), ref, pa.PA_KV_F16)
 
@@ -82,6 +82,37 @@ assert np.max(np.abs(tc - out.cpu().numpy().astype(np.float64))) <= 2e-3
     env = dict(os.environ, PA_PREFILL="0")
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stdout + r.stderr
+
+
+@pytest.mark.parametrize("kv", [pa.PA_KV_F16, pa.PA_KV_BF16])
+def test_long_ranges_of_mixed_lengths_against_oracle(kv):
+    # Row tiles of very different KV lengths in one call, at G = 8: a chunk
+    # after a 4000-token history (200 new tokens), a short chunk after 8936
+    # positions (71 KV tiles), a whole 4200-token prompt (row tiles reading
+    # 1 .. 33 KV tiles) and a decode row.
+    lens, T = [4200, 9000, 3], [200, 64, 1]
+    if kv == pa.PA_KV_F16:
+        lens, T = lens + [4200], T + [4200]
+    w, st, out, ref = run_case(8, 1, 16, kv, lens, T, seed=31 + kv)
+    compare(as_f64(out, kv), ref, kv)
+    again = st.causal()
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+
+
+def test_out_of_range_block_id_deep_in_a_long_range():
+    # a bad id met 37 KV tiles into a 71-tile range: every row of that
+    # sequence is NaN, the other sequence is untouched
+    H, Hkv, bs = 16, 2, 16
+    lens, T = [9000, 300], [64, 40]
+    w, st, out, ref = run_case(H, Hkv, bs, pa.PA_KV_F16, lens, T, seed=23)
+    compare(as_f64(out, pa.PA_KV_F16), ref, pa.PA_KV_F16)
+    bad = st.d["tables"].clone()
+    bad[0, 300] = w.num_blocks + 9          # position 4800
+    st.d["tables"] = bad
+    out2 = st.causal().cpu().numpy()
+    qs = w.query_start
+    assert np.isnan(out2[qs[0]:qs[1]]).all()
+    compare(out2[qs[1]:qs[2]].astype(np.float64), ref[qs[1]:qs[2]], pa.PA_KV_F16)
 
 
 def test_out_of_range_block_id_gives_nan_rows_of_that_sequence_only():
