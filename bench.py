@@ -440,7 +440,7 @@ def run_ours(args):
     ws = torch.zeros(nws, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def writes_on(st):
+    def writes_on(st, nk=nk, nv=nv):
         if has_pairs:
             pa.pa_block_copy(k, v, d_pairs, st)
         if kvd == "fp8":
@@ -448,7 +448,7 @@ def run_ours(args):
         else:
             pa.pa_kv_write(nk, nv, d_slots, k, v, st)
 
-    def decode_on(st):
+    def decode_on(st, q=q, out=out):
         if multi and typed:
             pa.pa_attention_causal_typed(out, q, k, v, d_tables, d_lens, d_qs, w.scale, w.max_context_len, ws, ks, vs,
                                          st)
@@ -534,6 +534,28 @@ def run_ours(args):
     h_nv = torch.from_numpy(np.ascontiguousarray(nv_host)).pin_memory().view(row_dt)
     h_out = torch.empty((layers,) + tuple(out.shape), dtype=out.dtype).pin_memory()
 
+    # Layer l's inputs are copied in on a copy stream while layer l - 1 computes
+    # (two device buffers of each), and its output is copied out while layer
+    # l + 1 computes; every copy stays inside the timed region.
+    cps = torch.cuda.Stream()
+    qb, nkb, nvb, outb = [q, torch.empty_like(q)], [nk, torch.empty_like(nk)], [nv, torch.empty_like(nv)], \
+        [out, torch.empty_like(out)]
+    ev_in = [torch.cuda.Event() for _ in range(2)]       # buffer b's inputs are on the device
+    ev_used = [torch.cuda.Event() for _ in range(2)]     # buffer b's inputs consumed, its output written
+    ev_out = [torch.cuda.Event() for _ in range(2)]      # buffer b's output copied out
+    for b in range(2):
+        ev_used[b].record(stream)
+        ev_out[b].record(stream)
+
+    def copy_in(l):
+        b = l & 1
+        with torch.cuda.stream(cps):
+            cps.wait_event(ev_used[b])
+            qb[b].copy_(h_q, non_blocking=True)
+            nkb[b].copy_(h_nk, non_blocking=True)
+            nvb[b].copy_(h_nv, non_blocking=True)
+            ev_in[b].record(cps)
+
     def e2e_step():
         d_tables.copy_(h_tables, non_blocking=True)
         d_lens.copy_(h_lens, non_blocking=True)
@@ -542,13 +564,21 @@ def run_ours(args):
             d_pairs.copy_(h_pairs, non_blocking=True)
         if multi:
             d_qs.copy_(h_qs, non_blocking=True)
+        copy_in(0)
         for l in range(layers):
-            q.copy_(h_q, non_blocking=True)
-            nk.copy_(h_nk, non_blocking=True)
-            nv.copy_(h_nv, non_blocking=True)
-            writes()
-            decode()
-            h_out[l].copy_(out, non_blocking=True)
+            b = l & 1
+            if l + 1 < layers:
+                copy_in(l + 1)
+            stream.wait_event(ev_in[b])
+            stream.wait_event(ev_out[b])
+            writes_on(stream, nkb[b], nvb[b])
+            decode_on(stream, qb[b], outb[b])
+            ev_used[b].record(stream)
+            with torch.cuda.stream(cps):
+                cps.wait_event(ev_used[b])
+                h_out[l].copy_(outb[b], non_blocking=True)
+                ev_out[b].record(cps)
+        stream.wait_stream(cps)   # the step's last output is on the host
 
     for _ in range(args.warmup):
         e2e_step()
