@@ -147,9 +147,10 @@ PA_API size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_h
  *   out[i][h] = sum_t softmax(s)_t * V_t[g].
  * The context is processed in partitions of PT tokens, PT the largest of
  * 1024, 512 and 256 for which num_seqs * num_kv_heads *
- * ceil(max_context_len / PT) >= 4096 (256 if none); a sequence longer than
- * one partition is finished by a log-sum-exp merge of its partitions.  PT
- * depends on these host-side sizes only.
+ * ceil(max_context_len / PT) >= 4096 * max(1, 8 / G), G = num_heads /
+ * num_kv_heads (256 if none); a sequence longer than one partition is
+ * finished by a log-sum-exp merge of its partitions.  PT depends on these
+ * host-side sizes only.
  * Arithmetic: fp16 inputs, fp32 accumulation, fp16 output.
  *
  *   out            fp16 [num_seqs][num_heads][head_dim]

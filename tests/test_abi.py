@@ -46,6 +46,12 @@ def test_workspace_size_is_a_host_bound():
     assert pa.pa_decode_workspace_size(100, 64, 8, 128, 256) < 100 * 64 * 128 * 4
     # few sequences: shorter partitions (256 tokens) so that the work still spreads
     assert pa.pa_decode_workspace_size(2, 8, 1, 128, 8192) >= 2 * 32 * 8 * 128 * 4
+    # groups smaller than 8 aim at 8 / G times as many items: 64 x 32 kv heads x
+    # 2048 tokens takes 1024-token partitions at G = 8, 256-token ones at G = 1
+    g8 = pa.pa_decode_workspace_size(64, 256, 32, 128, 2048)
+    assert 64 * 2 * 256 * 128 * 4 <= g8 < 64 * 3 * 256 * 128 * 4
+    g1 = pa.pa_decode_workspace_size(64, 32, 32, 128, 2048)
+    assert 64 * 8 * 32 * 128 * 4 <= g1 < 64 * 9 * 32 * 128 * 4
     assert pa.lib().pa_decode_workspace_size(1, 8, 0, 128, 10) == 0
     # multi-token form: a partial row per query row and partition (400 rows x 8 partitions of 1024)
     spec = pa.pa_attention_causal_workspace_size(100, 400, 64, 8, 128, 8192)
