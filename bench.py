@@ -60,6 +60,8 @@ def parse():
                    help="cache element type: fp16 (the pages'), bf16, or fp8 E4M3 codes with one scale per cache")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-graph", action="store_true", help="skip the CUDA Graph replay measurement")
+    p.add_argument("--no-records", action="store_true",
+                   help="headline run: skip the per-layer records of the other workloads")
     p.add_argument("--shared-prefix", action="store_true",
                    help="parallel-sampling workloads: decode with pa_decode_shared_prefix (samples of one prompt "
                         "read its blocks together)")
@@ -155,11 +157,11 @@ def causal_flops(w) -> int:
 
 def prefill_launch(w, kv_dtype) -> bool:
     """Whether a multi-token call also launches the tensor-core kernel for long
-    runs of new tokens (the library's rule: head_dim 128, fp16/bf16 cache, G
-    dividing 128, at least 32 query rows in the call; PA_PREFILL=0 disables)."""
+    runs of new tokens (the library's rule: head_dim 128, G dividing 128, at
+    least 32 query rows in the call; PA_PREFILL=0 disables)."""
     G = w.num_heads // w.num_kv_heads
     return (multi_token(w) and os.environ.get("PA_PREFILL", "1")[:1] != "0" and w.head_dim == 128
-            and kv_dtype != "fp8" and 128 % G == 0 and w.num_new_tokens * G >= 32)
+            and 128 % G == 0 and w.num_new_tokens * G >= 32)
 
 
 def kv_write_bytes(w, esz=2) -> int:
@@ -335,12 +337,10 @@ def workload(args):
                             multi=w.multi)
 
 
-def allocate(w, pa):
-    """Run the workload's history through the host allocator (parallel-sampling
+def history_allocator(w, pa):
+    """A host allocator holding the workload's history (parallel-sampling
     workloads: one prompt per group, forked to its samples, the parent
-    released), then this step's appends.  Returns the allocator, the step's
-    slot mapping and copy pairs, block tables, lengths and the step's
-    allocation time in microseconds."""
+    released): the state the step starts from."""
     al = pa.Allocator(w.num_blocks, w.block_size, free_order=w.free_order)
     ids = list(range(w.num_seqs))
     if w.num_prompts:
@@ -355,11 +355,28 @@ def allocate(w, pa):
         for s in ids:
             al.add_seq(s)
         al.append(ids, w.history_lens)
-    t0 = time.perf_counter()
+    return al
+
+
+def step_allocation(al, w):
+    """The step's host allocation (step a1): slots for the step's new tokens
+    (and the copy-on-write pairs they need), then the block tables and lengths
+    the kernels read."""
+    ids = list(range(w.num_seqs))
     slots, pairs = al.append(ids, w.new_counts)
-    alloc_us = (time.perf_counter() - t0) * 1e6
     tables, lens = al.block_tables(ids, w.max_blocks_per_seq)
-    return al, slots, pairs.reshape(-1, 2), tables, lens, alloc_us
+    return slots, pairs.reshape(-1, 2), tables, lens
+
+
+def allocate(w, pa):
+    """history_allocator, then the step's allocation.  Returns the allocator,
+    the step's slot mapping and copy pairs, block tables, lengths and the
+    step's allocation time in microseconds."""
+    al = history_allocator(w, pa)
+    t0 = time.perf_counter()
+    slots, pairs, tables, lens = step_allocation(al, w)
+    alloc_us = (time.perf_counter() - t0) * 1e6
+    return al, slots, pairs, tables, lens, alloc_us
 
 
 def unique_kv_bytes(w, tables, lens) -> int:
@@ -523,11 +540,21 @@ def run_ours(args):
         graph_ms = max_over_ranks(g0.elapsed_time(g1), dev)
         del g
 
-    # ---- end to end through the public API with pinned host buffers
-    h_tables = torch.from_numpy(tables).pin_memory()
-    h_lens = torch.from_numpy(lens).pin_memory()
-    h_slots = torch.from_numpy(slots).pin_memory()
-    h_pairs = torch.from_numpy(np.ascontiguousarray(pairs)).pin_memory()
+    # ---- end to end through the public API with pinned host buffers.  Every
+    # step starts from its own allocator holding the history (made before the
+    # timed region) and does the step's host allocation inside it: slots and
+    # copy pairs for the new tokens, block tables and lengths, written into
+    # pinned buffers (two sets, reused once their previous copies are done).
+    n_e2e = args.warmup + args.steps
+    fresh = [history_allocator(w, pa) for _ in range(n_e2e)]
+    hbufs = [{"tables": torch.from_numpy(tables).pin_memory(), "lens": torch.from_numpy(lens).pin_memory(),
+              "slots": torch.from_numpy(slots).pin_memory(),
+              "pairs": torch.from_numpy(np.ascontiguousarray(pairs)).pin_memory()} for _ in range(2)]
+    hdone = [torch.cuda.Event() for _ in range(2)]
+    for ev_h in hdone:
+        ev_h.record(stream)
+    e2e_alloc_s = []
+    h_tables, h_lens, h_slots, h_pairs = (hbufs[0][k] for k in ("tables", "lens", "slots", "pairs"))
     h_q = torch.from_numpy(np.ascontiguousarray(q_host)).pin_memory().view(row_dt)
     h_qs = torch.from_numpy(w.query_start).pin_memory() if multi else None
     h_nk = torch.from_numpy(np.ascontiguousarray(nk_host)).pin_memory().view(row_dt)
@@ -556,12 +583,23 @@ def run_ours(args):
             nvb[b].copy_(h_nv, non_blocking=True)
             ev_in[b].record(cps)
 
-    def e2e_step():
-        d_tables.copy_(h_tables, non_blocking=True)
-        d_lens.copy_(h_lens, non_blocking=True)
-        d_slots.copy_(h_slots, non_blocking=True)
+    def e2e_step(i):
+        t_a = time.perf_counter()
+        s_i, p_i, tab_i, len_i = step_allocation(fresh[i], w)
+        e2e_alloc_s.append(time.perf_counter() - t_a)
+        assert len(p_i) == len(pairs)
+        hb = hbufs[i & 1]
+        hdone[i & 1].synchronize()          # this set's copies of two steps ago are done
+        hb["tables"].numpy()[...] = tab_i
+        hb["lens"].numpy()[...] = len_i
+        hb["slots"].numpy()[...] = s_i
+        d_tables.copy_(hb["tables"], non_blocking=True)
+        d_lens.copy_(hb["lens"], non_blocking=True)
+        d_slots.copy_(hb["slots"], non_blocking=True)
         if has_pairs:
-            d_pairs.copy_(h_pairs, non_blocking=True)
+            hb["pairs"].numpy()[...] = p_i
+            d_pairs.copy_(hb["pairs"], non_blocking=True)
+        hdone[i & 1].record(stream)
         if multi:
             d_qs.copy_(h_qs, non_blocking=True)
         copy_in(0)
@@ -580,16 +618,23 @@ def run_ours(args):
                 ev_out[b].record(cps)
         stream.wait_stream(cps)   # the step's last output is on the host
 
-    for _ in range(args.warmup):
-        e2e_step()
+    for i in range(args.warmup):
+        e2e_step(i)
     barrier()
+    e2e_alloc_s.clear()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_host = time.perf_counter()
     e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
+    for i in range(args.steps):
+        e2e_step(args.warmup + i)
     e1.record(stream)
     barrier()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dev)
+    e2e_host_ms = (time.perf_counter() - t_host) * 1e3
+    # the device clock from the step's first command to its last, or the host's
+    # clock around the whole loop if that is longer (host-side allocation that
+    # the device waited for)
+    e2e_ms = max_over_ranks(max(e0.elapsed_time(e1), e2e_host_ms), dev)
+    del fresh
     h2d = h_tables.numel() * 4 + h_lens.numel() * 4 + h_slots.numel() * 8 + (h_pairs.numel() * 8 if has_pairs else 0) \
         + (h_qs.numel() * 4 if multi else 0) + layers * (h_q.numel() * 2 + h_nk.numel() * 2 + h_nv.numel() * 2)
     d2h = layers * out.numel() * 2
@@ -651,7 +696,11 @@ def run_ours(args):
             "peak_source": "MEASURED_PEAKS.json hbm_gbs (of measured)" if peaks else "fallback 6.8 TB/s (of fallback)",
         },
         "e2e": {"value": round(job_tokens_per_s(world, B, args.steps, e2e_ms), 2), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "host_alloc_us_per_step": round(1e6 * statistics.mean(e2e_alloc_s), 1),
+                "includes": "per step: host allocation (slots, copy pairs, block tables) from the history state, "
+                            "host->device copies of tables, lengths, slots and every layer's query and new K/V, "
+                            "the kernels, and every layer's output back to pinned host memory"},
         "graph": None if graph_ms is None else {
             "value": round(job_tokens_per_s(world, B, args.steps, graph_ms), 2), "unit": "tokens/s",
             "ms_per_step": round(graph_ms / args.steps, 4),
@@ -678,6 +727,11 @@ def run_ours(args):
         line["roofline"]["achieved_unique"] = round(ub / (dec_avg_ms / 1e3) / 1e9, 1)
         line["copy_pairs"] = int(len(pairs))
         line["decode_call"] = "pa_decode_shared_prefix" if shared_mode else "pa_decode"
+    if headline and world == 1 and not args.no_records:
+        line["workloads"] = []
+        for n, kd, sh in RECORDS:
+            line["workloads"].append(workload_record(n, kd, sh, pa, torch, dev))
+            torch.cuda.empty_cache()
     if not args.no_cpu_baseline and world == 1 and not w.num_prompts:
         smp = OracleSample(w, tables, lens, target_s=10.0, kv_dtype=kvd)
         rate, secs = smp.rate(layers)
@@ -687,6 +741,136 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
         torch.distributed.destroy_process_group()
+
+
+# ------------------------------------------- the other workloads, per layer
+
+# (workload, cache type, shared-prefix decode): the configurations timed beside
+# the headline, one record each in its JSON line
+RECORDS = (("mha7b", "f16", False), ("mix", "f16", False), ("cow16", "f16", False), ("cow16", "f16", True),
+           ("gqa72b", "fp8", False), ("spec72b", "f16", False), ("spec72b", "fp8", False), ("chunked", "f16", False))
+
+
+def workload_record(name, kvd, shared, pa, torch, dev, calls=20, warmup=3):
+    """One layer of a workload, timed call by call with CUDA events on the
+    launching stream: block copy (copy-on-write pairs, if any), KV write and
+    the attention call, each with its algorithmic bytes (and FLOPs) and the
+    fraction of the measured roof; the SM clock sampled meanwhile.  Inputs
+    are larger than L2, so nothing is flushed between calls."""
+    from paged_kv_cache_12_gb300 import workloads
+    w = workloads.make(name)
+    al, slots, pairs, tables, lens, alloc_us = allocate(w, pa)
+    multi = multi_token(w)
+    kpool, vpool, q1, qm, nk_h, nv_h = inputs(w, kvd)
+    cache_dt = {"f16": torch.float16, "bf16": torch.bfloat16, "fp8": torch.uint8}[kvd]
+    row_dt = torch.bfloat16 if kvd == "bf16" else torch.float16
+    up = lambda a, dt=None: (lambda t: t.view(dt) if dt is not None else t)(
+        torch.from_numpy(np.ascontiguousarray(a)).to(dev))
+    k, v = up(kpool, cache_dt), up(vpool, cache_dt)
+    q = up(qm if multi else q1, row_dt)
+    nk, nv = up(nk_h, row_dt), up(nv_h, row_dt)
+    d_slots, d_pairs, d_tables, d_lens = up(slots), up(pairs), up(tables), up(lens)
+    out = torch.empty_like(q)
+    ks, vs = FP8_SCALES if kvd == "fp8" else (1.0, 1.0)
+    typed = kvd != "f16"
+    st = torch.cuda.current_stream()
+    if multi:
+        d_qs = up(w.query_start)
+        nws = pa.pa_attention_causal_workspace_size(w.num_seqs, w.num_new_tokens, w.num_heads, w.num_kv_heads,
+                                                    w.head_dim, w.max_context_len)
+    elif shared:
+        S = w.samples_per_prompt
+        d_lead = up(np.repeat(np.arange(w.num_prompts) * S, S).astype(np.int32))
+        d_shl = torch.full((w.num_seqs,), w.prompt_len, dtype=torch.int32, device=dev)
+        nws = pa.pa_decode_shared_prefix_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim,
+                                                        w.max_context_len)
+    else:
+        nws = pa.pa_decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, w.max_context_len)
+    ws = torch.zeros(nws, dtype=torch.uint8, device=dev)
+
+    def call():
+        if multi and typed:
+            pa.pa_attention_causal_typed(out, q, k, v, d_tables, d_lens, d_qs, w.scale, w.max_context_len, ws, ks, vs,
+                                         st)
+        elif multi:
+            pa.pa_attention_causal(out, q, k, v, d_tables, d_lens, d_qs, w.scale, w.max_context_len, ws, st)
+        elif typed:
+            pa.pa_decode_typed(out, q, k, v, d_tables, d_lens, w.scale, w.max_context_len, ws, ks, vs, st)
+        elif shared:
+            pa.pa_decode_shared_prefix(out, q, k, v, d_tables, d_lens, d_lead, d_shl, w.scale, w.max_context_len, ws,
+                                       st)
+        else:
+            pa.pa_decode(out, q, k, v, d_tables, d_lens, w.scale, w.max_context_len, ws, st)
+
+    has_pairs = len(pairs) > 0
+    E = lambda: torch.cuda.Event(enable_timing=True)
+
+    def one(evs=None):
+        if evs:
+            evs[0].record(st)
+        if has_pairs:
+            pa.pa_block_copy(k, v, d_pairs, st)
+        if evs:
+            evs[1].record(st)
+        if kvd == "fp8":
+            pa.pa_kv_write_fp8(nk, nv, d_slots, k, v, ks, vs, st)
+        else:
+            pa.pa_kv_write(nk, nv, d_slots, k, v, st)
+        if evs:
+            evs[2].record(st)
+        call()
+        if evs:
+            evs[3].record(st)
+
+    for _ in range(warmup):
+        one()
+    torch.cuda.synchronize()
+    evs = [[E() for _ in range(4)] for _ in range(calls)]
+    with ClockSampler(dev.index or 0) as clk:
+        for e in evs:
+            one(e)
+        torch.cuda.synchronize()
+    assert pa.pa_workspace_status(ws) == pa.PA_OK
+    t_copy = [a[0].elapsed_time(a[1]) for a in evs]
+    t_write = [a[1].elapsed_time(a[2]) for a in evs]
+    t_call = [a[2].elapsed_time(a[3]) for a in evs]
+    esz = elem_bytes(kvd)
+    peaks = measured_peaks()
+    peak = peaks["hbm_gbs"] if peaks else 6800.0
+    tpeak = (peaks.get("bf16_tflops_sustained") or peaks.get("bf16_tflops")) if peaks else 1700.0
+    dbytes = causal_bytes(w, esz) if multi else decode_bytes(w, esz)
+    ms = statistics.mean(t_call)
+    gbs = dbytes / (ms / 1e3) / 1e9
+    call_name = ("pa_attention_causal" + ("_typed" if typed else "") if multi else
+                 "pa_decode_shared_prefix" if shared else "pa_decode_typed" if typed else "pa_decode")
+    rec = {"workload": name, "kv_dtype": kvd, "call": call_name, "num_seqs": w.num_seqs,
+           "ms": {"mean": round(ms, 5), "p10": round(float(np.percentile(t_call, 10)), 5),
+                  "p90": round(float(np.percentile(t_call, 90)), 5)},
+           "algorithmic_bytes": dbytes, "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),
+           "bound": "hbm", "frac": round(gbs / peak, 4)}
+    if multi:
+        flops = causal_flops(w)
+        tf = flops / (ms / 1e3) / 1e12
+        rec.update({"query_tokens": int(w.num_new_tokens), "flops": flops, "achieved_tflops": round(tf, 1),
+                    "tensor_frac": round(tf / tpeak, 4)})
+        if flops / (tpeak * 1e12) > dbytes / (peak * 1e9):
+            rec.update({"bound": "tensor", "frac": round(tf / tpeak, 4)})
+    if w.num_prompts:
+        ub = unique_kv_bytes(w, tables, lens)
+        rec.update({"unique_kv_bytes": ub, "achieved_unique_gbs": round(ub / (ms / 1e3) / 1e9, 1),
+                    "frac": round(ub / (ms / 1e3) / 1e9 / peak, 4), "frac_on": "unique bytes",
+                    "copy_pairs": int(len(pairs))})
+    wb = kv_write_bytes(w, esz)
+    rec["kv_write"] = {"ms": round(statistics.mean(t_write), 5), "algorithmic_bytes": wb,
+                       "achieved_gbs": round(wb / (statistics.mean(t_write) / 1e3) / 1e9, 1)}
+    if has_pairs:
+        cb = 2 * len(pairs) * w.num_kv_heads * w.block_size * w.head_dim * esz * 2
+        rec["block_copy"] = {"ms": round(statistics.mean(t_copy), 5), "algorithmic_bytes": cb,
+                             "achieved_gbs": round(cb / (statistics.mean(t_copy) / 1e3) / 1e9, 1)}
+    rec["host_alloc_us"] = round(alloc_us, 1)
+    rec["clocks"] = clk.summary()
+    w.drop_arrays()
+    return rec
 
 
 # ------------------------------------------------------------ reference arm
@@ -708,16 +892,24 @@ def run_reference(args):
     al.append_batch(ids, [int(x) for x in w.context_lens])
     tables, lens = al.tables(ids, w.max_blocks_per_seq)
     smp = OracleSample(w, tables, lens, target_s=2.0)
-    rates, secs = [], 0.0
+    rates, secs_list = [], []
     for i in range(args.warmup + args.steps):
         rate, secs = smp.rate()
         if i >= args.warmup:
             rates.append(rate)
+            secs_list.append(secs)
     value = statistics.mean(rates)
     line = {
         "impl": "reference",
+        # a step is one timed sample call (what ms_per_step x steps adds up to);
+        # value is the metric of the whole 80-layer, 100-sequence step that the
+        # sample stands for (see "extrapolation")
         "metric": METRIC, "value": round(value, 6), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": round(1e3 * w.num_seqs / value, 3),
+        "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(secs_list), 3),
+        "extrapolation": {"sequences_per_step": smp.n, "of_sequences": w.num_seqs, "layers_per_step": 1,
+                          "of_layers": LAYERS,
+                          "full_step_ms": round(1e3 * w.num_seqs / value, 3),
+                          "rule": "tokens/s = sequences timed / (seconds of the sample x 80 layers)"},
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": f"{WORKLOAD}: GQA 72B-shaped decode, {w.num_seqs} sequences x 8192-token context, "
                                f"64 query / 8 KV heads, head_dim 128, block 16, {LAYERS} layers per step",

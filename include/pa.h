@@ -240,7 +240,7 @@ PA_API size_t pa_attention_causal_workspace_size(int num_seqs, int num_query_tok
  * (T x G) -- a prompt chunk, or a few speculative tokens at a large G -- is
  * computed on the 5th-generation tensor cores in tiles of 128 query rows
  * (128 / G new tokens x the G heads of a kv head), each K/V tile read once
- * per tile (head_dim 128, fp16/bf16 caches, G dividing 128; PA_PREFILL=0 in
+ * per tile (head_dim 128, any cache type, G dividing 128; PA_PREFILL=0 in
  * the environment turns this off).  Other sequences take the decode
  * pipeline, which reduces up to 16 / G new tokens of a sequence together, so
  * a KV tile is read once for that many tokens' query rows.  Device-side cases: a
@@ -335,13 +335,24 @@ PA_API int pa_workspace_status(const void *workspace, int *status_out, void *str
  *    Calls whose work overlaps on the GPU -- on different streams without
  *    ordering between them -- race on the array and give wrong results:
  *    order them, or use pa_decode with a workspace per stream.
- * Results are identical to pa_decode's for the same inputs. */
+ *  - Arguments are checked as pa_decode checks them, and the same status is
+ *    returned; only then is the size checked against the array.
+ * Results are identical, bit for bit, to pa_decode's for the same inputs. */
 PA_API int pa_decode_static_ws(uint16_t *out, const uint16_t *query,
                                const uint16_t *k_cache, const uint16_t *v_cache,
                                const int32_t *block_tables, const int32_t *context_lens,
                                int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                int block_size, int64_t num_blocks, int max_blocks_per_seq,
                                int max_context_len, float scale, void *stream);
+
+/* The error word the last pa_decode_static_ws call on the current device left
+ * in the library's scratch array, for callers that never see that array's
+ * address: PA_OK, or PA_ERR_TIMEOUT if a kernel gave up waiting for its own
+ * copies into shared memory (the affected outputs are NaN).  The pages have no
+ * counterpart (see pa_decode_static_ws).  Synchronises `stream`; call it on the
+ * stream of the decode it asks about.  PA_ERR_CUDA if the array's address
+ * cannot be looked up. */
+PA_API int pa_decode_static_ws_status(int *status_out, void *stream);
 
 /* Failure-detection self-test.  Every wait of the decode kernel's pipeline
  * is bounded: after about a second it records PA_ERR_TIMEOUT in the

@@ -41,7 +41,7 @@ EXPORTS = (
     "pa_alloc_match_prefix", "pa_alloc_append_ids", "pa_alloc_block_hash", "pa_alloc_prefix_stats", "pa_sha256",
     "pa_decode_shared_prefix_workspace_size", "pa_decode_shared_prefix", "pa_selftest_wait_timeout",
     "pa_attention_causal_workspace_size", "pa_attention_causal", "pa_kv_write_fp8", "pa_block_copy_typed",
-    "pa_decode_typed", "pa_attention_causal_typed",
+    "pa_decode_typed", "pa_attention_causal_typed", "pa_decode_static_ws_status",
 )
 
 # cache element types (PA_KV_* in pa.h)
@@ -93,6 +93,7 @@ def lib():
             "pa_alloc_stats": ([vp, ctypes.POINTER(AllocStats)], i32),
             "pa_decode_static_ws": ([vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i64, i32, i32,
                                      ctypes.c_float, vp], i32),
+            "pa_decode_static_ws_status": ([ctypes.POINTER(i32), vp], i32),
             "pa_alloc_free_queue": ([vp, vp, i64, ctypes.POINTER(i64)], i32),
             "pa_alloc_enable_prefix_cache": ([vp], i32),
             "pa_alloc_match_prefix": ([vp, i64, vp, i32, ctypes.c_uint64, ctypes.POINTER(i32)], i32),
@@ -337,6 +338,15 @@ def pa_decode_static_ws(out, query, k_cache, v_cache, block_tables, context_lens
                                      block_tables.data_ptr(), context_lens.data_ptr(), B, hq, hkv, d, bs, nb,
                                      block_tables.shape[1], int(max_context_len), float(scale), _stream(stream)),
            "pa_decode_static_ws")
+
+
+def pa_decode_static_ws_status(stream=None) -> int:
+    """The error word the last pa_decode_static_ws call on the current device
+    left in the library's scratch array (PA_OK or PA_ERR_TIMEOUT); synchronises
+    the stream."""
+    st = ctypes.c_int(0)
+    _check(lib().pa_decode_static_ws_status(ctypes.byref(st), _stream(stream)), "pa_decode_static_ws_status")
+    return st.value
 
 
 def pa_decode_shared_prefix_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len) -> int:

@@ -122,14 +122,14 @@ int validate_slots(const int64_t *slot_mapping, int num_tokens, long long num_sl
     return 0;
 }
 
+// SM count of the current device, asked on every call (a cheap attribute
+// query), so that each device sizes its own grid.  The kernels stride over
+// their work, so the count only sets the grid cap.
 int num_sms() {
-    static int n = 0;
-    if (n == 0) {
-        int dev = 0;
-        if (cudaGetDevice(&dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-            n = 148;
-    }
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || n <= 0)
+        return 148;
     return n;
 }
 

@@ -520,13 +520,16 @@ int launch_kv_any(int kv, int D, int NT, bool causal, const CUtensorMap &tmk, co
 // NaN in the output's 16-bit type, twice.
 uint32_t nan_pair(int kv) { return kv == PA_KV_BF16 ? 0x7fc07fc0u : 0x7e007e00u; }
 
-// One decode call; lead/shared_len are null for pa_decode.
-int decode_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const void *v_cache,
-                const int32_t *block_tables, const int32_t *context_lens, const int32_t *lead,
-                const int32_t *shared_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
-                int64_t num_blocks, int max_blocks_per_seq, int max_context_len, float scale, int kv, float k_scale,
-                float v_scale, void *workspace, size_t workspace_bytes, cudaStream_t st) {
-    const bool grouped = lead != nullptr;
+// What decode_checks returns for a valid call with no work (num_seqs = 0).
+constexpr int NOTHING_TO_DO = 1;
+
+// The host-side checks of a decode call that need neither device data nor the
+// workspace, in the order the calls report them: PA_OK to go on,
+// NOTHING_TO_DO, or the error status.
+int decode_checks(const void *out, const void *query, const void *k_cache, const void *v_cache,
+                  const int32_t *block_tables, const int32_t *context_lens, bool grouped, const int32_t *shared_len,
+                  int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                  int max_blocks_per_seq, int max_context_len, float scale, int kv, float k_scale, float v_scale) {
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0 ||
         max_context_len < 0 || max_blocks_per_seq <= 0 || num_blocks <= 0 || !std::isfinite(scale) || !(scale > 0.f))
         return PA_ERR_INVALID_ARG;
@@ -534,13 +537,28 @@ int decode_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     if ((head_dim != 64 && head_dim != 128) || (block_size != 8 && block_size != 16 && block_size != 32) || G > 16)
         return PA_ERR_UNSUPPORTED;
     if (const int e = check_kv(kv, head_dim, k_scale, v_scale)) return e;
-    if (num_seqs == 0) return PA_OK;
+    if (num_seqs == 0) return NOTHING_TO_DO;
     if (!out || !query || !k_cache || !v_cache || !block_tables || !context_lens || (grouped && !shared_len))
         return PA_ERR_INVALID_ARG;
     if (!aligned16(out) || !aligned16(query) || !aligned16(k_cache) || !aligned16(v_cache))
         return PA_ERR_INVALID_ARG;
+    if ((long long)num_blocks * num_kv_heads * block_size >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
+    return PA_OK;
+}
+
+// One decode call; lead/shared_len are null for pa_decode.
+int decode_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const void *v_cache,
+                const int32_t *block_tables, const int32_t *context_lens, const int32_t *lead,
+                const int32_t *shared_len, int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                int64_t num_blocks, int max_blocks_per_seq, int max_context_len, float scale, int kv, float k_scale,
+                float v_scale, void *workspace, size_t workspace_bytes, cudaStream_t st) {
+    const bool grouped = lead != nullptr;
+    if (const int c = decode_checks(out, query, k_cache, v_cache, block_tables, context_lens, grouped, shared_len,
+                                    num_seqs, num_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                                    max_blocks_per_seq, max_context_len, scale, kv, k_scale, v_scale))
+        return c == NOTHING_TO_DO ? PA_OK : c;
+    const int G = num_heads / num_kv_heads;
     const long long rows = (long long)num_blocks * num_kv_heads * block_size;
-    if (rows >= (1LL << 31)) return PA_ERR_UNSUPPORTED;
     const WsLayout L = ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len, grouped);
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) || workspace_bytes < L.total)
         return PA_ERR_WORKSPACE;
@@ -708,8 +726,8 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     int *grp = reinterpret_cast<int *>(ws + L.grp);
     uint16_t *hout = out;
     // sequences with many new tokens go to the tensor-core prefill kernel
-    // (fp16 / bf16 caches, head_dim 128, G dividing the 128-row tile)
-    const bool pf = prefill_enabled() && head_dim == 128 && kv != PA_KV_FP8_E4M3 && PF_ROWS % G == 0 &&
+    // (head_dim 128, G dividing the 128-row tile; FP8 codes become fp16 tiles on chip)
+    const bool pf = prefill_enabled() && head_dim == 128 && PF_ROWS % G == 0 &&
                     (long long)num_query_tokens * G >= PF_MIN_ROWS;
     int4 *ptiles = reinterpret_cast<int4 *>(ws + L.ptiles);
     causal_prep_kernel<<<1, PREP_THREADS, 0, st>>>(context_lens, query_start, num_seqs, num_query_tokens, num_heads,
@@ -758,7 +776,8 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     pa_.bs = block_size;
     pa_.mbps = max_blocks_per_seq;
     pa_.num_blocks = num_blocks;
-    pa_.scale_log2 = scale * 1.4426950408889634f;
+    pa_.scale_log2 = args.scale_log2;   // with the K scale of an FP8 cache
+    pa_.v_scale = args.v_scale;
     pa_.wait_limit = wait_limit_cycles();
     return launch_prefill(kv, tmk, tmv, pa_, L.ptile_cap * num_kv_heads, st);
 }
@@ -918,12 +937,15 @@ extern "C" int pa_decode_static_ws(uint16_t *out, const uint16_t *query, const u
                                    const int32_t *context_lens, int num_seqs, int num_heads, int num_kv_heads,
                                    int head_dim, int block_size, int64_t num_blocks, int max_blocks_per_seq,
                                    int max_context_len, float scale, void *stream) {
-    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || head_dim <= 0 || max_context_len < 0)
-        return PA_ERR_INVALID_ARG;
+    // pa_decode's own argument checks first, so that both calls report the same status
+    const int c = decode_checks(out, query, k_cache, v_cache, block_tables, context_lens, false, nullptr, num_seqs,
+                                num_heads, num_kv_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
+                                max_context_len, scale, PA_KV_F16, 1.f, 1.f);
+    if (c < 0) return c;
     if (ws_layout(num_seqs, num_heads, num_kv_heads, head_dim, max_context_len, false).total >
         (size_t)PA_DECODE_STATIC_WS_BYTES)
         return PA_ERR_WORKSPACE;
-    if (num_seqs == 0) return PA_OK;
+    if (c == NOTHING_TO_DO) return PA_OK;
     int device = -1;
     if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
     void *ws = static_ws_address(device);
@@ -931,4 +953,13 @@ extern "C" int pa_decode_static_ws(uint16_t *out, const uint16_t *query, const u
     return pa_decode(out, query, k_cache, v_cache, block_tables, context_lens, num_seqs, num_heads, num_kv_heads,
                      head_dim, block_size, num_blocks, max_blocks_per_seq, max_context_len, scale, ws,
                      (size_t)PA_DECODE_STATIC_WS_BYTES, stream);
+}
+
+extern "C" int pa_decode_static_ws_status(int *status_out, void *stream) {
+    if (!status_out) return PA_ERR_INVALID_ARG;
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) return PA_ERR_CUDA;
+    void *ws = static_ws_address(device);
+    if (!ws) return PA_ERR_CUDA;
+    return pa_workspace_status(ws, status_out, stream);
 }

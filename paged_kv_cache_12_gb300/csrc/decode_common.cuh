@@ -354,11 +354,16 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
             const ConsumerSmem cs = consumer_smem<D, NT, KV>(smem, c);
             const int s = sc[c] % DEPTH;
             const uint32_t full = smem_u32(&cs.full[s]);
-            bool ok = mbar_wait_bounded(smem_u32(&cs.empty[s]), ((sc[c] / DEPTH) & 1) ^ 1, a.wait_limit);
+            // every lane waits; the warp goes on only if all of them saw the
+            // phase (a lane alone past a timeout would meet the shuffles and
+            // votes below without the others)
+            bool ok = __all_sync(0xffffffffu,
+                                 mbar_wait_bounded(smem_u32(&cs.empty[s]), ((sc[c] / DEPTH) & 1) ^ 1, a.wait_limit));
             bool first = false;
             if (ok && chunk[c] == nch[c]) {          // the consumer needs its next item
                 const int q = ic[c] & 1;
-                ok = mbar_wait_bounded(smem_u32(&cs.qfree[q]), ((ic[c] >> 1) & 1) ^ 1, a.wait_limit);
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait_bounded(smem_u32(&cs.qfree[q]), ((ic[c] >> 1) & 1) ^ 1, a.wait_limit));
                 if (ok && n_item < 0) {              // nothing left: tell the consumer to stop
                     if (lane == 0) {
                         ItemDesc e;
@@ -628,7 +633,8 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
     for (int item = 0;; ++item) {
         const int q = item & 1;
         int s = stage % DEPTH;
-        if (!mbar_wait_bounded(smem_u32(&cs.full[s]), (stage / DEPTH) & 1, a.wait_limit)) {
+        // warp-uniform outcome: the MMAs and shuffles below need every lane
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&cs.full[s]), (stage / DEPTH) & 1, a.wait_limit))) {
             if (lane == 0) atomicExch(&a.hdr->error, PA_ERR_TIMEOUT);
             return;   // the producer drains the copies in flight before the CTA ends
         }
@@ -701,7 +707,8 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
         for (int ch = 0; ch < nchunks; ++ch) {
             if (ch > 0) {
                 s = stage % DEPTH;
-                if (!mbar_wait_bounded(smem_u32(&cs.full[s]), (stage / DEPTH) & 1, a.wait_limit)) {
+                if (!__all_sync(0xffffffffu,
+                                mbar_wait_bounded(smem_u32(&cs.full[s]), (stage / DEPTH) & 1, a.wait_limit))) {
                     if (lane == 0) atomicExch(&a.hdr->error, PA_ERR_TIMEOUT);
                     return;   // the producer drains the copies in flight before the CTA ends
                 }

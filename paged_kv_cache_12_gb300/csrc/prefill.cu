@@ -32,7 +32,12 @@
 // and with two stages that latency, not the tensor or exponential work, set
 // the time per KV tile.
 // S for the next KV tile is computed while the softmax works on this one.
-// Every wait is bounded; tensor memory is released on every path.
+// FP8 E4M3 caches: the producer warps stage the one-byte codes by TMA and turn
+// them into exact fp16 tiles of the same layout (two stages), the K scale
+// folded into the softmax scale and the V scale into the output.
+// Every wait is bounded and every warp-collective instruction (tensor-memory
+// loads and stores, votes) runs in warp-uniform control flow; tensor memory
+// is released on every path.
 
 #include <cmath>
 #include <mutex>
@@ -53,16 +58,36 @@ constexpr int PM = 128;                    // query rows per work tile
 #endif
 constexpr int PN = PA_PF_PN;               // KV tokens per tile (64 or 128)
 constexpr int PD = 128;                    // head dim
-constexpr int PST = PA_PF_STAGES;          // K and V ring stages
-constexpr int KV_BYTES = PN * PD * 2;      // 2 blocks (64 dims) x PN tokens x 128 B
-constexpr int OFF_K = 0;
-constexpr int OFF_V = OFF_K + PST * KV_BYTES;
-constexpr int OFF_CTRL = OFF_V + PST * KV_BYTES;
-constexpr int CTRL_BYTES = 256;
-constexpr int CTRL_BAD = 224;              // int: 1 + the work item that met an out-of-range block id
-constexpr int CTRL_ABORT = 228;            // int: a role gave up waiting
-constexpr int PF_SMEM = OFF_CTRL + CTRL_BYTES + 1024;   // + alignment slack
+constexpr int PST = PA_PF_STAGES;          // K and V ring stages of a 16-bit cache
+constexpr int KV_BYTES = PN * PD * 2;      // a 16-bit K or V tile: 2 blocks (64 dims) x PN tokens x 128 B
+constexpr int F8_BYTES = PN * PD;          // an FP8 tile: PN tokens x 128 B
+constexpr int MAXST = 3;                   // barrier slots per ring
+constexpr int CTRL_BYTES = 512;
+constexpr int BAD_SLOTS = 16;              // out-of-range marks, one per work item of this CTA modulo 16
+constexpr int CTRL_BAD = 416;              // int[BAD_SLOTS]: 1 + the CTA-local index of an item that met an
+                                           // out-of-range block id (producers run at most a few KV tiles,
+                                           // hence items, ahead of the softmax that reads the mark)
+constexpr int CTRL_ABORT = CTRL_BAD + 4 * BAD_SLOTS;   // int: a role gave up waiting
 constexpr int PF_THREADS = 7 * 32;         // K producer, V producer, MMA, 4 softmax warps
+
+// Shared memory per cache type: the K and V rings the MMAs read (16-bit
+// tiles; R stages each) and, for an FP8 cache, the rings its codes are staged
+// in by TMA (S8 stages each) before the producer warps turn them into fp16
+// tiles of the same layout.
+template <int KV>
+struct PfL {
+    static constexpr bool F8 = KV == PA_KV_FP8_E4M3;
+    static constexpr int R = F8 ? 2 : PST;
+    static constexpr int S8 = F8 ? 3 : 0;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = R * KV_BYTES;
+    static constexpr int OFF_K8 = 2 * R * KV_BYTES;
+    static constexpr int OFF_V8 = OFF_K8 + S8 * F8_BYTES;
+    static constexpr int OFF_CTRL = OFF_V8 + S8 * F8_BYTES;
+    static constexpr int SMEM = OFF_CTRL + CTRL_BYTES + 1024;   // + alignment slack
+    static_assert(R <= MAXST && S8 <= MAXST, "ring stages");
+    static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
+};
 // tensor memory: S0 [0, PN), S1 [PN, 2 PN), O (128 fp32 columns), Q (128 dims,
 // two fp16/bf16 per column), P (PN tokens, two per column)
 constexpr int TMEM_COLS = 512;
@@ -71,24 +96,27 @@ constexpr int TM_Q = TM_O + PD;
 constexpr int TM_P = TM_Q + PD / 2;
 static_assert(TM_P + PN / 2 <= TMEM_COLS, "tensor-memory columns");
 static_assert(PN == 64 || PN == 128, "KV tile of 64 or 128 tokens");
-static_assert(OFF_CTRL + CTRL_BYTES + 1024 <= 227 * 1024, "shared memory of one CTA");
-static_assert(8 * (4 * PST + 11) + 8 <= CTRL_BAD && CTRL_ABORT + 4 <= CTRL_BYTES, "control block layout");
+static_assert(8 * (6 * MAXST + 11) + 8 <= CTRL_BAD && CTRL_ABORT + 4 <= CTRL_BYTES, "control block layout");
 
 struct PfBars {
     // pfull / pvdone: one per PV-number parity, so that a softmax warp a step
     // ahead of another never adds its arrival to the other step's phase
-    uint32_t kfull[PST], kempty[PST], vfull[PST], vempty[PST], sfull[2], sfree[2], pfull[2], pvdone[2], qfull;
+    // k8full / v8full: FP8 codes staged (TMA bytes landed)
+    uint32_t kfull[MAXST], kempty[MAXST], vfull[MAXST], vempty[MAXST], k8full[MAXST], v8full[MAXST];
+    uint32_t sfull[2], sfree[2], pfull[2], pvdone[2], qfull;
     uint32_t tmem_slot, flags;   // shared addresses
 };
 
-__device__ __forceinline__ PfBars pf_bars(uint8_t *smem) {
-    const uint32_t c = smem_u32(smem + OFF_CTRL);
+__device__ __forceinline__ PfBars pf_bars(uint8_t *smem, int off_ctrl) {
+    const uint32_t c = smem_u32(smem + off_ctrl);
     PfBars b;
     uint32_t a = c;
-    for (int s = 0; s < PST; ++s) b.kfull[s] = a, a += 8;
-    for (int s = 0; s < PST; ++s) b.kempty[s] = a, a += 8;
-    for (int s = 0; s < PST; ++s) b.vfull[s] = a, a += 8;
-    for (int s = 0; s < PST; ++s) b.vempty[s] = a, a += 8;
+    for (int s = 0; s < MAXST; ++s) b.kfull[s] = a, a += 8;
+    for (int s = 0; s < MAXST; ++s) b.kempty[s] = a, a += 8;
+    for (int s = 0; s < MAXST; ++s) b.vfull[s] = a, a += 8;
+    for (int s = 0; s < MAXST; ++s) b.vempty[s] = a, a += 8;
+    for (int s = 0; s < MAXST; ++s) b.k8full[s] = a, a += 8;
+    for (int s = 0; s < MAXST; ++s) b.v8full[s] = a, a += 8;
     b.sfull[0] = a, a += 8;
     b.sfull[1] = a, a += 8;
     b.sfree[0] = a, a += 8;
@@ -99,7 +127,7 @@ __device__ __forceinline__ PfBars pf_bars(uint8_t *smem) {
     b.pvdone[1] = a, a += 8;
     b.qfull = a, a += 8;
     b.tmem_slot = a, a += 8;
-    b.flags = a;   // barriers and slots end at byte 8 (4 PST + 11) + 8 = 216 <= CTRL_BAD
+    b.flags = a;   // barriers and slots end at byte 8 (6 MAXST + 11) + 8 = 240 <= CTRL_BAD
     return b;
 }
 
@@ -126,14 +154,24 @@ __device__ __forceinline__ PfTile pf_tile(const PrefillArgs &a, int item) {
 
 __device__ __forceinline__ void pf_error(const PrefillArgs &a) { atomicExch(&a.hdr->error, PA_ERR_TIMEOUT); }
 
+// The CTA-local index of a work item (items are dealt round-robin) and its
+// out-of-range mark in the control block.
+__device__ __forceinline__ int pf_local(int item) { return (item - (int)blockIdx.x) / (int)gridDim.x; }
+__device__ __forceinline__ volatile int *pf_bad_slot(uint8_t *smem, int off_ctrl, int local) {
+    return reinterpret_cast<volatile int *>(smem + off_ctrl + CTRL_BAD) + (local % BAD_SLOTS);
+}
+
 // ----------------------------------------------------------- producer
 
+template <int KV>
 __device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const PrefillArgs &a, const PfBars &bb,
                             volatile int *abort_flag, int total, int kv) {
+    using L = PfL<KV>;
+    constexpr int PST = L::R;
     const int lane = threadIdx.x & 31;
     const uint64_t pol = policy_evict_normal();
     const int box_rows = a.bs < 16 ? a.bs : 16;    // rows per TMA box: one box per block or 16-row group
-    const uint32_t base = smem_u32(smem) + (kv ? OFF_V : OFF_K);
+    const uint32_t base = smem_u32(smem) + (kv ? L::OFF_V : L::OFF_K);
     const uint32_t *full = kv ? bb.vfull : bb.kfull;
     const uint32_t *empty = kv ? bb.vempty : bb.kempty;
     int cnt = 0;
@@ -164,7 +202,7 @@ __device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const Prefill
             const unsigned boxes = __ballot_sync(0xffffffffu, mine);
             const bool bad = __any_sync(0xffffffffu, mine && (blk < 0 || blk >= a.num_blocks));
             if (lane == 0) {
-                if (bad) *reinterpret_cast<volatile int *>(smem + OFF_CTRL + CTRL_BAD) = item + 1;
+                if (bad) *pf_bad_slot(smem, L::OFF_CTRL, pf_local(item)) = pf_local(item) + 1;
                 mbar_arrive_expect_tx(full[s], bad ? 0u : (uint32_t)(__popc(boxes) * 2 * box_rows * 128));
             }
             __syncwarp();
@@ -181,10 +219,118 @@ __device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const Prefill
     drain();
 }
 
+// FP8 cache: the same work, through a staging ring.  The warp issues the TMA
+// copies of the codes of up to S8 KV tiles ahead (one 128-byte box column per
+// block); behind them it turns each staged tile into the 16-bit tile the MMAs
+// read, in the same swizzled layout a 16-bit TMA copy would have written:
+// code chunk j (dims 16 j .. 16 j + 15) of row r becomes fp16 chunks 2 (j % 4)
+// and 2 (j % 4) + 1 of the 64-dim block j / 4.  Every E4M3 value is an fp16
+// value, so the tile is exact; the scales are applied to the scores and the
+// output.  A staging slot is refilled only after this warp converted it.
+__device__ void pf_producer_fp8(uint8_t *smem, const CUtensorMap *map, const PrefillArgs &a, const PfBars &bb,
+                                volatile int *abort_flag, int total, int kv) {
+    using L = PfL<PA_KV_FP8_E4M3>;
+    constexpr int R = L::R, S8 = L::S8;
+    const int lane = threadIdx.x & 31;
+    const uint64_t pol = policy_evict_normal();
+    const int box_rows = a.bs < 16 ? a.bs : 16;
+    const uint32_t stage = smem_u32(smem) + (kv ? L::OFF_V8 : L::OFF_K8);
+    const uint8_t *stage_p = smem + (kv ? L::OFF_V8 : L::OFF_K8);
+    uint8_t *ring = smem + (kv ? L::OFF_V : L::OFF_K);
+    const uint32_t *full8 = kv ? bb.v8full : bb.k8full;
+    const uint32_t *full = kv ? bb.vfull : bb.kfull;
+    const uint32_t *empty = kv ? bb.vempty : bb.kempty;
+    // issue and conversion walk the same sequence of (work item, KV tile)
+    struct Walk {
+        int item, n;
+        PfTile t;
+    };
+    auto start = [&](Walk &w) {
+        w.item = blockIdx.x;
+        w.n = 0;
+        if (w.item < total) w.t = pf_tile(a, w.item);
+    };
+    auto step = [&](Walk &w) {
+        if (++w.n < w.t.nkv) return;
+        w.n = 0;
+        w.item += gridDim.x;
+        if (w.item < total) w.t = pf_tile(a, w.item);
+    };
+    Walk wi, wc;
+    start(wi);
+    start(wc);
+    int issued = 0, conv = 0;
+    bool ok = true;
+    auto fail = [&]() {
+        if (lane == 0) pf_error(a);
+        *abort_flag = 1;
+        ok = false;
+    };
+    auto issue = [&]() {
+        const int s8 = issued % S8;
+        const int t0 = wi.n * PN;
+        const int tok = t0 + lane * box_rows;
+        const bool mine = lane < PN / box_rows && tok < wi.t.L;
+        const int32_t blk = mine ? __ldg(a.block_tables + (long long)wi.t.seq * a.mbps + tok / a.bs) : 0;
+        const unsigned boxes = __ballot_sync(0xffffffffu, mine);
+        const bool bad = __any_sync(0xffffffffu, mine && (blk < 0 || blk >= a.num_blocks));
+        if (lane == 0) {
+            if (bad) *pf_bad_slot(smem, L::OFF_CTRL, pf_local(wi.item)) = pf_local(wi.item) + 1;
+            mbar_arrive_expect_tx(full8[s8], bad ? 0u : (uint32_t)(__popc(boxes) * box_rows * 128));
+        }
+        __syncwarp();
+        if (!bad && mine) {
+            const int y = (int)(((long long)blk * a.Hkv + wi.t.kvh) * a.bs) + tok % a.bs;
+            tma_load_2d(stage + s8 * F8_BYTES + lane * box_rows * 128, map, 0, y, full8[s8], pol);
+        }
+        __syncwarp();
+        ++issued;
+        step(wi);
+    };
+    auto convert = [&]() {
+        const int s8 = conv % S8, c = conv % R;
+        const bool got = !*abort_flag && mbar_wait_bounded(full8[s8], (uint32_t)((conv / S8) & 1), a.wait_limit) &&
+                         mbar_wait_bounded(empty[c], (uint32_t)(((conv / R) & 1) ^ 1), a.wait_limit);
+        if (!__all_sync(0xffffffffu, got)) return fail();
+        const uint8_t *src = stage_p + s8 * F8_BYTES;
+        uint8_t *dst = ring + c * KV_BYTES;
+#pragma unroll 4
+        for (int i = 0; i < PN / 4; ++i) {   // 4 rows x 8 code chunks per pass
+            const int r = 4 * i + (lane >> 3), j = lane & 7;
+            const uint4 x = *reinterpret_cast<const uint4 *>(src + r * 128 + ((j ^ (r & 7)) << 4));
+            const uint4 lo = make_uint4(e4m3x2_lo_to_f16x2(x.x), e4m3x2_hi_to_f16x2(x.x), e4m3x2_lo_to_f16x2(x.y),
+                                        e4m3x2_hi_to_f16x2(x.y));
+            const uint4 hi = make_uint4(e4m3x2_lo_to_f16x2(x.z), e4m3x2_hi_to_f16x2(x.z), e4m3x2_lo_to_f16x2(x.w),
+                                        e4m3x2_hi_to_f16x2(x.w));
+            uint8_t *row = dst + (j >> 2) * (PN * 128) + r * 128;
+            const int c0 = 2 * (j & 3);
+            *reinterpret_cast<uint4 *>(row + ((c0 ^ (r & 7)) << 4)) = lo;
+            *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (r & 7)) << 4)) = hi;
+        }
+        // the tile, written through the generic proxy, is for the tensor cores;
+        // the staged codes have been read before their slot is refilled
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full[c]);
+        ++conv;
+        step(wc);
+    };
+    while (ok && wc.item < total) {
+        while (wi.item < total && issued < conv + S8) issue();
+        convert();
+    }
+    // staged copies not converted (only after a failure) land before the warp leaves
+    for (int k = conv; k < issued; ++k) mbar_wait_bounded(full8[k % S8], (uint32_t)((k / S8) & 1), WAIT_LIMIT);
+}
+
 // ----------------------------------------------------------- MMA issuer
 
+template <int KV>
 __device__ void pf_mma(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, uint32_t tmem, bool bf16,
                        volatile int *abort_flag, int total) {
+    using L = PfL<KV>;
+    constexpr int PST = L::R;
+    constexpr int OFF_K = L::OFF_K, OFF_V = L::OFF_V;
     const uint32_t base = smem_u32(smem);
     const uint32_t id_s = idesc_f16(PM, PN, bf16, false);
     const uint32_t id_o = idesc_f16(PM, PD, bf16, true);
@@ -255,6 +401,9 @@ __device__ void pf_mma(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, ui
 template <int KV>
 __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, uint32_t tmem,
                            volatile int *abort_flag, int total) {
+    using L = PfL<KV>;
+    constexpr int PST = L::R;
+    constexpr int OFF_V = L::OFF_V, OFF_CTRL = L::OFF_CTRL;
     const int tid = threadIdx.x - 96;             // 0 .. 127
     const int lane = threadIdx.x & 31;
     const int quarter = (threadIdx.x >> 5) & 3;    // tensor-memory lanes 32 quarter .. + 31
@@ -337,9 +486,17 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
             for (int c = 8; c < PN; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
             const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                                    fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl2;
-            if (mx > mrun + RESCALE_THRESHOLD) {
-                const float nm = fmaxf(mrun, mx);
-                const float alpha = fast_exp2(mrun - nm);
+            // Whether to rescale is decided per row, but the tensor-memory round
+            // trip of O and the wait before it are warp-collective: when any
+            // row of the warp grows, every lane takes the branch, and a lane
+            // whose own row does not grow scales by exactly 1 (its bits stay).
+            // A branch taken by part of a warp would run tcgen05.ld/st and the
+            // vote of the bounded wait in divergent code, which can hang the
+            // warp outside any bounded wait.
+            const bool grow = mx > mrun + RESCALE_THRESHOLD;
+            if (__any_sync(0xffffffffu, grow)) {
+                const float nm = grow ? fmaxf(mrun, mx) : mrun;
+                const float alpha = grow ? fast_exp2(mrun - nm) : 1.f;
                 if (n > 0) {   // O holds PV up to number g - 1: rescale it in tensor memory
                     if (!wait(bb.pvdone[(g - 1) & 1], ((g - 1) >> 1) & 1)) break;
                     tc_fence_after_sync();
@@ -416,8 +573,8 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
         // ---- epilogue: O / l once the tile's last PV (number g - 1) is done
         if (!wait(bb.pvdone[(g - 1) & 1], ((g - 1) >> 1) & 1)) break;
         tc_fence_after_sync();
-        const bool bad = *reinterpret_cast<volatile int *>(smem + OFF_CTRL + CTRL_BAD) == item + 1;
-        const float inv = bad ? __int_as_float(0x7fc00000) : 1.f / l;
+        const bool bad = *pf_bad_slot(smem, OFF_CTRL, pf_local(item)) == pf_local(item) + 1;
+        const float inv = bad ? __int_as_float(0x7fc00000) : a.v_scale / l;
         uint16_t *orow = a.out + qrow;
 #pragma unroll 1
         for (int c4 = 0; c4 < PD / 32; ++c4) {
@@ -450,16 +607,21 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
                                                                  const PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const PfBars bb = pf_bars(smem);
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + OFF_CTRL + CTRL_ABORT);
+    using L = PfL<KV>;
+    const PfBars bb = pf_bars(smem, L::OFF_CTRL);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_CTRL + CTRL_ABORT);
     const int warp = threadIdx.x >> 5;
     const int total = *reinterpret_cast<volatile int *>(&a.hdr->pf_items);   // written by the prep kernel
     if (threadIdx.x == 0) {
-        for (int s = 0; s < PST; ++s) {
+        for (int s = 0; s < L::R; ++s) {
             mbar_init(bb.kfull[s], 1);
             mbar_init(bb.kempty[s], 1);
             mbar_init(bb.vfull[s], 1);
             mbar_init(bb.vempty[s], 1);
+        }
+        for (int s = 0; s < L::S8; ++s) {
+            mbar_init(bb.k8full[s], 1);
+            mbar_init(bb.v8full[s], 1);
         }
         mbar_init(bb.sfull[0], 1);
         mbar_init(bb.sfull[1], 1);
@@ -471,7 +633,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         mbar_init(bb.pvdone[1], 1);
         mbar_init(bb.qfull, 128);
         mbar_init(bb.flags, 1);            // all MMAs completed (before tensor memory is freed)
-        *reinterpret_cast<volatile int *>(smem + OFF_CTRL + CTRL_BAD) = 0;
+        for (int k = 0; k < BAD_SLOTS; ++k) *pf_bad_slot(smem, L::OFF_CTRL, k) = 0;
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -484,10 +646,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
     tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + (bb.tmem_slot - smem_u32(smem)));
     if (warp < 2) {
-        pf_producer(smem, warp ? &tmv : &tmk, a, bb, abort_flag, total, warp);
+        if constexpr (L::F8)
+            pf_producer_fp8(smem, warp ? &tmv : &tmk, a, bb, abort_flag, total, warp);
+        else
+            pf_producer<KV>(smem, warp ? &tmv : &tmk, a, bb, abort_flag, total, warp);
     } else if (warp == 2) {
         if ((threadIdx.x & 31) == 0) {
-            pf_mma(smem, a, bb, tmem, KV == PA_KV_BF16, abort_flag, total);
+            pf_mma<KV>(smem, a, bb, tmem, KV == PA_KV_BF16, abort_flag, total);
             // every MMA issued has completed before tensor memory is released
             umma_commit(bb.flags);
             mbar_wait_bounded(bb.flags, 0, WAIT_LIMIT);
@@ -511,7 +676,8 @@ int launch_prefill_kv(const CUtensorMap &tmk, const CUtensorMap &tmv, const Pref
     static cudaError_t init_err = cudaSuccess;
     static std::once_flag once;
     std::call_once(once, [] {   // one CTA per SM
-        init_err = cudaFuncSetAttribute(prefill_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, PF_SMEM);
+        init_err =
+            cudaFuncSetAttribute(prefill_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfL<KV>::SMEM);
         int dev = 0, sms = 0;
         if (init_err == cudaSuccess) init_err = cudaGetDevice(&dev);
         if (init_err == cudaSuccess) init_err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -519,7 +685,7 @@ int launch_prefill_kv(const CUtensorMap &tmk, const CUtensorMap &tmv, const Pref
     });
     if (init_err != cudaSuccess || grid <= 0) return PA_ERR_CUDA;
     const int g = (int)(max_items < grid ? (max_items > 0 ? max_items : 1) : grid);
-    prefill_kernel<KV><<<g, PF_THREADS, PF_SMEM, st>>>(tmk, tmv, args);
+    prefill_kernel<KV><<<g, PF_THREADS, PfL<KV>::SMEM, st>>>(tmk, tmv, args);
     return cuda_status(cudaGetLastError());
 }
 
@@ -529,6 +695,7 @@ int launch_prefill(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const
                    long long max_items, cudaStream_t st) {
     if (kv == PA_KV_BF16) return launch_prefill_kv<PA_KV_BF16>(tmk, tmv, args, max_items, st);
     if (kv == PA_KV_F16) return launch_prefill_kv<PA_KV_F16>(tmk, tmv, args, max_items, st);
+    if (kv == PA_KV_FP8_E4M3) return launch_prefill_kv<PA_KV_FP8_E4M3>(tmk, tmv, args, max_items, st);
     return PA_ERR_UNSUPPORTED;
 }
 

@@ -19,7 +19,8 @@ struct PrefillArgs {
     WsHeader *hdr;                    // error word; pf_items = work items (tiles x Hkv)
     int Hq, Hkv, G, bs, mbps;
     long long num_blocks;
-    float scale_log2;
+    float scale_log2;                 // softmax scale (times the K scale of an FP8 cache) x log2(e)
+    float v_scale;                    // V scale of an FP8 cache (1 otherwise)
     long long wait_limit;
 };
 
@@ -31,7 +32,7 @@ struct PrefillArgs {
 constexpr int PF_ROWS = 128;
 constexpr int PF_MIN_ROWS = PA_PF_MIN_ROWS;
 
-// Launch the prefill kernel on `st` (fp16 or bf16 caches, head_dim 128);
+// Launch the prefill kernel on `st` (fp16, bf16 or FP8 E4M3 caches, head_dim 128);
 // it reads its item count from the workspace header; max_items is a host
 // bound that trims the grid.  tmk / tmv: the caches' tensor maps.
 int launch_prefill(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,

@@ -77,6 +77,19 @@ def test_host_checks_fail_before_any_launch():
     assert L.pa_block_copy(nul, nul, nul, 0, 8, 128, 16, 10, nul) == pa.PA_OK
     assert L.pa_decode(nul, nul, nul, nul, nul, nul, 0, 8, 1, 128, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_OK
     assert L.pa_decode(nul, nul, nul, nul, nul, nul, 1, 8, 1, 128, 16, 10, 1, 16, -0.1, nul, 0, nul) == pa.PA_ERR_INVALID_ARG
+    # the variant without a workspace checks its arguments as pa_decode does
+    # and only then its scratch size (fake aligned addresses: never read)
+    S = L.pa_decode_static_ws
+    fake = ctypes.c_void_p(1 << 20)
+    assert S(nul, nul, nul, nul, nul, nul, 1, 8, 1, 96, 16, 10, 1, 16, 0.1, nul) == pa.PA_ERR_UNSUPPORTED
+    assert S(nul, nul, nul, nul, nul, nul, 1, 32, 1, 128, 16, 10, 1, 16, 0.1, nul) == pa.PA_ERR_UNSUPPORTED
+    assert S(nul, nul, nul, nul, nul, nul, 1, 6, 4, 128, 16, 10, 1, 16, 0.1, nul) == pa.PA_ERR_INVALID_ARG
+    assert S(nul, nul, nul, nul, nul, nul, 1, 8, 1, 128, 16, 0, 1, 16, 0.1, nul) == pa.PA_ERR_INVALID_ARG
+    assert S(nul, nul, nul, nul, nul, nul, 1, 8, 1, 128, 16, 10, 1, 16, float("nan"), nul) == pa.PA_ERR_INVALID_ARG
+    assert S(nul, nul, nul, nul, nul, nul, 1, 8, 1, 128, 16, 10, 1, 16, 0.1, nul) == pa.PA_ERR_INVALID_ARG
+    assert S(nul, nul, nul, nul, nul, nul, 0, 8, 1, 128, 16, 10, 1, 16, 0.1, nul) == pa.PA_OK
+    assert S(fake, fake, fake, fake, fake, fake, 4096, 64, 8, 128, 16, 10, 1, 32768, 0.1, nul) == pa.PA_ERR_WORKSPACE
+    assert L.pa_decode_static_ws_status(nul, nul) == pa.PA_ERR_INVALID_ARG
     # the multi-token form: same shape rules; no query rows launches nothing; rows need sequences
     C = L.pa_attention_causal
     assert C(nul, nul, nul, nul, nul, nul, nul, 1, 4, 8, 1, 96, 16, 10, 1, 16, 0.1, nul, 0, nul) == pa.PA_ERR_UNSUPPORTED

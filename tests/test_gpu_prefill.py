@@ -2,7 +2,8 @@
 page section 2.5): a sequence whose new tokens x G reach 32 query rows is
 computed in 128-row tiles with tcgen05 MMAs.  Results must be the oracle's
 causal attention within the decode tolerance, for every G that divides the
-tile, every block size, fp16 and bf16 caches, chunks after long histories
+tile, every block size, fp16, bf16 and FP8 E4M3 caches (FP8 codes are turned
+into exact fp16 tiles on chip), chunks after long histories
 (many KV tiles, running-maximum rescales), whole prompts, partial row tiles and
 contexts that end inside a KV tile (the V rows past them are poisoned NaN)."""
 import os
@@ -15,7 +16,7 @@ import pytest
 import oracle
 import paged_kv_cache_12_gb300 as pa
 from paged_kv_cache_12_gb300 import workloads
-from test_gpu_kv_dtypes import TypedStep, compare, as_f64
+from test_gpu_kv_dtypes import KS, TypedStep, compare, as_f64, to_bf16_bits
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -26,10 +27,34 @@ if not torch.cuda.is_available():  # pragma: no cover
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def run_case(H, Hkv, bs, kv, lens, T, seed):
+def encode(x, kv):
+    """fp64 values -> cache elements of type kv (fp8: the oracle's quantiser)."""
+    if kv == pa.PA_KV_FP8_E4M3:
+        return oracle.fp8_quantise(np.asarray(x, dtype=np.float64), KS)
+    if kv == pa.PA_KV_BF16:
+        return to_bf16_bits(x)
+    return np.asarray(x, dtype=np.float16).view(np.uint16)
+
+
+def plant_keys(st, plants):
+    """Overwrite history keys: plants = [(seq, position, new token j, query head
+    h, factor)] makes K at `position` of `seq` (kv head h // G) `factor` times
+    the query row of new token j, head h, so that row's score there stands far
+    above every other it sees."""
+    w = st.w
+    G = w.num_heads // w.num_kv_heads
+    for seq, pos, j, h, f in plants:
+        q = st.qm[w.query_start[seq] + j, h]
+        qv = (q.astype(np.uint32) << 16).view(np.float32) if st.kv == pa.PA_KV_BF16 else q
+        blk = st.tables[seq][pos // w.block_size]
+        st.k0[blk, h // G, pos % w.block_size] = encode(f * np.asarray(qv, dtype=np.float64), st.kv)
+
+
+def run_case(H, Hkv, bs, kv, lens, T, seed, plants=()):
     w = workloads.custom(seed=seed, num_seqs=len(lens), num_heads=H, num_kv_heads=Hkv, head_dim=128, block_size=bs,
                          context_lens=lens, new_tokens=T, multi=True)
     st = TypedStep(w, kv)
+    plant_keys(st, plants)
     st.run_gpu()
     kc, vc = st.oracle_caches()
     out = st.causal()
@@ -38,7 +63,7 @@ def run_case(H, Hkv, bs, kv, lens, T, seed):
     return w, st, out, ref
 
 
-@pytest.mark.parametrize("kv", [pa.PA_KV_F16, pa.PA_KV_BF16])
+@pytest.mark.parametrize("kv", [pa.PA_KV_F16, pa.PA_KV_BF16, pa.PA_KV_FP8_E4M3])
 @pytest.mark.parametrize("H,Hkv", [(8, 8), (16, 8), (32, 8), (64, 8), (16, 1)])
 @pytest.mark.parametrize("bs", [8, 16, 32])
 def test_prompt_chunks_against_oracle(kv, H, Hkv, bs):
@@ -55,9 +80,54 @@ def test_prompt_chunks_against_oracle(kv, H, Hkv, bs):
 
 def test_long_history_many_kv_tiles():
     # 16k positions before a 256-token chunk: 130 KV tiles of 128 tokens per
-    # row tile, scores drawn large enough that the running maximum moves often
+    # row tile (the running maximum grows a little, below the 2^8 rescale
+    # threshold; test_running_maximum_grows_for_some_rows_of_a_warp crosses it)
     w, st, out, ref = run_case(32, 8, 16, pa.PA_KV_F16, [16384 + 256], [256], seed=5)
     compare(as_f64(out, pa.PA_KV_F16), ref, pa.PA_KV_F16)
+
+
+@pytest.mark.parametrize("kv", [pa.PA_KV_F16, pa.PA_KV_BF16, pa.PA_KV_FP8_E4M3])
+def test_running_maximum_grows_for_some_rows_of_a_warp(kv):
+    # Keys planted in later KV tiles (positions 300, 1000, 1700, 2500) make the
+    # running maximum of single query rows jump by far more than 2^8 after the
+    # first tile, while the other rows of the same 32-row warp keep theirs:
+    # the rescale of O in tensor memory must run for the whole warp, with
+    # unchanged rows scaled by exactly 1.  With N(0, 1) data alone the maximum
+    # never moves that far after the first tile.
+    H, Hkv, bs = 32, 8, 16
+    lens, T = [3000, 2600], [256, 40]
+    plants = [(0, 300, 3, 1, 2.0), (0, 1000, 40, 6, 2.0), (0, 1700, 100, 9, 2.0), (1, 2500, 7, 30, 2.0),
+              (1, 1000, 20, 5, 2.0)]
+    w, st, out, ref = run_case(H, Hkv, bs, kv, lens, T, seed=41 + kv, plants=plants)
+    compare(as_f64(out, kv), ref, kv)
+    again = st.causal()
+    assert torch.equal(out.view(torch.int16), again.view(torch.int16))
+
+
+@pytest.mark.parametrize("kv", [pa.PA_KV_F16, pa.PA_KV_FP8_E4M3])
+def test_several_items_per_cta_with_out_of_range_ids(kv):
+    # 48 sequences x 4 new tokens at G = 8: 384 work items, so every CTA of the
+    # persistent grid runs two or three, one behind the other; the producers
+    # read ahead into the next item.  Three of every four sequences meet an
+    # out-of-range block id: their rows are NaN, every other row is the oracle's.
+    H, Hkv, bs = 64, 8, 16
+    lens = [600 + 37 * i for i in range(48)]
+    T = [4] * 48
+    w, st, out, ref = run_case(H, Hkv, bs, kv, lens, T, seed=57 + kv)
+    compare(as_f64(out, kv), ref, kv)
+    bad = st.d["tables"].clone()
+    for i in range(48):
+        if i % 4 != 3:
+            bad[i, (lens[i] // bs) // 2] = w.num_blocks + i
+    st.d["tables"] = bad
+    out2 = st.causal().cpu().numpy()
+    qs = w.query_start
+    for i in range(48):
+        rows = out2[qs[i]:qs[i + 1]]
+        if i % 4 != 3:
+            assert np.isnan(rows).all(), f"sequence {i}"
+        else:
+            compare(rows.astype(np.float64), ref[qs[i]:qs[i + 1]], kv)
 
 
 def test_deterministic_and_equal_to_the_decode_pipeline(tmp_path):
@@ -84,7 +154,7 @@ assert np.max(np.abs(tc - out.cpu().numpy().astype(np.float64))) <= 2e-3
     assert r.returncode == 0, r.stdout + r.stderr
 
 
-@pytest.mark.parametrize("kv", [pa.PA_KV_F16, pa.PA_KV_BF16])
+@pytest.mark.parametrize("kv", [pa.PA_KV_F16, pa.PA_KV_BF16, pa.PA_KV_FP8_E4M3])
 def test_long_ranges_of_mixed_lengths_against_oracle(kv):
     # Row tiles of very different KV lengths in one call, at G = 8: a chunk
     # after a 4000-token history (200 new tokens), a short chunk after 8936
