@@ -65,6 +65,8 @@ def parse():
     p.add_argument("--shared-prefix", action="store_true",
                    help="parallel-sampling workloads: decode with pa_decode_shared_prefix (samples of one prompt "
                         "read its blocks together)")
+    p.add_argument("--spec-tokens", type=int, default=4,
+                   help="spec72b: new (speculative) tokens per sequence (default 4)")
     p.add_argument("--seqs", type=int, default=None,
                    help="same shape with fewer sequences (small cases for profiling); default: the full 100")
     return p.parse_args()
@@ -325,7 +327,8 @@ class OracleSample:
 
 def workload(args):
     from paged_kv_cache_12_gb300 import workloads
-    w = workloads.make(args.workload)
+    w = workloads.make(args.workload, spec_tokens=args.spec_tokens) if args.workload == "spec72b" \
+        else workloads.make(args.workload)
     if args.seqs is None or args.seqs == w.num_seqs:
         return w
     if w.num_prompts:
@@ -751,11 +754,12 @@ RECORDS = (("mha7b", "f16", False), ("mix", "f16", False), ("cow16", "f16", Fals
            ("gqa72b", "fp8", False), ("spec72b", "f16", False), ("spec72b", "fp8", False), ("chunked", "f16", False))
 
 
-def workload_record(name, kvd, shared, pa, torch, dev, calls=20, warmup=3):
+def workload_record(name, kvd, shared, pa, torch, dev, seconds=0.4, warmup=3):
     """One layer of a workload, timed call by call with CUDA events on the
     launching stream: block copy (copy-on-write pairs, if any), KV write and
     the attention call, each with its algorithmic bytes (and FLOPs) and the
-    fraction of the measured roof; the SM clock sampled meanwhile.  Inputs
+    fraction of the measured roof; the SM clock sampled meanwhile (as many
+    calls as take about `seconds`, so that the sampler sees them).  Inputs
     are larger than L2, so nothing is flushed between calls."""
     from paged_kv_cache_12_gb300 import workloads
     w = workloads.make(name)
@@ -822,9 +826,12 @@ def workload_record(name, kvd, shared, pa, torch, dev, calls=20, warmup=3):
         if evs:
             evs[3].record(st)
 
+    t_w = time.perf_counter()
     for _ in range(warmup):
         one()
     torch.cuda.synchronize()
+    per_call = (time.perf_counter() - t_w) / warmup
+    calls = int(min(2000, max(20, seconds / max(per_call, 1e-6))))
     evs = [[E() for _ in range(4)] for _ in range(calls)]
     with ClockSampler(dev.index or 0) as clk:
         for e in evs:
@@ -843,7 +850,7 @@ def workload_record(name, kvd, shared, pa, torch, dev, calls=20, warmup=3):
     gbs = dbytes / (ms / 1e3) / 1e9
     call_name = ("pa_attention_causal" + ("_typed" if typed else "") if multi else
                  "pa_decode_shared_prefix" if shared else "pa_decode_typed" if typed else "pa_decode")
-    rec = {"workload": name, "kv_dtype": kvd, "call": call_name, "num_seqs": w.num_seqs,
+    rec = {"workload": name, "kv_dtype": kvd, "call": call_name, "num_seqs": w.num_seqs, "calls": calls,
            "ms": {"mean": round(ms, 5), "p10": round(float(np.percentile(t_call, 10)), 5),
                   "p90": round(float(np.percentile(t_call, 90)), 5)},
            "algorithmic_bytes": dbytes, "achieved_gbs": round(gbs, 1), "hbm_frac": round(gbs / peak, 4),

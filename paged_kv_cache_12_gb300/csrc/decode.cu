@@ -270,12 +270,15 @@ __device__ __forceinline__ int last_le(const int32_t *a, int n, int x) {
 // NaN rows; a query_start that is not a non-decreasing cover of [0, NQ) makes
 // every row NaN.
 // A sequence with at least pf_min_rows query rows (new tokens x G; 0: none)
-// goes to the tensor-core prefill kernel instead: it gets no items here, and
-// its ceil(T G / 128) row tiles are listed in ptiles, last rows first.
+// goes to the tensor-core prefill kernels instead: it gets no items here.  Its
+// ceil(T G / 128) row tiles, last rows first, are listed in ptiles when there
+// is one (or when pairs is 0), otherwise in pptiles as pairs of neighbouring
+// tiles {seq, tile, tile - 1, 0} (an odd one out as {seq, 0, -1, 0}).
 __global__ void __launch_bounds__(PREP_THREADS) causal_prep_kernel(
     const int32_t *__restrict__ context_lens, const int32_t *__restrict__ qs, int B, int NQ, int Hq, int D, int Hkv,
     int max_ctx, long long max_table_tokens, int pt, int ms, WsHeader *hdr, int *part_off, int *vlen, int *gstart,
-    ItemRec *items, int *grp, uint16_t *out, uint32_t nan2, int pf_min_rows, int4 *ptiles) {
+    ItemRec *items, int *grp, uint16_t *out, uint32_t nan2, int pf_min_rows, int4 *ptiles, int4 *pptiles,
+    int pairs) {
     constexpr int NBK = MAX_PART_TOKENS / CHUNK;
     __shared__ int warp_sums[PREP_THREADS / 32];
     __shared__ int hist[NBK], cursor[NBK];
@@ -328,21 +331,27 @@ __global__ void __launch_bounds__(PREP_THREADS) causal_prep_kernel(
         if (i < B) gstart[i] = e;
         run_g += tot;
     }
-    // pass 2b: row tiles of the prefill kernel
-    int run_t = 0;
+    // pass 2b: row tiles of the prefill kernels
+    int run_t = 0, run_p = 0;
     for (int base = 0; base < B; base += PREP_THREADS) {
         const int i = base + threadIdx.x;
         int n = 0, L, T;
         if (i < B && qs_ok && seq_ok(i, L, T) && prefill(T)) n = (int)(((long long)T * G + 127) / 128);
-        int tot;
-        const int e = run_t + block_exclusive_scan(n, warp_sums, &tot);
-        for (int k = 0; k < n; ++k) ptiles[e + k] = make_int4(i, n - 1 - k, 0, 0);
+        const bool paired = pairs && n >= 2;
+        const int ns = paired ? 0 : n, np = paired ? (n + 1) / 2 : 0;
+        int tot, totp;
+        const int e = run_t + block_exclusive_scan(ns, warp_sums, &tot);
+        const int ep = run_p + block_exclusive_scan(np, warp_sums, &totp);
+        for (int k = 0; k < ns; ++k) ptiles[e + k] = make_int4(i, n - 1 - k, 0, 0);
+        for (int k = 0; k < np; ++k) pptiles[ep + k] = make_int4(i, n - 1 - 2 * k, n - 2 - 2 * k, 0);
         run_t += tot;
+        run_p += totp;
     }
     if (threadIdx.x == 0) {
         gstart[B] = run_g;
         part_off[NQ] = run;
         hdr->pf_items = run_t * Hkv;
+        hdr->pf2_items = run_p * Hkv;
     }
     __syncthreads();
     const int NG = run_g;
@@ -493,6 +502,16 @@ long long wait_limit_cycles() {
 bool prefill_enabled() {
     static const bool on = [] {
         const char *e = std::getenv("PA_PREFILL");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
+// Whether sequences with several row tiles take them in pairs on the two-tile
+// tensor-core kernel (unless PA_PREFILL_PAIRS=0, read once).
+bool prefill_pairs_enabled() {
+    static const bool on = [] {
+        const char *e = std::getenv("PA_PREFILL_PAIRS");
         return !(e && e[0] == '0');
     }();
     return on;
@@ -730,11 +749,14 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     const bool pf = prefill_enabled() && head_dim == 128 && PF_ROWS % G == 0 &&
                     (long long)num_query_tokens * G >= PF_MIN_ROWS;
     int4 *ptiles = reinterpret_cast<int4 *>(ws + L.ptiles);
+    int4 *ppairs = reinterpret_cast<int4 *>(ws + L.ppairs);
+    // sequences with several row tiles take them two at a time (16-bit caches)
+    const bool pairs = pf && kv != PA_KV_FP8_E4M3 && prefill_pairs_enabled() && prefill2_usable(kv);
     causal_prep_kernel<<<1, PREP_THREADS, 0, st>>>(context_lens, query_start, num_seqs, num_query_tokens, num_heads,
                                                    head_dim, num_kv_heads, max_context_len,
                                                    (long long)max_blocks_per_seq * block_size, L.pt, ms, hdr,
                                                    part_off, vlen, gstart, items, grp, hout, nan_pair(kv),
-                                                   pf ? PF_MIN_ROWS : 0, ptiles);
+                                                   pf ? PF_MIN_ROWS : 0, ptiles, ppairs, pairs ? 1 : 0);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
 
     DecodeArgs args;
@@ -769,6 +791,7 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     pa_.context_lens = context_lens;
     pa_.query_start = query_start;
     pa_.tiles = ptiles;
+    pa_.pairs = ppairs;
     pa_.hdr = hdr;
     pa_.Hq = num_heads;
     pa_.Hkv = num_kv_heads;
@@ -779,6 +802,11 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     pa_.scale_log2 = args.scale_log2;   // with the K scale of an FP8 cache
     pa_.v_scale = args.v_scale;
     pa_.wait_limit = wait_limit_cycles();
+    if (pairs) {
+        // pairs first (the long chunks), then the sequences of one row tile
+        const int rc2 = launch_prefill2(kv, tmk, tmv, pa_, (L.ptile_cap + 1) / 2 * num_kv_heads, st);
+        if (rc2 != PA_OK) return rc2;
+    }
     return launch_prefill(kv, tmk, tmv, pa_, L.ptile_cap * num_kv_heads, st);
 }
 

@@ -21,6 +21,9 @@
 #ifndef PA_DECODE_MINB_FP8
 #define PA_DECODE_MINB_FP8 6
 #endif
+#ifndef PA_DECODE_DEPTH_FP8
+#define PA_DECODE_DEPTH_FP8 (2 * PA_DECODE_DEPTH)
+#endif
 #ifndef PA_FP8_LATE_V
 #define PA_FP8_LATE_V 0
 #endif
@@ -76,13 +79,14 @@ struct WsHeader {
     int error;
     int total_items;
     int counter;
-    int pf_items;    // multi-token form: work items of the tensor-core prefill kernel
-    int pad[60];
+    int pf_items;    // multi-token form: work items of the one-tile tensor-core kernel
+    int pf2_items;   // multi-token form: work items of the two-tile tensor-core kernel
+    int pad[59];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
 struct WsLayout {
-    size_t part_off, gsize, gshared, items, grp, ml, o, ptiles, total;
+    size_t part_off, gsize, gshared, items, grp, ml, o, ptiles, ppairs, total;
     int pmax, pt;
     long long item_cap, ptile_cap;
 };
@@ -144,9 +148,12 @@ inline WsLayout ws_layout_causal(int B, int NQ, int Hq, int Hkv, int D, int max_
     off += up256(sizeof(float2) * (size_t)parts * Hq);
     w.o = off;
     off += up256(sizeof(float) * (size_t)parts * Hq * D);
-    // prefill tiles: 128 query rows (new tokens x G) of one sequence each
+    // prefill tiles: 128 query rows (new tokens x G) of one sequence each,
+    // listed alone or in pairs of neighbouring tiles
     w.ptile_cap = ((long long)NQ * G + 127) / 128 + B;
     w.ptiles = off;
+    off += up256(sizeof(int4) * (size_t)w.ptile_cap);
+    w.ppairs = off;
     off += up256(sizeof(int4) * (size_t)w.ptile_cap);
     w.total = off;
     return w;
@@ -195,7 +202,8 @@ struct Cfg {
     // pipeline stages per consumer: a two-tile consumer keeps fewer warps on
     // an SM (registers), so each keeps more stages in flight; one-byte
     // elements make a stage half as large, so there are twice as many
-    static constexpr int DEPTH = (NT == 1 ? PA_DECODE_DEPTH : PA_DECODE_DEPTH_WIDE) * (FP8 ? 2 : 1);
+    static constexpr int DEPTH = NT == 1 ? (FP8 ? PA_DECODE_DEPTH_FP8 : PA_DECODE_DEPTH)
+                                         : PA_DECODE_DEPTH_WIDE * (FP8 ? 2 : 1);
     static constexpr int BOXES = D * ESZ / 128;            // 128-byte boxes per tile row
     static constexpr int BOX_ELEMS = 128 / ESZ;            // elements per box row
     static constexpr int TILE = BOXES * CHUNK * 128;       // one 16-token K or V tile
@@ -678,6 +686,10 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
             }
         }
         const int nchunks = dp->nchunks;
+        // the second head tile holds query rows 8 .. 15; an item with at most
+        // 8 rows (a private range at G <= 8, one decode row of a multi-token
+        // call) skips its MMAs and softmax (warp-uniform; no bit changes)
+        const bool tile1 = NT == 2 && dp->nmem * a.G > 8;
         // CAUSAL: tokens of the item (from its start) that each column's query
         // row sees -- at least one, as every member sees the item's first token
         int lim[NT][2];
@@ -744,6 +756,7 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
                         for (int t = 0; t < NT; ++t) {
+                            if (t == 1 && !tile1) continue;
                             float *acc_s = h ? sb[t] : sa[t];
                             mma_16816(acc_s[0], acc_s[1], acc_s[2], acc_s[3], af[h][0], af[h][1], af[h][2], af[h][3],
                                       qb[t][2 * u + h][0], qb[t][2 * u + h][1], acc_s[0], acc_s[1], acc_s[2], acc_s[3]);
@@ -756,6 +769,7 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                     ldmatrix_x4(kt + (k >> 2) * (C::BOXES > 1 ? CHUNK * 128 : 0) + koff[k & 3], a0, a1, a2, a3);
 #pragma unroll
                     for (int t = 0; t < NT; ++t) {
+                        if (t == 1 && !tile1) continue;
                         float *acc_s = (k & 1) ? sb[t] : sa[t];
                         mma_kv<KV>(acc_s[0], acc_s[1], acc_s[2], acc_s[3], a0, a1, a2, a3, qb[t][k][0], qb[t][k][1]);
                     }
@@ -797,6 +811,10 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
             uint32_t pb[NT][2];
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
+                if (t == 1 && !tile1) {
+                    pb[t][0] = pb[t][1] = 0u;
+                    continue;
+                }
                 float s0 = sa[t][0] + sb[t][0], s1 = sa[t][1] + sb[t][1];   // token r, heads 2cq, 2cq+1
                 float s2 = sa[t][2] + sb[t][2], s3 = sa[t][3] + sb[t][3];   // token r + 8
                 if constexpr (CAUSAL) {
@@ -866,6 +884,7 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                         }
 #pragma unroll
                         for (int t = 0; t < NT; ++t)
+                            if (t == 0 || tile1)
                             mma_kv<KV>(acc[2 * u + h][t][0], acc[2 * u + h][t][1], acc[2 * u + h][t][2],
                                        acc[2 * u + h][t][3], f[0], f[1], f[2], f[3], pb[t][0], pb[t][1]);
                     }
@@ -885,8 +904,9 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                 for (int i = 0; i < MT; ++i)
 #pragma unroll
                     for (int t = 0; t < NT; ++t)
-                        mma_kv<KV>(acc[i][t][0], acc[i][t][1], acc[i][t][2], acc[i][t][3], va[i][0], va[i][1],
-                                   va[i][2], va[i][3], pb[t][0], pb[t][1]);
+                        if (t == 0 || tile1)
+                            mma_kv<KV>(acc[i][t][0], acc[i][t][1], acc[i][t][2], acc[i][t][3], va[i][0], va[i][1],
+                                       va[i][2], va[i][3], pb[t][0], pb[t][1]);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&cs.empty[s]));   // stage free for the next copy

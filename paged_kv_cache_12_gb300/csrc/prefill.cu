@@ -68,7 +68,6 @@ constexpr int CTRL_BAD = 416;              // int[BAD_SLOTS]: 1 + the CTA-local 
                                            // out-of-range block id (producers run at most a few KV tiles,
                                            // hence items, ahead of the softmax that reads the mark)
 constexpr int CTRL_ABORT = CTRL_BAD + 4 * BAD_SLOTS;   // int: a role gave up waiting
-constexpr int PF_THREADS = 7 * 32;         // K producer, V producer, MMA, 4 softmax warps
 
 // Shared memory per cache type: the K and V rings the MMAs read (16-bit
 // tiles; R stages each) and, for an FP8 cache, the rings its codes are staged
@@ -85,6 +84,10 @@ struct PfL {
     static constexpr int OFF_V8 = OFF_K8 + S8 * F8_BYTES;
     static constexpr int OFF_CTRL = OFF_V8 + S8 * F8_BYTES;
     static constexpr int SMEM = OFF_CTRL + CTRL_BYTES + 1024;   // + alignment slack
+    // K producer, V producer, MMA, 4 softmax warps; an FP8 cache adds the
+    // warp that issues the copies of the codes (warps 0 and 1 convert); 8
+    // warps at most keep two warps per SM sub-partition (registers)
+    static constexpr int THREADS = (F8 ? 8 : 7) * 32;
     static_assert(R <= MAXST && S8 <= MAXST, "ring stages");
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
 };
@@ -96,13 +99,15 @@ constexpr int TM_Q = TM_O + PD;
 constexpr int TM_P = TM_Q + PD / 2;
 static_assert(TM_P + PN / 2 <= TMEM_COLS, "tensor-memory columns");
 static_assert(PN == 64 || PN == 128, "KV tile of 64 or 128 tokens");
-static_assert(8 * (6 * MAXST + 11) + 8 <= CTRL_BAD && CTRL_ABORT + 4 <= CTRL_BYTES, "control block layout");
+static_assert(8 * (8 * MAXST + 11) + 8 <= CTRL_BAD && CTRL_ABORT + 4 <= CTRL_BYTES, "control block layout");
 
 struct PfBars {
     // pfull / pvdone: one per PV-number parity, so that a softmax warp a step
     // ahead of another never adds its arrival to the other step's phase
-    // k8full / v8full: FP8 codes staged (TMA bytes landed)
+    // k8full / v8full: FP8 codes staged (TMA bytes landed); k8empty / v8empty:
+    // the staged codes converted (the staging slot may be refilled)
     uint32_t kfull[MAXST], kempty[MAXST], vfull[MAXST], vempty[MAXST], k8full[MAXST], v8full[MAXST];
+    uint32_t k8empty[MAXST], v8empty[MAXST];
     uint32_t sfull[2], sfree[2], pfull[2], pvdone[2], qfull;
     uint32_t tmem_slot, flags;   // shared addresses
 };
@@ -117,6 +122,8 @@ __device__ __forceinline__ PfBars pf_bars(uint8_t *smem, int off_ctrl) {
     for (int s = 0; s < MAXST; ++s) b.vempty[s] = a, a += 8;
     for (int s = 0; s < MAXST; ++s) b.k8full[s] = a, a += 8;
     for (int s = 0; s < MAXST; ++s) b.v8full[s] = a, a += 8;
+    for (int s = 0; s < MAXST; ++s) b.k8empty[s] = a, a += 8;
+    for (int s = 0; s < MAXST; ++s) b.v8empty[s] = a, a += 8;
     b.sfull[0] = a, a += 8;
     b.sfull[1] = a, a += 8;
     b.sfree[0] = a, a += 8;
@@ -127,7 +134,7 @@ __device__ __forceinline__ PfBars pf_bars(uint8_t *smem, int off_ctrl) {
     b.pvdone[1] = a, a += 8;
     b.qfull = a, a += 8;
     b.tmem_slot = a, a += 8;
-    b.flags = a;   // barriers and slots end at byte 8 (6 MAXST + 11) + 8 = 240 <= CTRL_BAD
+    b.flags = a;   // barriers and slots end at byte 8 (8 MAXST + 11) + 8 = 288 <= CTRL_BAD
     return b;
 }
 
@@ -136,21 +143,32 @@ struct PfTile {
     int seq, kvh, row0, ntok, C, nkv, L, q0;
 };
 
-__device__ __forceinline__ PfTile pf_tile(const PrefillArgs &a, int item) {
-    const int4 rec = a.tiles[item / a.Hkv];
+// Row tile `rt` (128 / G consecutive new tokens) of sequence `seq`, kv head kvh.
+__device__ __forceinline__ PfTile pf_row_tile(const PrefillArgs &a, int seq, int kvh, int rt) {
     PfTile t;
-    t.seq = rec.x;
-    t.kvh = item % a.Hkv;
+    t.seq = seq;
+    t.kvh = kvh;
     const int tpt = PM / a.G;               // new tokens per tile
     t.L = a.context_lens[t.seq];
     t.q0 = a.query_start[t.seq];
     const int T = a.query_start[t.seq + 1] - t.q0;
-    t.row0 = rec.y * tpt;                   // first new token of the tile
+    t.row0 = rt * tpt;                      // first new token of the tile
     t.ntok = min(tpt, T - t.row0);
     t.C = t.L - T + 1;                      // positions the first new token sees
     t.nkv = (t.C + t.row0 + t.ntok - 1 + PN - 1) / PN;
     return t;
 }
+
+// Work item of the one-tile kernel: (row tile, kv head).
+__device__ __forceinline__ PfTile pf_tile(const PrefillArgs &a, int item) {
+    const int4 rec = a.tiles[item / a.Hkv];
+    return pf_row_tile(a, rec.x, item % a.Hkv, rec.y);
+}
+
+// What a producer warp needs of a work item: the KV range it streams.
+struct PfRange {
+    int seq, kvh, nkv, L;
+};
 
 __device__ __forceinline__ void pf_error(const PrefillArgs &a) { atomicExch(&a.hdr->error, PA_ERR_TIMEOUT); }
 
@@ -163,25 +181,31 @@ __device__ __forceinline__ volatile int *pf_bad_slot(uint8_t *smem, int off_ctrl
 
 // ----------------------------------------------------------- producer
 
-template <int KV>
-__device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const PrefillArgs &a, const PfBars &bb,
-                            volatile int *abort_flag, int total, int kv) {
-    using L = PfL<KV>;
-    constexpr int PST = L::R;
+// A producer warp: streams the K or V tiles (NMAP = 1: map[0]) or both (NMAP
+// = 2: map[0] into ring 0, map[1] into ring 1, the same block ids) of every
+// work item of this CTA -- range(item) gives the item's KV range -- into rings
+// of PST stages at byte offsets off_ring[] of shared memory, paced by full[]
+// and empty[].  A 16-bit tile is two 64-column boxes per row group; an FP8
+// tile (F8: codes for a staging ring) one 128-byte box per row group.
+template <int PST, bool F8, int NMAP, class RangeOf>
+__device__ void pf_stream(uint8_t *smem, const int *off_ring, int off_ctrl, const uint32_t *const *full,
+                          const uint32_t *const *empty, const CUtensorMap *const *map, const PrefillArgs &a,
+                          volatile int *abort_flag, int total, RangeOf range) {
+    constexpr int TILE = F8 ? F8_BYTES : KV_BYTES;
+    constexpr int NBOX = F8 ? 1 : 2;
     const int lane = threadIdx.x & 31;
     const uint64_t pol = policy_evict_normal();
     const int box_rows = a.bs < 16 ? a.bs : 16;    // rows per TMA box: one box per block or 16-row group
-    const uint32_t base = smem_u32(smem) + (kv ? L::OFF_V : L::OFF_K);
-    const uint32_t *full = kv ? bb.vfull : bb.kfull;
-    const uint32_t *empty = kv ? bb.vempty : bb.kempty;
     int cnt = 0;
     // Before leaving, the last copy into every stage has landed (bounded).
     auto drain = [&]() {
-        for (int s = 0; s < PST; ++s)
-            if (cnt > s) mbar_wait_bounded(full[s], (uint32_t)(((s + (cnt - 1 - s) / PST * PST) / PST) & 1), WAIT_LIMIT);
+        for (int r = 0; r < NMAP; ++r)
+            for (int s = 0; s < PST; ++s)
+                if (cnt > s)
+                    mbar_wait_bounded(full[r][s], (uint32_t)(((s + (cnt - 1 - s) / PST * PST) / PST) & 1), WAIT_LIMIT);
     };
     for (int item = blockIdx.x; item < total; item += gridDim.x) {
-        const PfTile t = pf_tile(a, item);
+        const PfRange t = range(item);
         const int32_t *row = a.block_tables + (long long)t.seq * a.mbps;
         for (int n = 0; n < t.nkv; ++n) {
             // lane j owns box j of the tile (tokens t0 + j box_rows ..): its block id,
@@ -192,7 +216,10 @@ __device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const Prefill
             const int32_t blk = mine ? __ldg(row + tok / a.bs) : 0;
             const int s = cnt % PST;
             // the warp decides together (no lane may leave alone)
-            const bool got = !*abort_flag && mbar_wait_bounded(empty[s], ((cnt / PST) & 1) ^ 1, a.wait_limit);
+            bool got = !*abort_flag;
+#pragma unroll
+            for (int r = 0; r < NMAP; ++r)
+                got = got && mbar_wait_bounded(empty[r][s], ((cnt / PST) & 1) ^ 1, a.wait_limit);
             if (!__all_sync(0xffffffffu, got)) {
                 if (lane == 0) pf_error(a);
                 *abort_flag = 1;
@@ -202,15 +229,20 @@ __device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const Prefill
             const unsigned boxes = __ballot_sync(0xffffffffu, mine);
             const bool bad = __any_sync(0xffffffffu, mine && (blk < 0 || blk >= a.num_blocks));
             if (lane == 0) {
-                if (bad) *pf_bad_slot(smem, L::OFF_CTRL, pf_local(item)) = pf_local(item) + 1;
-                mbar_arrive_expect_tx(full[s], bad ? 0u : (uint32_t)(__popc(boxes) * 2 * box_rows * 128));
+                if (bad) *pf_bad_slot(smem, off_ctrl, pf_local(item)) = pf_local(item) + 1;
+#pragma unroll
+                for (int r = 0; r < NMAP; ++r)
+                    mbar_arrive_expect_tx(full[r][s], bad ? 0u : (uint32_t)(__popc(boxes) * NBOX * box_rows * 128));
             }
             __syncwarp();
             if (!bad && mine) {
-                const uint32_t dst = base + s * KV_BYTES + lane * box_rows * 128;
                 const int y = (int)(((long long)blk * a.Hkv + t.kvh) * a.bs) + tok % a.bs;
-                tma_load_2d(dst, map, 0, y, full[s], pol);
-                tma_load_2d(dst + PN * 128, map, 64, y, full[s], pol);
+#pragma unroll
+                for (int r = 0; r < NMAP; ++r) {
+                    const uint32_t dst = smem_u32(smem) + off_ring[r] + s * TILE + lane * box_rows * 128;
+                    tma_load_2d(dst, map[r], 0, y, full[r][s], pol);
+                    if (!F8) tma_load_2d(dst + PN * 128, map[r], 64, y, full[r][s], pol);
+                }
             }
             __syncwarp();
             ++cnt;
@@ -219,108 +251,78 @@ __device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const Prefill
     drain();
 }
 
-// FP8 cache: the same work, through a staging ring.  The warp issues the TMA
-// copies of the codes of up to S8 KV tiles ahead (one 128-byte box column per
-// block); behind them it turns each staged tile into the 16-bit tile the MMAs
-// read, in the same swizzled layout a 16-bit TMA copy would have written:
-// code chunk j (dims 16 j .. 16 j + 15) of row r becomes fp16 chunks 2 (j % 4)
-// and 2 (j % 4) + 1 of the 64-dim block j / 4.  Every E4M3 value is an fp16
-// value, so the tile is exact; the scales are applied to the scores and the
-// output.  A staging slot is refilled only after this warp converted it.
-__device__ void pf_producer_fp8(uint8_t *smem, const CUtensorMap *map, const PrefillArgs &a, const PfBars &bb,
-                                volatile int *abort_flag, int total, int kv) {
+template <int KV>
+__device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const PrefillArgs &a, const PfBars &bb,
+                            volatile int *abort_flag, int total, int kv) {
+    using L = PfL<KV>;
+    const int off[1] = {kv ? L::OFF_V : L::OFF_K};
+    const uint32_t *full[1] = {kv ? bb.vfull : bb.kfull};
+    const uint32_t *empty[1] = {kv ? bb.vempty : bb.kempty};
+    const CUtensorMap *maps[1] = {map};
+    pf_stream<L::R, false, 1>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total, [&](int item) {
+                        const PfTile t = pf_tile(a, item);
+                        return PfRange{t.seq, t.kvh, t.nkv, t.L};
+                    });
+}
+
+// FP8 cache: warp 7 streams the codes of the K and V tiles into 3-stage
+// staging rings (pf_stream, one 128-byte box column per block), and warps 0
+// and 1 turn each staged tile into the 16-bit tile the MMAs read, in the same
+// swizzled layout a 16-bit TMA copy would have written: code chunk j (dims
+// 16 j .. 16 j + 15) of row r becomes fp16 chunks 2 (j % 4) and 2 (j % 4) + 1
+// of the 64-dim block j / 4.  Every E4M3 value is an fp16 value, so the tile
+// is exact; the scales are applied to the scores and the output.  The
+// converting warp loads no block id and issues no copy, so it never waits on
+// memory latency except for the staged tile itself.
+__device__ void pf_convert_fp8(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, volatile int *abort_flag,
+                               int total, int kv) {
     using L = PfL<PA_KV_FP8_E4M3>;
     constexpr int R = L::R, S8 = L::S8;
     const int lane = threadIdx.x & 31;
-    const uint64_t pol = policy_evict_normal();
-    const int box_rows = a.bs < 16 ? a.bs : 16;
-    const uint32_t stage = smem_u32(smem) + (kv ? L::OFF_V8 : L::OFF_K8);
     const uint8_t *stage_p = smem + (kv ? L::OFF_V8 : L::OFF_K8);
     uint8_t *ring = smem + (kv ? L::OFF_V : L::OFF_K);
     const uint32_t *full8 = kv ? bb.v8full : bb.k8full;
+    const uint32_t *empty8 = kv ? bb.v8empty : bb.k8empty;
     const uint32_t *full = kv ? bb.vfull : bb.kfull;
     const uint32_t *empty = kv ? bb.vempty : bb.kempty;
-    // issue and conversion walk the same sequence of (work item, KV tile)
-    struct Walk {
-        int item, n;
-        PfTile t;
-    };
-    auto start = [&](Walk &w) {
-        w.item = blockIdx.x;
-        w.n = 0;
-        if (w.item < total) w.t = pf_tile(a, w.item);
-    };
-    auto step = [&](Walk &w) {
-        if (++w.n < w.t.nkv) return;
-        w.n = 0;
-        w.item += gridDim.x;
-        if (w.item < total) w.t = pf_tile(a, w.item);
-    };
-    Walk wi, wc;
-    start(wi);
-    start(wc);
-    int issued = 0, conv = 0;
-    bool ok = true;
-    auto fail = [&]() {
-        if (lane == 0) pf_error(a);
-        *abort_flag = 1;
-        ok = false;
-    };
-    auto issue = [&]() {
-        const int s8 = issued % S8;
-        const int t0 = wi.n * PN;
-        const int tok = t0 + lane * box_rows;
-        const bool mine = lane < PN / box_rows && tok < wi.t.L;
-        const int32_t blk = mine ? __ldg(a.block_tables + (long long)wi.t.seq * a.mbps + tok / a.bs) : 0;
-        const unsigned boxes = __ballot_sync(0xffffffffu, mine);
-        const bool bad = __any_sync(0xffffffffu, mine && (blk < 0 || blk >= a.num_blocks));
-        if (lane == 0) {
-            if (bad) *pf_bad_slot(smem, L::OFF_CTRL, pf_local(wi.item)) = pf_local(wi.item) + 1;
-            mbar_arrive_expect_tx(full8[s8], bad ? 0u : (uint32_t)(__popc(boxes) * box_rows * 128));
-        }
-        __syncwarp();
-        if (!bad && mine) {
-            const int y = (int)(((long long)blk * a.Hkv + wi.t.kvh) * a.bs) + tok % a.bs;
-            tma_load_2d(stage + s8 * F8_BYTES + lane * box_rows * 128, map, 0, y, full8[s8], pol);
-        }
-        __syncwarp();
-        ++issued;
-        step(wi);
-    };
-    auto convert = [&]() {
-        const int s8 = conv % S8, c = conv % R;
-        const bool got = !*abort_flag && mbar_wait_bounded(full8[s8], (uint32_t)((conv / S8) & 1), a.wait_limit) &&
-                         mbar_wait_bounded(empty[c], (uint32_t)(((conv / R) & 1) ^ 1), a.wait_limit);
-        if (!__all_sync(0xffffffffu, got)) return fail();
-        const uint8_t *src = stage_p + s8 * F8_BYTES;
-        uint8_t *dst = ring + c * KV_BYTES;
+    int conv = 0;
+    for (int item = blockIdx.x; item < total; item += gridDim.x) {
+        const int nkv = pf_tile(a, item).nkv;
+        for (int n = 0; n < nkv; ++n, ++conv) {
+            const int s8 = conv % S8, c = conv % R;
+            const bool got = !*abort_flag &&
+                             mbar_wait_bounded(full8[s8], (uint32_t)((conv / S8) & 1), a.wait_limit) &&
+                             mbar_wait_bounded(empty[c], (uint32_t)(((conv / R) & 1) ^ 1), a.wait_limit);
+            if (!__all_sync(0xffffffffu, got)) {
+                if (lane == 0) pf_error(a);
+                *abort_flag = 1;
+                return;   // the staging warp drains its own copies
+            }
+            const uint8_t *src = stage_p + s8 * F8_BYTES;
+            uint8_t *dst = ring + c * KV_BYTES;
 #pragma unroll 4
-        for (int i = 0; i < PN / 4; ++i) {   // 4 rows x 8 code chunks per pass
-            const int r = 4 * i + (lane >> 3), j = lane & 7;
-            const uint4 x = *reinterpret_cast<const uint4 *>(src + r * 128 + ((j ^ (r & 7)) << 4));
-            const uint4 lo = make_uint4(e4m3x2_lo_to_f16x2(x.x), e4m3x2_hi_to_f16x2(x.x), e4m3x2_lo_to_f16x2(x.y),
-                                        e4m3x2_hi_to_f16x2(x.y));
-            const uint4 hi = make_uint4(e4m3x2_lo_to_f16x2(x.z), e4m3x2_hi_to_f16x2(x.z), e4m3x2_lo_to_f16x2(x.w),
-                                        e4m3x2_hi_to_f16x2(x.w));
-            uint8_t *row = dst + (j >> 2) * (PN * 128) + r * 128;
-            const int c0 = 2 * (j & 3);
-            *reinterpret_cast<uint4 *>(row + ((c0 ^ (r & 7)) << 4)) = lo;
-            *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (r & 7)) << 4)) = hi;
+            for (int i = 0; i < PN / 4; ++i) {   // 4 rows x 8 code chunks per pass
+                const int r = 4 * i + (lane >> 3), j = lane & 7;
+                const uint4 x = *reinterpret_cast<const uint4 *>(src + r * 128 + ((j ^ (r & 7)) << 4));
+                const uint4 lo = make_uint4(e4m3x2_lo_to_f16x2(x.x), e4m3x2_hi_to_f16x2(x.x),
+                                            e4m3x2_lo_to_f16x2(x.y), e4m3x2_hi_to_f16x2(x.y));
+                const uint4 hi = make_uint4(e4m3x2_lo_to_f16x2(x.z), e4m3x2_hi_to_f16x2(x.z),
+                                            e4m3x2_lo_to_f16x2(x.w), e4m3x2_hi_to_f16x2(x.w));
+                uint8_t *row = dst + (j >> 2) * (PN * 128) + r * 128;
+                const int c0 = 2 * (j & 3);
+                *reinterpret_cast<uint4 *>(row + ((c0 ^ (r & 7)) << 4)) = lo;
+                *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (r & 7)) << 4)) = hi;
+            }
+            // the tile, written through the generic proxy, is for the tensor
+            // cores, and the staged codes were read before the slot is refilled
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(full[c]);
+                mbar_arrive(empty8[s8]);
+            }
         }
-        // the tile, written through the generic proxy, is for the tensor cores;
-        // the staged codes have been read before their slot is refilled
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(full[c]);
-        ++conv;
-        step(wc);
-    };
-    while (ok && wc.item < total) {
-        while (wi.item < total && issued < conv + S8) issue();
-        convert();
     }
-    // staged copies not converted (only after a failure) land before the warp leaves
-    for (int k = conv; k < issued; ++k) mbar_wait_bounded(full8[k % S8], (uint32_t)((k / S8) & 1), WAIT_LIMIT);
 }
 
 // ----------------------------------------------------------- MMA issuer
@@ -602,7 +604,7 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
 }
 
 template <int KV>
-__global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmk,
+__global__ void __launch_bounds__(PfL<KV>::THREADS, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                  const __grid_constant__ CUtensorMap tmv,
                                                                  const PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
@@ -612,6 +614,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + L::OFF_CTRL + CTRL_ABORT);
     const int warp = threadIdx.x >> 5;
     const int total = *reinterpret_cast<volatile int *>(&a.hdr->pf_items);   // written by the prep kernel
+    if ((int)blockIdx.x >= total) return;   // no work item for this CTA (the whole CTA leaves)
     if (threadIdx.x == 0) {
         for (int s = 0; s < L::R; ++s) {
             mbar_init(bb.kfull[s], 1);
@@ -622,6 +625,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         for (int s = 0; s < L::S8; ++s) {
             mbar_init(bb.k8full[s], 1);
             mbar_init(bb.v8full[s], 1);
+            mbar_init(bb.k8empty[s], 1);
+            mbar_init(bb.v8empty[s], 1);
         }
         mbar_init(bb.sfull[0], 1);
         mbar_init(bb.sfull[1], 1);
@@ -647,7 +652,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + (bb.tmem_slot - smem_u32(smem)));
     if (warp < 2) {
         if constexpr (L::F8)
-            pf_producer_fp8(smem, warp ? &tmv : &tmk, a, bb, abort_flag, total, warp);
+            pf_convert_fp8(smem, a, bb, abort_flag, total, warp);
         else
             pf_producer<KV>(smem, warp ? &tmv : &tmk, a, bb, abort_flag, total, warp);
     } else if (warp == 2) {
@@ -658,8 +663,17 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
             mbar_wait_bounded(bb.flags, 0, WAIT_LIMIT);
         }
         __syncwarp();
-    } else {
+    } else if (warp < 7) {
         pf_softmax<KV>(smem, a, bb, tmem, abort_flag, total);
+    } else if constexpr (L::F8) {   // warp 7: the codes of K and V into the staging rings
+        const int off[2] = {L::OFF_K8, L::OFF_V8};
+        const uint32_t *full[2] = {bb.k8full, bb.v8full};
+        const uint32_t *empty[2] = {bb.k8empty, bb.v8empty};
+        const CUtensorMap *maps[2] = {&tmk, &tmv};
+        pf_stream<L::S8, true, 2>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total, [&](int item) {
+            const PfTile t = pf_tile(a, item);
+            return PfRange{t.seq, t.kvh, t.nkv, t.L};
+        });
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -667,6 +681,473 @@ __global__ void __launch_bounds__(PF_THREADS, 1) prefill_kernel(const __grid_con
         tc_fence_after_sync();
         tmem_dealloc(tmem, TMEM_COLS);
     }
+}
+
+// ===================================================== two row tiles per CTA
+//
+// A sequence with a long run of new tokens has many row tiles over nearly the
+// same KV range.  Here one CTA takes two neighbouring row tiles of it (tile 0
+// the later rows, which see the longer range) and every K/V tile it loads
+// feeds both, so L2 delivers half the bytes per FLOP of the one-tile kernel.
+// Tensor memory holds S0, S1 (one 128-column buffer per tile), O0 and O1 (all
+// 512 columns); each tile's P (fp16/bf16, two per column) is written over the
+// first 64 columns of its own S once the softmax has read them, and Q lives
+// in shared memory.  So S_x(n + 1) may only be issued after PV_x(n) -- which
+// reads P_x(n) from those columns -- and the MMA thread alternates the tiles:
+//   PV0(n), S0(n + 1), PV1(n), S1(n + 1), ...
+// while tile 1's softmax works on S1(n), tile 0's MMAs run, and the other way
+// round.  MMAs issued by one thread complete in issue order, and a commit
+// tracks every MMA issued before it: when S_x(n) is complete so is PV_x(n - 1),
+// so the softmax may rescale O_x then without waiting for anything else.
+// Warps: 0 and 1 produce K and V (3- and 2-stage rings), 2 issues the MMAs,
+// 3 idles, 4-7 run tile 0's softmax and 8-11 tile 1's, one row per thread.
+
+constexpr int P2_THREADS = 12 * 32;
+constexpr int Q_BYTES = PM * PD * 2;       // one 128-row Q tile, fp16/bf16, 128-byte swizzled K-major
+constexpr int P2_RK = 3, P2_RV = 2;        // K and V ring stages
+constexpr int P2_OFF_K = 0;
+constexpr int P2_OFF_V = P2_RK * KV_BYTES;
+constexpr int P2_OFF_Q = P2_OFF_V + P2_RV * KV_BYTES;
+constexpr int P2_OFF_CTRL = P2_OFF_Q + 2 * Q_BYTES;
+constexpr int P2_SMEM = P2_OFF_CTRL + CTRL_BYTES + 1024;   // + alignment slack
+constexpr int TM2_O = 2 * PN;              // O0 at columns 256 .., O1 at 384 ..
+constexpr int P2_REGS_LAUNCH = 168;        // per thread at launch: 65536 / 384, rounded down to 8
+constexpr int P2_REGS_LOW = 104;           // producers, MMA issuer (warpgroup 0)
+constexpr int P2_REGS_HIGH = 200;          // the two softmax warpgroups
+static_assert(128 * P2_REGS_LOW + 256 * P2_REGS_HIGH <= P2_THREADS * P2_REGS_LAUNCH,
+              "register split within the launch's pool");
+static_assert(P2_SMEM <= 227 * 1024, "shared memory of one CTA");
+static_assert(TM2_O + 2 * PD <= TMEM_COLS && PN == 128, "tensor-memory columns of the two-tile kernel");
+
+struct P2Bars {
+    uint32_t kfull[P2_RK], kempty[P2_RK], vfull[P2_RV], vempty[P2_RV];
+    uint32_t sfull[2], pfull[2], pvdone[2], qfull[2];   // per tile
+    uint32_t tmem_slot, flags;
+};
+static_assert(8 * (2 * P2_RK + 2 * P2_RV + 8 + 2) <= CTRL_BAD, "control block layout of the two-tile kernel");
+
+__device__ __forceinline__ P2Bars p2_bars(uint8_t *smem) {
+    uint32_t a = smem_u32(smem + P2_OFF_CTRL);
+    P2Bars b;
+    for (int s = 0; s < P2_RK; ++s) b.kfull[s] = a, a += 8;
+    for (int s = 0; s < P2_RK; ++s) b.kempty[s] = a, a += 8;
+    for (int s = 0; s < P2_RV; ++s) b.vfull[s] = a, a += 8;
+    for (int s = 0; s < P2_RV; ++s) b.vempty[s] = a, a += 8;
+    for (int x = 0; x < 2; ++x) b.sfull[x] = a, a += 8;
+    for (int x = 0; x < 2; ++x) b.pfull[x] = a, a += 8;
+    for (int x = 0; x < 2; ++x) b.pvdone[x] = a, a += 8;
+    for (int x = 0; x < 2; ++x) b.qfull[x] = a, a += 8;
+    b.tmem_slot = a, a += 8;
+    b.flags = a;
+    return b;
+}
+
+// Work item of the two-tile kernel: tile 0 and, if the pair has one, tile 1
+// (nkv of an absent tile 1 is 0).
+struct P2Item {
+    PfTile t[2];
+};
+
+__device__ __forceinline__ P2Item p2_item(const PrefillArgs &a, int item) {
+    const int4 rec = a.pairs[item / a.Hkv];
+    P2Item p;
+    p.t[0] = pf_row_tile(a, rec.x, item % a.Hkv, rec.y);
+    if (rec.z >= 0) {
+        p.t[1] = pf_row_tile(a, rec.x, item % a.Hkv, rec.z);
+    } else {
+        p.t[1] = p.t[0];
+        p.t[1].nkv = 0;
+    }
+    return p;
+}
+
+template <int KV>
+__device__ void p2_mma(uint8_t *smem, const PrefillArgs &a, const P2Bars &bb, uint32_t tmem, volatile int *abort_flag,
+                       int total) {
+    const bool bf16 = KV == PA_KV_BF16;
+    const uint32_t base = smem_u32(smem);
+    const uint32_t id_s = idesc_f16(PM, PN, bf16, false);
+    const uint32_t id_o = idesc_f16(PM, PD, bf16, true);
+    // K-major 128-byte-swizzled A (Q) and B (K) tiles: K-step k (16 dims) is at
+    // byte 32 (k % 4) of the 64-dim half k / 4, halves 128 rows x 128 bytes apart
+    const uint64_t dk0 = sw128_desc(base + P2_OFF_K, 16, 1024);
+    const uint64_t dq0 = sw128_desc(base + P2_OFF_Q, 16, 1024);
+    const uint64_t dv0 = sw128_desc(base + P2_OFF_V, PN * 128, 1024);
+    int kc = 0, vc = 0, qc[2] = {0, 0}, pc[2] = {0, 0};
+    bool ok = true;
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (!ok) return false;
+        if (*abort_flag || !mbar_wait_bounded(bar, parity, a.wait_limit)) {
+            pf_error(a);
+            *abort_flag = 1;
+            ok = false;
+        }
+        return ok;
+    };
+    auto issue_s = [&](int x, int ks) {   // S_x = Q_x K^T, K from ring stage ks
+        const uint64_t dk = dk0 + (uint64_t)(ks * (KV_BYTES >> 4));
+        const uint64_t dq = dq0 + (uint64_t)(x * (Q_BYTES >> 4));
+#pragma unroll
+        for (int k = 0; k < PD / 16; ++k) {
+            const uint64_t off = (uint64_t)((((k >> 2) * (PN * 128)) + (k & 3) * 32) >> 4);
+            umma_f16(tmem + x * PN, dq + off, dk + off, id_s, k > 0 ? 1u : 0u);
+        }
+        umma_commit(bb.sfull[x]);
+    };
+    auto issue_pv = [&](int x, int vs, int n) {   // O_x += P_x V, P_x in the first 64 columns of S_x
+        const uint64_t dv = dv0 + (uint64_t)(vs * (KV_BYTES >> 4));
+#pragma unroll
+        for (int k = 0; k < PN / 16; ++k)   // K-step k: 16 tokens = P columns 8k .. 8k + 7, V row 16 k
+            umma_f16_ts(tmem + TM2_O + x * PD, tmem + x * PN + 8 * k, dv + (uint64_t)((k * 16 * 128) >> 4), id_o,
+                        (n > 0 || k > 0) ? 1u : 0u);
+        umma_commit(bb.pvdone[x]);
+    };
+    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const P2Item p = p2_item(a, item);
+        const int nkv0 = p.t[0].nkv, nkv1 = p.t[1].nkv;
+        if (!wait(bb.qfull[0], qc[0] & 1)) break;
+        ++qc[0];
+        if (nkv1 > 0) {
+            if (!wait(bb.qfull[1], qc[1] & 1)) break;
+            ++qc[1];
+        }
+        {   // S0(0), S1(0)
+            const int ks = kc % P2_RK;
+            if (!wait(bb.kfull[ks], (kc / P2_RK) & 1)) break;
+            tc_fence_after_sync();
+            issue_s(0, ks);
+            if (nkv1 > 0) issue_s(1, ks);
+            umma_commit(bb.kempty[ks]);
+            ++kc;
+        }
+        for (int n = 0; n < nkv0 && ok; ++n) {
+            const int vs = vc % P2_RV;
+            const int ks = kc % P2_RK;                 // K tile n + 1
+            const bool more0 = n + 1 < nkv0, more1 = n + 1 < nkv1;
+            if (!wait(bb.pfull[0], pc[0] & 1)) break;
+            ++pc[0];
+            if (!wait(bb.vfull[vs], (vc / P2_RV) & 1)) break;
+            tc_fence_after_sync();
+            issue_pv(0, vs, n);
+            if (more0) {
+                if (!wait(bb.kfull[ks], (kc / P2_RK) & 1)) break;
+                tc_fence_after_sync();
+                issue_s(0, ks);
+            }
+            if (n < nkv1) {
+                if (!wait(bb.pfull[1], pc[1] & 1)) break;
+                ++pc[1];
+                tc_fence_after_sync();
+                issue_pv(1, vs, n);
+                if (more1) issue_s(1, ks);             // more1 implies more0: K tile n + 1 is in
+            }
+            umma_commit(bb.vempty[vs]);
+            ++vc;
+            if (more0) {
+                umma_commit(bb.kempty[ks]);
+                ++kc;
+            }
+        }
+    }
+}
+
+template <int KV>
+__device__ void p2_softmax(uint8_t *smem, const PrefillArgs &a, const P2Bars &bb, uint32_t tmem,
+                           volatile int *abort_flag, int total, int x) {
+    const int lane = threadIdx.x & 31;
+    const int quarter = (threadIdx.x >> 5) & 3;    // tensor-memory lanes 32 quarter .. + 31
+    const int m = quarter * 32 + lane;             // this thread's query row in its tile
+    const int tid = m;                             // 0 .. 127 within the tile's warpgroup
+    const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t scol = (uint32_t)(x * PN), ocol = (uint32_t)(TM2_O + x * PD);
+    uint8_t *qs = smem + P2_OFF_Q + x * Q_BYTES;
+    const float sl2 = a.scale_log2;
+    int sc = 0, pvc = 0, vcount = 0;   // S_x completed, PV_x issued, V tiles passed (tile 0 zeroes V)
+    bool ok = true;
+    auto wait = [&](uint32_t bar, uint32_t parity) {
+        if (!ok) return false;
+        const bool got = !*abort_flag && mbar_wait_bounded(bar, parity, a.wait_limit);
+        if (!__all_sync(0xffffffffu, got)) {
+            if (lane == 0) pf_error(a);
+            *abort_flag = 1;
+            ok = false;
+        }
+        return ok;
+    };
+    for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
+        const P2Item p = p2_item(a, item);
+        const PfTile &t = p.t[x];
+        if (t.nkv == 0) continue;                  // the pair has no tile 1
+        const int tok = m / a.G, hh = m - tok * a.G;
+        const bool valid = tok < t.ntok;
+        const long long qrow = ((long long)(t.q0 + t.row0 + tok) * a.Hq + t.kvh * a.G + hh) * PD;
+        // ---- Q row into shared memory in the 128-byte-swizzled K-major layout
+        // (zeros past the tile's new tokens); this tile's products of the
+        // previous item, which read Q, are done (its last PV was waited for)
+        {
+            const uint4 *src = reinterpret_cast<const uint4 *>(a.query + qrow);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4 *>(qs + (c >> 3) * (PM * 128) + m * 128 + (((c & 7) ^ (m & 7)) << 4)) = v;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bb.qfull[x]);
+        }
+        const int vis = valid ? t.C + t.row0 + tok : 1;   // positions this row sees
+        float mrun = -INFINITY, l = 0.f;
+        for (int n = 0; n < t.nkv && ok; ++n) {
+            if (!wait(bb.sfull[x], sc & 1)) break;
+            ++sc;
+            tc_fence_after_sync();
+            // ---- the row of S, whole, in registers
+            float s[PN];
+#pragma unroll
+            for (int q = 0; q < PN / 32; ++q) {
+                uint32_t r[32];
+                tmem_ld32(trow + scol + 32 * q, r);
+#pragma unroll
+                for (int c = 0; c < 32; ++c) s[32 * q + c] = __uint_as_float(r[c]);
+            }
+            tmem_wait_ld();
+            const int t0 = n * PN;
+            if (t0 + PN > vis) {   // the tile reaches past this row's position
+#pragma unroll
+                for (int c = 0; c < PN; ++c) s[c] = t0 + c < vis ? s[c] : -INFINITY;
+            }
+            // row maximum of the raw scores (scale > 0), eight partial maxima
+            float mp[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) mp[j] = s[j];
+#pragma unroll
+            for (int c = 8; c < PN; ++c) mp[c & 7] = fmaxf(mp[c & 7], s[c]);
+            const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                                   fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl2;
+            // rescale decided per row, run warp-wide (tensor-memory accesses are
+            // warp-collective); rows that do not grow scale by exactly 1
+            const bool grow = mx > mrun + RESCALE_THRESHOLD;
+            if (__any_sync(0xffffffffu, grow)) {
+                const float nm = grow ? fmaxf(mrun, mx) : mrun;
+                const float alpha = grow ? fast_exp2(mrun - nm) : 1.f;
+                if (n > 0) {   // PV_x(n - 1) is complete (S_x(n) was committed after it)
+#pragma unroll 1
+                    for (int c4 = 0; c4 < PD / 32; ++c4) {
+                        uint32_t o[32];
+                        tmem_ld32(trow + ocol + c4 * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tmem_st32(trow + ocol + c4 * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+                l *= alpha;
+                mrun = nm;
+            }
+            // ---- the sequence's last KV tile: V rows past the context are zeroed
+            // (P is 0 there, but the slots may hold anything); tile 0 runs every
+            // KV tile of the pair, and PV1(n) is issued after PV0(n)
+            bool zeroed = false;
+            if (x == 0) {
+                const int vs = vcount % P2_RV;
+                const int vphase = (vcount / P2_RV) & 1;
+                ++vcount;
+                if (t0 + PN > t.L) {
+                    if (!wait(bb.vfull[vs], vphase)) break;
+                    const int first = t.L - t0;
+                    uint8_t *vt = smem + P2_OFF_V + vs * KV_BYTES;
+                    for (int k = tid; k < 2 * PN * 8; k += 128) {
+                        const int h = k / (PN * 8), rr = (k / 8) % PN, cc = k % 8;
+                        if (rr >= first)
+                            *reinterpret_cast<uint4 *>(vt + h * (PN * 128) + rr * 128 + cc * 16) =
+                                make_uint4(0, 0, 0, 0);
+                    }
+                    zeroed = true;
+                }
+            }
+            // ---- p = 2^(s scale log2(e) - m), packed two per column over the
+            // first 64 columns of S (already read), and the row sum
+            float lp[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) lp[j] = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t r[32];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {   // tokens 64 h + 8 c .. + 7
+                    float pv[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        pv[j] = fast_exp2(fmaf(s[64 * h + 8 * c + j], sl2, -mrun));
+                        lp[j] += pv[j];
+                    }
+                    r[4 * c] = pack_p<KV>(pv[0], pv[1]);
+                    r[4 * c + 1] = pack_p<KV>(pv[2], pv[3]);
+                    r[4 * c + 2] = pack_p<KV>(pv[4], pv[5]);
+                    r[4 * c + 3] = pack_p<KV>(pv[6], pv[7]);
+                }
+                tmem_st32(trow + scol + 32 * h, r);
+            }
+            l += ((lp[0] + lp[1]) + (lp[2] + lp[3])) + ((lp[4] + lp[5]) + (lp[6] + lp[7]));
+            tmem_wait_st();
+            if (zeroed) fence_proxy_async_smem();   // the zeroed V rows, for the tensor cores
+            tc_fence_before_sync();
+            mbar_arrive(bb.pfull[x]);
+            ++pvc;
+        }
+        if (!ok) break;
+        // ---- epilogue: O / l once this tile's last PV is done
+        if (!wait(bb.pvdone[x], (pvc - 1) & 1)) break;
+        tc_fence_after_sync();
+        const bool bad = *pf_bad_slot(smem, P2_OFF_CTRL, pf_local(item)) == pf_local(item) + 1;
+        const float inv = bad ? __int_as_float(0x7fc00000) : a.v_scale / l;
+        uint16_t *orow = a.out + qrow;
+#pragma unroll 1
+        for (int c4 = 0; c4 < PD / 32; ++c4) {
+            uint32_t o[32];
+            tmem_ld32(trow + ocol + c4 * 32, o);
+            tmem_wait_ld();
+            if (valid) {
+#pragma unroll
+                for (int c = 0; c < 32; c += 8) {
+                    uint4 v;
+                    v.x = (uint32_t)out_bits<KV>(__uint_as_float(o[c]) * inv) |
+                          ((uint32_t)out_bits<KV>(__uint_as_float(o[c + 1]) * inv) << 16);
+                    v.y = (uint32_t)out_bits<KV>(__uint_as_float(o[c + 2]) * inv) |
+                          ((uint32_t)out_bits<KV>(__uint_as_float(o[c + 3]) * inv) << 16);
+                    v.z = (uint32_t)out_bits<KV>(__uint_as_float(o[c + 4]) * inv) |
+                          ((uint32_t)out_bits<KV>(__uint_as_float(o[c + 5]) * inv) << 16);
+                    v.w = (uint32_t)out_bits<KV>(__uint_as_float(o[c + 6]) * inv) |
+                          ((uint32_t)out_bits<KV>(__uint_as_float(o[c + 7]) * inv) << 16);
+                    *reinterpret_cast<uint4 *>(orow + c4 * 32 + c) = v;
+                }
+            }
+        }
+        tc_fence_before_sync();
+    }
+}
+
+template <int KV>
+__global__ void __launch_bounds__(P2_THREADS, 1) prefill2_kernel(const __grid_constant__ CUtensorMap tmk,
+                                                                  const __grid_constant__ CUtensorMap tmv,
+                                                                  const PrefillArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const P2Bars bb = p2_bars(smem);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + P2_OFF_CTRL + CTRL_ABORT);
+    const int warp = threadIdx.x >> 5;
+    const int total = *reinterpret_cast<volatile int *>(&a.hdr->pf2_items);   // written by the prep kernel
+    if ((int)blockIdx.x >= total) return;   // no work item for this CTA (the whole CTA leaves)
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < P2_RK; ++s) {
+            mbar_init(bb.kfull[s], 1);
+            mbar_init(bb.kempty[s], 1);
+        }
+        for (int s = 0; s < P2_RV; ++s) {
+            mbar_init(bb.vfull[s], 1);
+            mbar_init(bb.vempty[s], 1);
+        }
+        for (int x = 0; x < 2; ++x) {
+            mbar_init(bb.sfull[x], 1);
+            mbar_init(bb.pfull[x], 128);
+            mbar_init(bb.pvdone[x], 1);
+            mbar_init(bb.qfull[x], 128);
+        }
+        mbar_init(bb.flags, 1);            // all MMAs completed (before tensor memory is freed)
+        for (int k = 0; k < BAD_SLOTS; ++k) *pf_bad_slot(smem, P2_OFF_CTRL, k) = 0;
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 2) {   // this warp owns the tensor memory
+        tmem_alloc(bb.tmem_slot, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + (bb.tmem_slot - smem_u32(smem)));
+    // register split: the producer / MMA warpgroup gives registers to the two
+    // softmax warpgroups (128 x 104 + 256 x 200 = 384 x 168, the launch's pool)
+    if (warp >= 4) {
+        regs_increase<P2_REGS_HIGH>();
+        p2_softmax<KV>(smem, a, bb, tmem, abort_flag, total, (warp - 4) >> 2);
+    } else {
+        regs_decrease<P2_REGS_LOW>();
+        if (warp < 2) {
+            // both producers stream the pair's whole range: tile 0's, the longer one
+            auto range = [&](int item) {
+                const P2Item p = p2_item(a, item);
+                return PfRange{p.t[0].seq, p.t[0].kvh, p.t[0].nkv, p.t[0].L};
+            };
+            if (warp == 0) {
+                const int off[1] = {P2_OFF_K};
+                const uint32_t *full[1] = {bb.kfull};
+                const uint32_t *empty[1] = {bb.kempty};
+                const CUtensorMap *maps[1] = {&tmk};
+                pf_stream<P2_RK, false, 1>(smem, off, P2_OFF_CTRL, full, empty, maps, a, abort_flag, total, range);
+            } else {
+                const int off[1] = {P2_OFF_V};
+                const uint32_t *full[1] = {bb.vfull};
+                const uint32_t *empty[1] = {bb.vempty};
+                const CUtensorMap *maps[1] = {&tmv};
+                pf_stream<P2_RV, false, 1>(smem, off, P2_OFF_CTRL, full, empty, maps, a, abort_flag, total, range);
+            }
+        } else if (warp == 2) {
+            if ((threadIdx.x & 31) == 0) {
+                p2_mma<KV>(smem, a, bb, tmem, abort_flag, total);
+                // every MMA issued has completed before tensor memory is released
+                umma_commit(bb.flags);
+                mbar_wait_bounded(bb.flags, 0, WAIT_LIMIT);
+            }
+            __syncwarp();
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 2) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// One-time set-up of the two-tile kernel for a cache type: shared memory,
+// grid, and whether it may run at all.  The register split assumes the
+// kernel launches with P2_REGS_LAUNCH registers per thread; were it built with
+// another count, the warpgroups' shares would not match the pool and the
+// softmax warpgroups' register increase could wait forever -- then the kernel
+// is never launched and pairs go to the one-tile kernel instead.
+struct P2Setup {
+    int grid = 0;
+    bool usable = false;
+    cudaError_t err = cudaSuccess;
+};
+
+template <int KV>
+const P2Setup &prefill2_setup() {
+    static P2Setup su;
+    static std::once_flag once;
+    std::call_once(once, [] {   // one CTA per SM
+        su.err = cudaFuncSetAttribute(prefill2_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, P2_SMEM);
+        int dev = 0, sms = 0;
+        cudaFuncAttributes fa;
+        if (su.err == cudaSuccess) su.err = cudaGetDevice(&dev);
+        if (su.err == cudaSuccess) su.err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (su.err == cudaSuccess) su.err = cudaFuncGetAttributes(&fa, prefill2_kernel<KV>);
+        su.grid = sms;
+        su.usable = su.err == cudaSuccess && sms > 0 && fa.numRegs == P2_REGS_LAUNCH;
+    });
+    return su;
+}
+
+template <int KV>
+int launch_prefill2_kv(const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args, long long max_items,
+                       cudaStream_t st) {
+    const P2Setup &su = prefill2_setup<KV>();
+    if (su.err != cudaSuccess) return PA_ERR_CUDA;
+    if (!su.usable) return PA_ERR_UNSUPPORTED;
+    const int g = (int)(max_items < su.grid ? (max_items > 0 ? max_items : 1) : su.grid);
+    prefill2_kernel<KV><<<g, P2_THREADS, P2_SMEM, st>>>(tmk, tmv, args);
+    return cuda_status(cudaGetLastError());
 }
 
 template <int KV>
@@ -685,7 +1166,7 @@ int launch_prefill_kv(const CUtensorMap &tmk, const CUtensorMap &tmv, const Pref
     });
     if (init_err != cudaSuccess || grid <= 0) return PA_ERR_CUDA;
     const int g = (int)(max_items < grid ? (max_items > 0 ? max_items : 1) : grid);
-    prefill_kernel<KV><<<g, PF_THREADS, PfL<KV>::SMEM, st>>>(tmk, tmv, args);
+    prefill_kernel<KV><<<g, PfL<KV>::THREADS, PfL<KV>::SMEM, st>>>(tmk, tmv, args);
     return cuda_status(cudaGetLastError());
 }
 
@@ -696,6 +1177,19 @@ int launch_prefill(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const
     if (kv == PA_KV_BF16) return launch_prefill_kv<PA_KV_BF16>(tmk, tmv, args, max_items, st);
     if (kv == PA_KV_F16) return launch_prefill_kv<PA_KV_F16>(tmk, tmv, args, max_items, st);
     if (kv == PA_KV_FP8_E4M3) return launch_prefill_kv<PA_KV_FP8_E4M3>(tmk, tmv, args, max_items, st);
+    return PA_ERR_UNSUPPORTED;
+}
+
+bool prefill2_usable(int kv) {
+    if (kv == PA_KV_BF16) return prefill2_setup<PA_KV_BF16>().usable;
+    if (kv == PA_KV_F16) return prefill2_setup<PA_KV_F16>().usable;
+    return false;
+}
+
+int launch_prefill2(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
+                    long long max_items, cudaStream_t st) {
+    if (kv == PA_KV_BF16) return launch_prefill2_kv<PA_KV_BF16>(tmk, tmv, args, max_items, st);
+    if (kv == PA_KV_F16) return launch_prefill2_kv<PA_KV_F16>(tmk, tmv, args, max_items, st);
     return PA_ERR_UNSUPPORTED;
 }
 

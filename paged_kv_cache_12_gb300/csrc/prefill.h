@@ -10,13 +10,14 @@
 namespace pa {
 
 struct PrefillArgs {
-    uint16_t *out;                    // fp16 / bf16 [num_query_tokens][Hq][128]
+    uint16_t *out;                    // fp16 (bf16 for a bf16 cache) [num_query_tokens][Hq][128]
     const uint16_t *query;            // same layout
     const int32_t *block_tables;
     const int32_t *context_lens;
     const int32_t *query_start;
-    const int4 *tiles;                // {sequence, row tile, 0, 0}, longest first
-    WsHeader *hdr;                    // error word; pf_items = work items (tiles x Hkv)
+    const int4 *tiles;                // one-tile kernel: {sequence, row tile, 0, 0}, longest first
+    const int4 *pairs;                // two-tile kernel: {sequence, row tile, the tile before it or -1, 0}
+    WsHeader *hdr;                    // error word; pf_items / pf2_items = work items (entries x Hkv)
     int Hq, Hkv, G, bs, mbps;
     long long num_blocks;
     float scale_log2;                 // softmax scale (times the K scale of an FP8 cache) x log2(e)
@@ -32,10 +33,20 @@ struct PrefillArgs {
 constexpr int PF_ROWS = 128;
 constexpr int PF_MIN_ROWS = PA_PF_MIN_ROWS;
 
-// Launch the prefill kernel on `st` (fp16, bf16 or FP8 E4M3 caches, head_dim 128);
-// it reads its item count from the workspace header; max_items is a host
-// bound that trims the grid.  tmk / tmv: the caches' tensor maps.
+// Launch the one-tile prefill kernel on `st` (fp16, bf16 or FP8 E4M3 caches,
+// head_dim 128); it reads its item count from the workspace header; max_items
+// is a host bound that trims the grid.  tmk / tmv: the caches' tensor maps.
 int launch_prefill(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
                    long long max_items, cudaStream_t st);
+
+// Whether the two-tile kernel can run for this cache type (fp16 or bf16, and
+// built with the register count its register split assumes); checked once.
+bool prefill2_usable(int kv);
+
+// Launch the two-tile prefill kernel (fp16 or bf16 caches): each work item is
+// two neighbouring row tiles of one sequence and kv head, which share every
+// K/V tile the CTA loads.
+int launch_prefill2(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
+                    long long max_items, cudaStream_t st);
 
 }  // namespace pa

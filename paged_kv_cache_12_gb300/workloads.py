@@ -217,10 +217,11 @@ def custom(name="custom", seed=7, num_seqs=4, num_heads=4, num_kv_heads=2, head_
                     multi=bool(multi))
 
 
-def make(name: str, prompt_extra: int | None = None) -> Workload:
+def make(name: str, prompt_extra: int | None = None, spec_tokens: int = 4) -> Workload:
     """The named workload.  For cow16/cow32, ``prompt_extra`` = None draws the
     partial-tail variant's extra tokens r in 1..block-1 from the seed;
-    ``prompt_extra=0`` gives the whole-block 2048-token prompt."""
+    ``prompt_extra=0`` gives the whole-block 2048-token prompt.  For spec72b,
+    ``spec_tokens`` is the number of new (speculative) tokens per sequence."""
     k = WORKLOADS.index(name)
     seed = 1000 + k
     rl = _rng(seed, _S_LENGTHS)
@@ -258,7 +259,8 @@ def make(name: str, prompt_extra: int | None = None) -> Workload:
     if name == "spec72b":
         lens = np.full(100, 8192, dtype=np.int32)
         nb = _spare_pool(lens, 16, 100)
-        return Workload(name, seed, 100, 64, 8, 128, 16, nb, lens, lens - 4, _order(seed, nb), multi=True)
+        return Workload(name, seed, 100, 64, 8, 128, 16, nb, lens, lens - int(spec_tokens), _order(seed, nb),
+                        multi=True)
     if name == "chunked":
         u = rl.uniform(math.log(64), math.log(32768), size=64)
         lens = np.rint(np.exp(u)).astype(np.int32)

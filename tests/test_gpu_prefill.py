@@ -110,8 +110,10 @@ def test_several_items_per_cta_with_out_of_range_ids(kv):
     # persistent grid runs two or three, one behind the other; the producers
     # read ahead into the next item.  Three of every four sequences meet an
     # out-of-range block id: their rows are NaN, every other row is the oracle's.
+    # (Contexts short enough that the fp8 pool is the oracle's quantisation of
+    # N(0, 1) data, whose outputs the absolute bar is made for.)
     H, Hkv, bs = 64, 8, 16
-    lens = [600 + 37 * i for i in range(48)]
+    lens = [300 + 7 * i for i in range(48)]
     T = [4] * 48
     w, st, out, ref = run_case(H, Hkv, bs, kv, lens, T, seed=57 + kv)
     compare(as_f64(out, kv), ref, kv)

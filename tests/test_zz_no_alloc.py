@@ -60,15 +60,18 @@ def test_calls_in_a_row_match_pa_decode_bit_for_bit():
 
 
 def test_too_large_is_refused():
-    w = workloads.custom(seed=43, num_seqs=2, num_heads=8, num_kv_heads=1, head_dim=128, block_size=16,
-                         context_lens=[40, 40])
-    st = Step(w)
-    d = st.upload(torch)
+    # valid arguments (64 query / 8 KV heads) whose workspace would exceed the array
     need = pa.pa_decode_workspace_size(4096, 64, 8, 128, 32768)
     assert need > pa.PA_DECODE_STATIC_WS_BYTES
+    cache = torch.zeros((16, 8, 16, 128), dtype=torch.float16, device="cuda")
     big_q = torch.zeros((4096, 64, 128), dtype=torch.float16, device="cuda")
     big_t = torch.zeros((4096, 1), dtype=torch.int32, device="cuda")
     big_l = torch.zeros((4096,), dtype=torch.int32, device="cuda")
     with pytest.raises(pa.PAError) as e:
-        pa.pa_decode_static_ws(torch.empty_like(big_q), big_q, d["k"], d["v"], big_t, big_l, w.scale, 32768)
+        pa.pa_decode_static_ws(torch.empty_like(big_q), big_q, cache, cache, big_t, big_l, 0.088, 32768)
     assert e.value.code == pa.PA_ERR_WORKSPACE
+    # an unsupported shape is reported as pa_decode reports it, before the size
+    cache1 = torch.zeros((16, 1, 16, 128), dtype=torch.float16, device="cuda")
+    with pytest.raises(pa.PAError) as e:
+        pa.pa_decode_static_ws(torch.empty_like(big_q), big_q, cache1, cache1, big_t, big_l, 0.088, 32768)
+    assert e.value.code == pa.PA_ERR_UNSUPPORTED
