@@ -159,11 +159,11 @@ def causal_flops(w) -> int:
 
 def prefill_launch(w, kv_dtype) -> bool:
     """Whether a multi-token call also launches the tensor-core kernel for long
-    runs of new tokens (the library's rule: head_dim 128, G dividing 128, at
-    least 32 query rows in the call; PA_PREFILL=0 disables)."""
+    runs of new tokens (the library's rule: head_dim 128, G dividing 128, more
+    than 16 query rows in the call; PA_PREFILL=0 disables)."""
     G = w.num_heads // w.num_kv_heads
     return (multi_token(w) and os.environ.get("PA_PREFILL", "1")[:1] != "0" and w.head_dim == 128
-            and 128 % G == 0 and w.num_new_tokens * G >= 32)
+            and 128 % G == 0 and w.num_new_tokens * G >= 17)
 
 
 def kv_write_bytes(w, esz=2) -> int:
@@ -708,7 +708,10 @@ def run_ours(args):
             "value": round(job_tokens_per_s(world, B, args.steps, graph_ms), 2), "unit": "tokens/s",
             "ms_per_step": round(graph_ms / args.steps, 4),
             "note": "the whole step captured once in a CUDA Graph and replayed"},
-        "gpu_launches": args.steps * layers * (3 + (1 if has_pairs else 0) + (1 if prefill_launch(w, kvd) else 0)),
+        # per layer: KV write, prep, decode pipeline, block copy (if pairs), the
+        # tensor-core kernels (one-tile, and two-tile for 16-bit caches)
+        "gpu_launches": args.steps * layers * (3 + (1 if has_pairs else 0) +
+                                               ((1 + (kvd != "fp8")) if prefill_launch(w, kvd) else 0)),
         "alloc_us_per_step": round(alloc_us, 1),
         "clocks": clk.summary(),
     }

@@ -236,14 +236,20 @@ PA_API size_t pa_attention_causal_workspace_size(int num_seqs, int num_query_tok
  *                  <= query_start[num_seqs] = num_query_tokens (T = 0 allowed)
  *   num_query_tokens  host-side row count of query and out
  *   other arguments as in pa_decode.
- * Two kernels share the work.  A sequence with at least 32 query rows
- * (T x G) -- a prompt chunk, or a few speculative tokens at a large G -- is
- * computed on the 5th-generation tensor cores in tiles of 128 query rows
+ * Two kinds of kernel share the work.  A sequence with more than 16 query
+ * rows (T x G) -- a prompt chunk, or a few speculative tokens at a large G --
+ * is computed on the 5th-generation tensor cores in tiles of 128 query rows
  * (128 / G new tokens x the G heads of a kv head), each K/V tile read once
  * per tile (head_dim 128, any cache type, G dividing 128; PA_PREFILL=0 in
  * the environment turns this off).  Other sequences take the decode
  * pipeline, which reduces up to 16 / G new tokens of a sequence together, so
- * a KV tile is read once for that many tokens' query rows.  Device-side cases: a
+ * a KV tile is read once for that many tokens' query rows.  In a call that
+ * may send rows to the tensor cores (head_dim 128, G dividing 128, more than
+ * 16 query rows in the call), the decode pipeline runs on a stream of the
+ * library's own beside the tensor-core kernels (forked from `stream` and joined back into it with
+ * events; the first such call on a device creates that stream and its events,
+ * so make it before any stream capture; PA_PREFILL_SIDE=0 keeps all work on
+ * `stream`).  Device-side cases: a
  * sequence with T > L or an invalid L (as in pa_decode) gets NaN rows; a
  * query_start that is not a non-decreasing cover of [0, num_query_tokens)
  * makes every row NaN.  num_query_tokens = 0 launches nothing.  Workspace:

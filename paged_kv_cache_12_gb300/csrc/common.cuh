@@ -29,6 +29,14 @@ __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Consecutive mbarriers, 8 bytes apart in shared memory, addressed by index
+// arithmetic: an array of their addresses indexed at run time would live in
+// local memory and cost a load before every wait or arrival.
+struct BarRing {
+    uint32_t base;
+    __device__ __forceinline__ uint32_t operator[](int i) const { return base + 8u * (uint32_t)i; }
+};
+
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }

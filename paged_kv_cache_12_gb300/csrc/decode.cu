@@ -517,6 +517,46 @@ bool prefill_pairs_enabled() {
     return on;
 }
 
+// ------------------------- the decode pipeline beside the tensor-core kernels
+
+// A multi-token call with both kinds of sequence runs the decode pipeline (an
+// HBM-bound kernel) on a second stream beside the tensor-core kernels (bound
+// by the tensor cores and L2), forked from and joined back into the caller's
+// stream with events.  The tensor-core kernels are launched first and take
+// one SM each; the decode pipeline's CTAs take the SMs their last round leaves
+// idle instead of waiting for all of them.  One stream and two events per
+// device, created by the first such call on the device (before any stream
+// capture); a mutex keeps each call's record / wait pairs together when
+// several host threads call at once.  PA_PREFILL_SIDE=0 (read once) keeps
+// everything on the caller's stream.
+struct Side {
+    std::mutex mu;
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+    bool ok = false, tried = false;
+};
+
+constexpr int MAX_SIDE_DEVICES = 64;
+
+Side *side_of(int dev) {
+    static std::mutex mu;
+    static Side sides[MAX_SIDE_DEVICES];
+    static const bool on = [] {
+        const char *e = std::getenv("PA_PREFILL_SIDE");
+        return !(e && e[0] == '0');
+    }();
+    if (!on || dev < 0 || dev >= MAX_SIDE_DEVICES) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    Side &sd = sides[dev];
+    if (!sd.tried) {
+        sd.tried = true;
+        sd.ok = cudaStreamCreateWithFlags(&sd.stream, cudaStreamNonBlocking) == cudaSuccess &&
+                cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming) == cudaSuccess &&
+                cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming) == cudaSuccess;
+    }
+    return sd.ok ? &sd : nullptr;
+}
+
 // Checks of the cache element type and its scales; 0 when valid.
 int check_kv(int kv, int head_dim, float k_scale, float v_scale) {
     if (kv != PA_KV_F16 && kv != PA_KV_BF16 && kv != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
@@ -782,8 +822,7 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     args.ws_ml = reinterpret_cast<float2 *>(ws + L.ml);
     args.ws_o = reinterpret_cast<float *>(ws + L.o);
     const long long max_items = L.item_cap * num_kv_heads;
-    const int rc = launch_kv_any(kv, head_dim, PA_CAUSAL_NT, true, tmk, tmv, args, max_items, st);
-    if (rc != PA_OK || !pf) return rc;
+    if (!pf) return launch_kv_any(kv, head_dim, PA_CAUSAL_NT, true, tmk, tmv, args, max_items, st);
     PrefillArgs pa_;
     pa_.out = hout;
     pa_.query = query;
@@ -802,12 +841,31 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     pa_.scale_log2 = args.scale_log2;   // with the K scale of an FP8 cache
     pa_.v_scale = args.v_scale;
     pa_.wait_limit = wait_limit_cycles();
-    if (pairs) {
-        // pairs first (the long chunks), then the sequences of one row tile
-        const int rc2 = launch_prefill2(kv, tmk, tmv, pa_, (L.ptile_cap + 1) / 2 * num_kv_heads, st);
-        if (rc2 != PA_OK) return rc2;
+    // the tensor-core kernels on `on`: pairs first (the long chunks), then the
+    // sequences of one row tile
+    auto tensor_core = [&](cudaStream_t on) {
+        if (pairs) {
+            const int rc2 = launch_prefill2(kv, tmk, tmv, pa_, (L.ptile_cap + 1) / 2 * num_kv_heads, on);
+            if (rc2 != PA_OK) return rc2;
+        }
+        return launch_prefill(kv, tmk, tmv, pa_, L.ptile_cap * num_kv_heads, on);
+    };
+    int dev = -1;
+    Side *side = cudaGetDevice(&dev) == cudaSuccess ? side_of(dev) : nullptr;
+    if (!side) {   // one stream: the decode pipeline, then the tensor-core kernels
+        const int rc = launch_kv_any(kv, head_dim, PA_CAUSAL_NT, true, tmk, tmv, args, max_items, st);
+        return rc != PA_OK ? rc : tensor_core(st);
     }
-    return launch_prefill(kv, tmk, tmv, pa_, L.ptile_cap * num_kv_heads, st);
+    std::lock_guard<std::mutex> lock(side->mu);
+    if (cudaEventRecord(side->fork, st) != cudaSuccess) return PA_ERR_CUDA;   // after the prep kernel
+    int rc = tensor_core(st);
+    if (rc != PA_OK) return rc;
+    if (cudaStreamWaitEvent(side->stream, side->fork, 0) != cudaSuccess) return PA_ERR_CUDA;
+    rc = launch_kv_any(kv, head_dim, PA_CAUSAL_NT, true, tmk, tmv, args, max_items, side->stream);
+    if (cudaEventRecord(side->join, side->stream) != cudaSuccess ||
+        cudaStreamWaitEvent(st, side->join, 0) != cudaSuccess)
+        return PA_ERR_CUDA;
+    return rc;
 }
 
 }  // namespace

@@ -106,32 +106,20 @@ struct PfBars {
     // ahead of another never adds its arrival to the other step's phase
     // k8full / v8full: FP8 codes staged (TMA bytes landed); k8empty / v8empty:
     // the staged codes converted (the staging slot may be refilled)
-    uint32_t kfull[MAXST], kempty[MAXST], vfull[MAXST], vempty[MAXST], k8full[MAXST], v8full[MAXST];
-    uint32_t k8empty[MAXST], v8empty[MAXST];
-    uint32_t sfull[2], sfree[2], pfull[2], pvdone[2], qfull;
-    uint32_t tmem_slot, flags;   // shared addresses
+    BarRing kfull, kempty, vfull, vempty, k8full, v8full, k8empty, v8empty;   // MAXST each
+    BarRing sfull, sfree, pfull, pvdone;                                      // 2 each
+    uint32_t qfull, tmem_slot, flags;   // shared addresses
 };
 
 __device__ __forceinline__ PfBars pf_bars(uint8_t *smem, int off_ctrl) {
-    const uint32_t c = smem_u32(smem + off_ctrl);
+    uint32_t a = smem_u32(smem + off_ctrl);
     PfBars b;
-    uint32_t a = c;
-    for (int s = 0; s < MAXST; ++s) b.kfull[s] = a, a += 8;
-    for (int s = 0; s < MAXST; ++s) b.kempty[s] = a, a += 8;
-    for (int s = 0; s < MAXST; ++s) b.vfull[s] = a, a += 8;
-    for (int s = 0; s < MAXST; ++s) b.vempty[s] = a, a += 8;
-    for (int s = 0; s < MAXST; ++s) b.k8full[s] = a, a += 8;
-    for (int s = 0; s < MAXST; ++s) b.v8full[s] = a, a += 8;
-    for (int s = 0; s < MAXST; ++s) b.k8empty[s] = a, a += 8;
-    for (int s = 0; s < MAXST; ++s) b.v8empty[s] = a, a += 8;
-    b.sfull[0] = a, a += 8;
-    b.sfull[1] = a, a += 8;
-    b.sfree[0] = a, a += 8;
-    b.sfree[1] = a, a += 8;
-    b.pfull[0] = a, a += 8;
-    b.pfull[1] = a, a += 8;
-    b.pvdone[0] = a, a += 8;
-    b.pvdone[1] = a, a += 8;
+    BarRing *rings[8] = {&b.kfull, &b.kempty, &b.vfull, &b.vempty, &b.k8full, &b.v8full, &b.k8empty, &b.v8empty};
+    for (int r = 0; r < 8; ++r) rings[r]->base = a, a += 8 * MAXST;
+    b.sfull.base = a, a += 16;
+    b.sfree.base = a, a += 16;
+    b.pfull.base = a, a += 16;
+    b.pvdone.base = a, a += 16;
     b.qfull = a, a += 8;
     b.tmem_slot = a, a += 8;
     b.flags = a;   // barriers and slots end at byte 8 (8 MAXST + 11) + 8 = 288 <= CTRL_BAD
@@ -188,9 +176,9 @@ __device__ __forceinline__ volatile int *pf_bad_slot(uint8_t *smem, int off_ctrl
 // and empty[].  A 16-bit tile is two 64-column boxes per row group; an FP8
 // tile (F8: codes for a staging ring) one 128-byte box per row group.
 template <int PST, bool F8, int NMAP, class RangeOf>
-__device__ void pf_stream(uint8_t *smem, const int *off_ring, int off_ctrl, const uint32_t *const *full,
-                          const uint32_t *const *empty, const CUtensorMap *const *map, const PrefillArgs &a,
-                          volatile int *abort_flag, int total, RangeOf range) {
+__device__ void pf_stream(uint8_t *smem, const int *off_ring, int off_ctrl, const BarRing *full, const BarRing *empty,
+                          const CUtensorMap *const *map, const PrefillArgs &a, volatile int *abort_flag, int total,
+                          RangeOf range) {
     constexpr int TILE = F8 ? F8_BYTES : KV_BYTES;
     constexpr int NBOX = F8 ? 1 : 2;
     const int lane = threadIdx.x & 31;
@@ -256,8 +244,8 @@ __device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const Prefill
                             volatile int *abort_flag, int total, int kv) {
     using L = PfL<KV>;
     const int off[1] = {kv ? L::OFF_V : L::OFF_K};
-    const uint32_t *full[1] = {kv ? bb.vfull : bb.kfull};
-    const uint32_t *empty[1] = {kv ? bb.vempty : bb.kempty};
+    const BarRing full[1] = {kv ? bb.vfull : bb.kfull};
+    const BarRing empty[1] = {kv ? bb.vempty : bb.kempty};
     const CUtensorMap *maps[1] = {map};
     pf_stream<L::R, false, 1>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total, [&](int item) {
                         const PfTile t = pf_tile(a, item);
@@ -281,10 +269,10 @@ __device__ void pf_convert_fp8(uint8_t *smem, const PrefillArgs &a, const PfBars
     const int lane = threadIdx.x & 31;
     const uint8_t *stage_p = smem + (kv ? L::OFF_V8 : L::OFF_K8);
     uint8_t *ring = smem + (kv ? L::OFF_V : L::OFF_K);
-    const uint32_t *full8 = kv ? bb.v8full : bb.k8full;
-    const uint32_t *empty8 = kv ? bb.v8empty : bb.k8empty;
-    const uint32_t *full = kv ? bb.vfull : bb.kfull;
-    const uint32_t *empty = kv ? bb.vempty : bb.kempty;
+    const BarRing full8 = kv ? bb.v8full : bb.k8full;
+    const BarRing empty8 = kv ? bb.v8empty : bb.k8empty;
+    const BarRing full = kv ? bb.vfull : bb.kfull;
+    const BarRing empty = kv ? bb.vempty : bb.kempty;
     int conv = 0;
     for (int item = blockIdx.x; item < total; item += gridDim.x) {
         const int nkv = pf_tile(a, item).nkv;
@@ -300,18 +288,24 @@ __device__ void pf_convert_fp8(uint8_t *smem, const PrefillArgs &a, const PfBars
             }
             const uint8_t *src = stage_p + s8 * F8_BYTES;
             uint8_t *dst = ring + c * KV_BYTES;
+            // lane: row r, code chunk j; its fp16 chunks 2 (j % 4) (dims 0-7 of
+            // the chunk) and 2 (j % 4) + 1 (dims 8-15) go to the 64-dim half
+            // j / 4.  Lanes of the second half store the odd chunk first, so
+            // each group of 8 lanes (one row) stores to 8 distinct 16-byte bank
+            // groups in either store (the halves are 16 KB apart: same banks).
+            const int j = lane & 7, h = j >> 2, c0 = 2 * (j & 3);
 #pragma unroll 4
             for (int i = 0; i < PN / 4; ++i) {   // 4 rows x 8 code chunks per pass
-                const int r = 4 * i + (lane >> 3), j = lane & 7;
+                const int r = 4 * i + (lane >> 3);
                 const uint4 x = *reinterpret_cast<const uint4 *>(src + r * 128 + ((j ^ (r & 7)) << 4));
-                const uint4 lo = make_uint4(e4m3x2_lo_to_f16x2(x.x), e4m3x2_hi_to_f16x2(x.x),
-                                            e4m3x2_lo_to_f16x2(x.y), e4m3x2_hi_to_f16x2(x.y));
-                const uint4 hi = make_uint4(e4m3x2_lo_to_f16x2(x.z), e4m3x2_hi_to_f16x2(x.z),
-                                            e4m3x2_lo_to_f16x2(x.w), e4m3x2_hi_to_f16x2(x.w));
-                uint8_t *row = dst + (j >> 2) * (PN * 128) + r * 128;
-                const int c0 = 2 * (j & 3);
-                *reinterpret_cast<uint4 *>(row + ((c0 ^ (r & 7)) << 4)) = lo;
-                *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (r & 7)) << 4)) = hi;
+                const uint32_t a0 = h ? x.z : x.x, a1 = h ? x.w : x.y, b0 = h ? x.x : x.z, b1 = h ? x.y : x.w;
+                const uint4 first = make_uint4(e4m3x2_lo_to_f16x2(a0), e4m3x2_hi_to_f16x2(a0),
+                                               e4m3x2_lo_to_f16x2(a1), e4m3x2_hi_to_f16x2(a1));
+                const uint4 second = make_uint4(e4m3x2_lo_to_f16x2(b0), e4m3x2_hi_to_f16x2(b0),
+                                                e4m3x2_lo_to_f16x2(b1), e4m3x2_hi_to_f16x2(b1));
+                uint8_t *row = dst + h * (PN * 128) + r * 128;
+                *reinterpret_cast<uint4 *>(row + (((c0 + h) ^ (r & 7)) << 4)) = first;
+                *reinterpret_cast<uint4 *>(row + (((c0 + 1 - h) ^ (r & 7)) << 4)) = second;
             }
             // the tile, written through the generic proxy, is for the tensor
             // cores, and the staged codes were read before the slot is refilled
@@ -667,8 +661,8 @@ __global__ void __launch_bounds__(PfL<KV>::THREADS, 1) prefill_kernel(const __gr
         pf_softmax<KV>(smem, a, bb, tmem, abort_flag, total);
     } else if constexpr (L::F8) {   // warp 7: the codes of K and V into the staging rings
         const int off[2] = {L::OFF_K8, L::OFF_V8};
-        const uint32_t *full[2] = {bb.k8full, bb.v8full};
-        const uint32_t *empty[2] = {bb.k8empty, bb.v8empty};
+        const BarRing full[2] = {bb.k8full, bb.v8full};
+        const BarRing empty[2] = {bb.k8empty, bb.v8empty};
         const CUtensorMap *maps[2] = {&tmk, &tmv};
         pf_stream<L::S8, true, 2>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total, [&](int item) {
             const PfTile t = pf_tile(a, item);
@@ -720,8 +714,8 @@ static_assert(P2_SMEM <= 227 * 1024, "shared memory of one CTA");
 static_assert(TM2_O + 2 * PD <= TMEM_COLS && PN == 128, "tensor-memory columns of the two-tile kernel");
 
 struct P2Bars {
-    uint32_t kfull[P2_RK], kempty[P2_RK], vfull[P2_RV], vempty[P2_RV];
-    uint32_t sfull[2], pfull[2], pvdone[2], qfull[2];   // per tile
+    BarRing kfull, kempty, vfull, vempty;   // P2_RK / P2_RV stages
+    BarRing sfull, pfull, pvdone, qfull;    // per tile
     uint32_t tmem_slot, flags;
 };
 static_assert(8 * (2 * P2_RK + 2 * P2_RV + 8 + 2) <= CTRL_BAD, "control block layout of the two-tile kernel");
@@ -729,14 +723,14 @@ static_assert(8 * (2 * P2_RK + 2 * P2_RV + 8 + 2) <= CTRL_BAD, "control block la
 __device__ __forceinline__ P2Bars p2_bars(uint8_t *smem) {
     uint32_t a = smem_u32(smem + P2_OFF_CTRL);
     P2Bars b;
-    for (int s = 0; s < P2_RK; ++s) b.kfull[s] = a, a += 8;
-    for (int s = 0; s < P2_RK; ++s) b.kempty[s] = a, a += 8;
-    for (int s = 0; s < P2_RV; ++s) b.vfull[s] = a, a += 8;
-    for (int s = 0; s < P2_RV; ++s) b.vempty[s] = a, a += 8;
-    for (int x = 0; x < 2; ++x) b.sfull[x] = a, a += 8;
-    for (int x = 0; x < 2; ++x) b.pfull[x] = a, a += 8;
-    for (int x = 0; x < 2; ++x) b.pvdone[x] = a, a += 8;
-    for (int x = 0; x < 2; ++x) b.qfull[x] = a, a += 8;
+    b.kfull.base = a, a += 8 * P2_RK;
+    b.kempty.base = a, a += 8 * P2_RK;
+    b.vfull.base = a, a += 8 * P2_RV;
+    b.vempty.base = a, a += 8 * P2_RV;
+    b.sfull.base = a, a += 16;
+    b.pfull.base = a, a += 16;
+    b.pvdone.base = a, a += 16;
+    b.qfull.base = a, a += 16;
     b.tmem_slot = a, a += 8;
     b.flags = a;
     return b;
@@ -876,7 +870,7 @@ __device__ void p2_softmax(uint8_t *smem, const PrefillArgs &a, const P2Bars &bb
     };
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
         const P2Item p = p2_item(a, item);
-        const PfTile &t = p.t[x];
+        const PfTile t = x ? p.t[1] : p.t[0];      // (a run-time index would put the pair in local memory)
         if (t.nkv == 0) continue;                  // the pair has no tile 1
         const int tok = m / a.G, hh = m - tok * a.G;
         const bool valid = tok < t.ntok;
@@ -1081,14 +1075,14 @@ __global__ void __launch_bounds__(P2_THREADS, 1) prefill2_kernel(const __grid_co
             };
             if (warp == 0) {
                 const int off[1] = {P2_OFF_K};
-                const uint32_t *full[1] = {bb.kfull};
-                const uint32_t *empty[1] = {bb.kempty};
+                const BarRing full[1] = {bb.kfull};
+                const BarRing empty[1] = {bb.kempty};
                 const CUtensorMap *maps[1] = {&tmk};
                 pf_stream<P2_RK, false, 1>(smem, off, P2_OFF_CTRL, full, empty, maps, a, abort_flag, total, range);
             } else {
                 const int off[1] = {P2_OFF_V};
-                const uint32_t *full[1] = {bb.vfull};
-                const uint32_t *empty[1] = {bb.vempty};
+                const BarRing full[1] = {bb.vfull};
+                const BarRing empty[1] = {bb.vempty};
                 const CUtensorMap *maps[1] = {&tmv};
                 pf_stream<P2_RV, false, 1>(smem, off, P2_OFF_CTRL, full, empty, maps, a, abort_flag, total, range);
             }

@@ -1,5 +1,5 @@
 """The tensor-core kernel for long runs of new tokens (prompt chunks; deepsonar
-page section 2.5): a sequence whose new tokens x G reach 32 query rows is
+page section 2.5): a sequence whose new tokens x G exceed 16 query rows is
 computed in 128-row tiles with tcgen05 MMAs.  Results must be the oracle's
 causal attention within the decode tolerance, for every G that divides the
 tile, every block size, fp16, bf16 and FP8 E4M3 caches (FP8 codes are turned
