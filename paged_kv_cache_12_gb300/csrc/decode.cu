@@ -100,11 +100,11 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
     const int32_t *__restrict__ context_lens, const int32_t *__restrict__ lead,
     const int32_t *__restrict__ shared_len, int B, int Hq, int D, int Hkv, int bs, int max_ctx,
     long long max_table_tokens, int pt, int ms, WsHeader *hdr, int *part_off, int *gsize, int *gshared,
-    ItemRec *items, int *grp, uint16_t *out, uint32_t nan2) {
+    ItemRec *items, int *grp, uint16_t *out, uint32_t nan2, int mt, int4 *sitems) {
     constexpr int NBK = MAX_PART_TOKENS / CHUNK;     // length buckets of the short items
     __shared__ int warp_sums[PREP_THREADS / 32];
     __shared__ int hist[NBK], cursor[NBK];
-    int run_p = 0, run_f = 0;                        // uniform running totals
+    int run_p = 0, run_f = 0, run_s = 0;             // uniform running totals
     for (int k = threadIdx.x; k < NBK; k += PREP_THREADS) hist[k] = cursor[k] = 0;
     if (grp)
         for (long long k = threadIdx.x; k < (long long)B * Hkv; k += PREP_THREADS) grp[k] = 0;
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
                 for (int j = i; j < B && lead[j] == i; ++j, ++M) {
                     const int L = context_lens[j];
                     ok = ok && valid_len(L) && L > 0;
-                    S = min(S, ok ? L : 0);
+                    S = min(S, ok ? L - 1 : 0);   // every member keeps at least one token of its own
                 }
                 S = S / bs * bs;   // whole blocks only, also after capping by a member's context
                 if (!ok || M < 2) S = 0;
@@ -157,18 +157,26 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
                 if (ld == i && S > 0) {
                     Ms = gsize[i];
                     Ps = (S + pt - 1) / pt;
-                    nfull += (S / pt) * ((Ms + ms - 1) / ms);
+                    if (!mt) nfull += (S / pt) * ((Ms + ms - 1) / ms);
                 }
             }
         }
-        int tp, tf;
+        int tp, tf, ts;
         const int ep = run_p + block_exclusive_scan(P, warp_sums, &tp);
         int ef = run_f + block_exclusive_scan(nfull, warp_sums, &tf);
+        // shared ranges on the tensor cores: every partition of a leader's
+        // shared range, for up to mt members at a time
+        const int nsh = mt && Ps > 0 ? Ps * ((Ms + mt - 1) / mt) : 0;
+        int es = run_s + block_exclusive_scan(nsh, warp_sums, &ts);
         if (i < B) {
             part_off[i] = ep;
             if (P > 0) {
                 const int ps_i = (S + pt - 1) / pt;
-                if (Ps > 0) {   // leader: full shared items
+                if (Ps > 0 && mt) {   // leader: its shared ranges, for the tensor-core kernel
+                    for (int p = 0; p < Ps; ++p)
+                        for (int k = 0; k < Ms; k += mt)
+                            sitems[es++] = make_int4(i + k, min(mt, Ms - k), p * pt, min((p + 1) * pt, S));
+                } else if (Ps > 0) {   // leader: full shared items
                     for (int p = 0; p < S / pt; ++p)
                         for (int k = 0; k < Ms; k += ms) {
                             ItemRec r;
@@ -196,6 +204,7 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
         }
         run_p += tp;
         run_f += tf;
+        run_s += ts;
     }
     __syncthreads();
     int total_items = run_f;
@@ -214,7 +223,7 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
         int ld;
         const int S = shared_of(i, ld);
         const int ps_i = (S + pt - 1) / pt;
-        if (ld == i && S > 0 && S % pt) {
+        if (!mt && ld == i && S > 0 && S % pt) {
             const int Ms = gsize[i];
             for (int k = 0; k < Ms; k += ms) {
                 ItemRec r;
@@ -237,6 +246,7 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
         total_items = cursor[nbk - 1];
         part_off[B] = run_p;
         hdr->total_items = total_items * Hkv;
+        hdr->pf_items = run_s * Hkv;
         hdr->counter = 0;
         hdr->error = 0;
     }
@@ -557,6 +567,16 @@ Side *side_of(int dev) {
     return sd.ok ? &sd : nullptr;
 }
 
+// Whether a grouped decode reduces its shared ranges on the tensor cores
+// (unless PA_SHARED_TC=0, read once).
+bool shared_tc_enabled() {
+    static const bool on = [] {
+        const char *e = std::getenv("PA_SHARED_TC");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
 // Checks of the cache element type and its scales; 0 when valid.
 int check_kv(int kv, int head_dim, float k_scale, float v_scale) {
     if (kv != PA_KV_F16 && kv != PA_KV_BF16 && kv != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
@@ -665,10 +685,16 @@ int decode_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
         !cache_tensor_map(&tmv, v_cache, rows, head_dim, box_rows, kv))
         return PA_ERR_CUDA;
 
-    // query rows per item: one sequence's G heads, or, for a shared range,
-    // as many members' G heads as two head tiles hold
-    const int NT = (G > 8 || grouped) ? 2 : 1;
-    const int ms = grouped ? (16 / G > 1 ? 16 / G : 1) : 1;
+    // Shared ranges of a grouped call go to the tensor-core kernel (fp16 cache,
+    // head_dim 128, G dividing its 128-row tile), up to 128 / G members per
+    // item; the decode kernel then reduces each member's own partitions only.
+    const bool tc = grouped && kv == PA_KV_F16 && head_dim == 128 && PF_ROWS % G == 0 && prefill_enabled() &&
+                    shared_tc_enabled();
+    const int mt = tc ? PF_ROWS / G : 0;
+    // query rows per decode item: one sequence's G heads, or, for a shared
+    // range on this kernel, as many members' G heads as two head tiles hold
+    const int NT = (G > 8 || (grouped && !tc)) ? 2 : 1;
+    const int ms = grouped && !tc ? (16 / G > 1 ? 16 / G : 1) : 1;
 
     uint8_t *ws = static_cast<uint8_t *>(workspace);
     WsHeader *hdr = reinterpret_cast<WsHeader *>(ws);
@@ -682,11 +708,39 @@ int decode_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     float *ws_o = reinterpret_cast<float *>(ws + L.o);
     uint16_t *hout = out;
 
+    int4 *sitems = reinterpret_cast<int4 *>(ws + L.ptiles);
     decode_prep_kernel<<<1, PREP_THREADS, 0, st>>>(context_lens, lead, shared_len, num_seqs, num_heads, head_dim,
                                                    num_kv_heads, block_size, max_context_len,
                                                    (long long)max_blocks_per_seq * block_size, L.pt, ms, hdr,
-                                                   part_off, gsize, gshared, items, grp, hout, nan_pair(kv));
+                                                   part_off, gsize, gshared, items, grp, hout, nan_pair(kv), mt,
+                                                   sitems);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+    if (tc) {   // the shared ranges' partial rows, before the decode kernel merges them
+        PrefillArgs pa_{};
+        pa_.out = hout;
+        pa_.query = query;
+        pa_.block_tables = block_tables;
+        pa_.context_lens = context_lens;
+        pa_.query_start = nullptr;
+        pa_.tiles = sitems;
+        pa_.pairs = nullptr;
+        pa_.hdr = hdr;
+        pa_.Hq = num_heads;
+        pa_.Hkv = num_kv_heads;
+        pa_.G = G;
+        pa_.bs = block_size;
+        pa_.mbps = max_blocks_per_seq;
+        pa_.num_blocks = num_blocks;
+        pa_.scale_log2 = scale * 1.4426950408889634f;
+        pa_.v_scale = 1.f;
+        pa_.wait_limit = wait_limit_cycles();
+        pa_.part_off = part_off;
+        pa_.ws_ml = ws_ml;
+        pa_.ws_o = ws_o;
+        pa_.pt = L.pt;
+        const int rc = launch_shared_ranges(tmk, tmv, pa_, L.ptile_cap * num_kv_heads, st);
+        if (rc != PA_OK) return rc;
+    }
 
     DecodeArgs args;
     args.out = hout;
@@ -704,6 +758,7 @@ int decode_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     args.wait_limit = wait_limit_cycles();
     args.scale_log2 = scale * (kv == PA_KV_FP8_E4M3 ? k_scale : 1.f) * 1.4426950408889634f;
     args.v_scale = kv == PA_KV_FP8_E4M3 ? v_scale : 1.f;
+    args.tc_shared = tc ? 1 : 0;
     args.hdr = hdr;
     args.part_off = part_off;
     args.items = items;
@@ -815,6 +870,7 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     args.wait_limit = wait_limit_cycles();
     args.scale_log2 = scale * (kv == PA_KV_FP8_E4M3 ? k_scale : 1.f) * 1.4426950408889634f;
     args.v_scale = kv == PA_KV_FP8_E4M3 ? v_scale : 1.f;
+    args.tc_shared = 0;
     args.hdr = hdr;
     args.part_off = part_off;
     args.items = items;

@@ -117,6 +117,12 @@ inline WsLayout ws_layout(int B, int Hq, int Hkv, int D, int max_ctx, bool group
     if (multi) off += up256(sizeof(float2) * (size_t)parts * Hq);
     w.o = off;
     if (multi) off += up256(sizeof(float) * (size_t)parts * Hq * D);
+    // grouped calls: the list of shared ranges for the tensor-core kernel (at
+    // most one per leader, partition and member group: B x pmax)
+    w.ptile_cap = grouped ? (long long)B * w.pmax : 0;
+    w.ptiles = off;
+    off += up256(sizeof(int4) * (size_t)w.ptile_cap);
+    w.ppairs = off;
     w.total = off;
     return w;
 }
@@ -180,6 +186,7 @@ struct DecodeArgs {
     long long wait_limit;   // bound of every pipeline wait, clock cycles
     float scale_log2;        // softmax scale (times the K scale of an fp8 cache) * log2(e)
     float v_scale;           // V scale of an fp8 cache (1 otherwise)
+    int tc_shared;           // shared ranges were reduced by the tensor-core kernel before this one
     WsHeader *hdr;
     const int *part_off;
     const ItemRec *items;
@@ -611,9 +618,12 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
     // drained, so the fence is cheap) and inspected at that item's end (so the
     // atomics' latency is hidden); a lane holding a group's last ticket has
     // the warp merge that group.
+    // owe_T: tickets of the group (its partitions this kernel reduces: all P,
+    // or, when the tensor-core kernel already reduced the shared ranges, the
+    // member's own ones); the merge runs over all P partitions
     bool owe = false;
-    int owe_seq = 0, owe_kvh = 0, owe_P = 0;          // per lane: member lane
-    int pend_ticket = 0, pend_seq = 0, pend_kvh = 0, pend_P = 0;
+    int owe_seq = 0, owe_kvh = 0, owe_P = 0, owe_T = 0;   // per lane: member lane
+    int pend_ticket = 0, pend_seq = 0, pend_kvh = 0, pend_P = 0, pend_T = 0;
     auto take_ticket = [&]() {
         __syncwarp();
         __threadfence();
@@ -622,11 +632,12 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
         pend_seq = owe_seq;
         pend_kvh = owe_kvh;
         pend_P = owe_P;
+        pend_T = owe_T;
         owe = false;
         owe_P = 0;
     };
     auto settle = [&]() {
-        unsigned last = __ballot_sync(0xffffffffu, pend_P > 1 && pend_ticket == pend_P - 1);
+        unsigned last = __ballot_sync(0xffffffffu, pend_P > 1 && pend_ticket == pend_T - 1);
         if (last) __threadfence();
         while (last) {
             const int l0 = __ffs(last) - 1;
@@ -977,7 +988,9 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
         if (lane < dsc.nmem) {   // tickets owed for this item's members
             owe_seq = dsc.seq0 + lane;
             owe_kvh = dsc.kvh;
-            owe_P = dsc.canon0 < 0 ? partitions_of(__ldg(&a.context_lens[owe_seq]), dsc.shared, a.pt) : dsc.P0;
+            const int Lm = __ldg(&a.context_lens[owe_seq]);
+            owe_P = dsc.canon0 < 0 ? partitions_of(Lm, dsc.shared, a.pt) : dsc.P0;
+            owe_T = a.tc_shared ? (Lm - dsc.shared + a.pt - 1) / a.pt : owe_P;
         }
         owe = __any_sync(0xffffffffu, owe_P > 1);
     }

@@ -127,8 +127,16 @@ __device__ __forceinline__ PfBars pf_bars(uint8_t *smem, int off_ctrl) {
 }
 
 // Geometry of one work tile, the same in every warp.
+// Modes of the one-tile kernel: new tokens of a sequence attending causally
+// (their output rows), or the members of a shared-prefix group over a range
+// of their shared blocks (their partial rows, merged by the decode kernel).
+constexpr int PF_CAUSAL = 0, PF_SHARED = 1;
+
+// seq: the block-table row; tokens kv0 .. kv0 + L - 1 of it are the KV range,
+// nkv tiles of PN tokens; rows: ntok query tokens (or members) from query row
+// q0 + row0, G heads each; C: positions the first new token sees (causal).
 struct PfTile {
-    int seq, kvh, row0, ntok, C, nkv, L, q0;
+    int seq, kvh, row0, ntok, C, nkv, L, q0, kv0;
 };
 
 // Row tile `rt` (128 / G consecutive new tokens) of sequence `seq`, kv head kvh.
@@ -144,6 +152,7 @@ __device__ __forceinline__ PfTile pf_row_tile(const PrefillArgs &a, int seq, int
     t.ntok = min(tpt, T - t.row0);
     t.C = t.L - T + 1;                      // positions the first new token sees
     t.nkv = (t.C + t.row0 + t.ntok - 1 + PN - 1) / PN;
+    t.kv0 = 0;
     return t;
 }
 
@@ -153,9 +162,37 @@ __device__ __forceinline__ PfTile pf_tile(const PrefillArgs &a, int item) {
     return pf_row_tile(a, rec.x, item % a.Hkv, rec.y);
 }
 
-// What a producer warp needs of a work item: the KV range it streams.
+// Work item of the shared-prefix mode: (first member, members, shared range
+// [t0, t1)) x kv head.  The members' query rows (G heads each, member-major)
+// all see the whole range, read through the first member's table (the
+// members' first shared / block_size entries are the same blocks).
+__device__ __forceinline__ PfTile pf_shared_item(const PrefillArgs &a, int item) {
+    const int4 rec = a.tiles[item / a.Hkv];
+    PfTile t;
+    t.seq = rec.x;
+    t.kvh = item % a.Hkv;
+    t.q0 = rec.x;        // the members' query rows are rows rec.x ... of the decode query
+    t.row0 = 0;
+    t.ntok = rec.y;      // members
+    t.kv0 = rec.z;
+    t.L = rec.w - rec.z; // tokens of the range
+    t.C = t.L;
+    t.nkv = (t.L + PN - 1) / PN;
+    return t;
+}
+
+template <int MODE>
+__device__ __forceinline__ PfTile pf_item(const PrefillArgs &a, int item) {
+    if constexpr (MODE == PF_SHARED)
+        return pf_shared_item(a, item);
+    else
+        return pf_tile(a, item);
+}
+
+// What a producer warp needs of a work item: the KV range it streams, tokens
+// kv0 .. kv0 + L - 1 of table row seq.
 struct PfRange {
-    int seq, kvh, nkv, L;
+    int seq, kvh, nkv, L, kv0;
 };
 
 __device__ __forceinline__ void pf_error(const PrefillArgs &a) { atomicExch(&a.hdr->error, PA_ERR_TIMEOUT); }
@@ -199,9 +236,9 @@ __device__ void pf_stream(uint8_t *smem, const int *off_ring, int off_ctrl, cons
             // lane j owns box j of the tile (tokens t0 + j box_rows ..): its block id,
             // loaded before the wait so that the load's latency overlaps it
             const int t0 = n * PN;
-            const int tok = t0 + lane * box_rows;
+            const int tok = t0 + lane * box_rows;              // within the range
             const bool mine = lane < PN / box_rows && tok < t.L;
-            const int32_t blk = mine ? __ldg(row + tok / a.bs) : 0;
+            const int32_t blk = mine ? __ldg(row + (t.kv0 + tok) / a.bs) : 0;
             const int s = cnt % PST;
             // the warp decides together (no lane may leave alone)
             bool got = !*abort_flag;
@@ -224,7 +261,7 @@ __device__ void pf_stream(uint8_t *smem, const int *off_ring, int off_ctrl, cons
             }
             __syncwarp();
             if (!bad && mine) {
-                const int y = (int)(((long long)blk * a.Hkv + t.kvh) * a.bs) + tok % a.bs;
+                const int y = (int)(((long long)blk * a.Hkv + t.kvh) * a.bs) + (t.kv0 + tok) % a.bs;
 #pragma unroll
                 for (int r = 0; r < NMAP; ++r) {
                     const uint32_t dst = smem_u32(smem) + off_ring[r] + s * TILE + lane * box_rows * 128;
@@ -239,7 +276,7 @@ __device__ void pf_stream(uint8_t *smem, const int *off_ring, int off_ctrl, cons
     drain();
 }
 
-template <int KV>
+template <int KV, int MODE>
 __device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const PrefillArgs &a, const PfBars &bb,
                             volatile int *abort_flag, int total, int kv) {
     using L = PfL<KV>;
@@ -248,8 +285,8 @@ __device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const Prefill
     const BarRing empty[1] = {kv ? bb.vempty : bb.kempty};
     const CUtensorMap *maps[1] = {map};
     pf_stream<L::R, false, 1>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total, [&](int item) {
-                        const PfTile t = pf_tile(a, item);
-                        return PfRange{t.seq, t.kvh, t.nkv, t.L};
+                        const PfTile t = pf_item<MODE>(a, item);
+                        return PfRange{t.seq, t.kvh, t.nkv, t.L, t.kv0};
                     });
 }
 
@@ -321,7 +358,7 @@ __device__ void pf_convert_fp8(uint8_t *smem, const PrefillArgs &a, const PfBars
 
 // ----------------------------------------------------------- MMA issuer
 
-template <int KV>
+template <int KV, int MODE>
 __device__ void pf_mma(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, uint32_t tmem, bool bf16,
                        volatile int *abort_flag, int total) {
     using L = PfL<KV>;
@@ -368,7 +405,7 @@ __device__ void pf_mma(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, ui
         ++sc;
     };
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        const PfTile t = pf_tile(a, item);
+        const PfTile t = pf_item<MODE>(a, item);
         if (!wait(bb.qfull, qc & 1)) break;
         ++qc;
         issue_s();
@@ -394,7 +431,7 @@ __device__ void pf_mma(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, ui
 
 // ------------------------------------------------------------- softmax
 
-template <int KV>
+template <int KV, int MODE>
 __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, uint32_t tmem,
                            volatile int *abort_flag, int total) {
     using L = PfL<KV>;
@@ -423,34 +460,41 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
         }
         return ok;
     };
+    const int tok = m / a.G, hh = m - tok * a.G;   // new token (or member) and head of this row
+    // ---- an item's Q rows into this thread's lane of the tensor-memory A
+    // tile, two dims per column (zeros past the item's rows).  The next item's
+    // rows are stored as soon as this item's last PV is done (every product
+    // that read Q is then done too), before this item's epilogue, so that the
+    // next item's first S product overlaps the epilogue.
+    auto store_q = [&](const PfTile &tq) {
+        const bool v = tok < tq.ntok;
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            a.query + ((long long)(tq.q0 + tq.row0 + tok) * a.Hq + tq.kvh * a.G + hh) * PD);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t r[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const uint4 x = v ? __ldg(src + 8 * h + c) : make_uint4(0, 0, 0, 0);
+                r[4 * c] = x.x;
+                r[4 * c + 1] = x.y;
+                r[4 * c + 2] = x.z;
+                r[4 * c + 3] = x.w;
+            }
+            tmem_st32(trow + TM_Q + 32 * h, r);
+        }
+        tmem_wait_st();
+        tc_fence_before_sync();
+        mbar_arrive(bb.qfull);
+    };
+    if ((int)blockIdx.x < total) store_q(pf_item<MODE>(a, blockIdx.x));
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        const PfTile t = pf_tile(a, item);
-        const int tok = m / a.G, hh = m - tok * a.G;
+        const PfTile t = pf_item<MODE>(a, item);
         const bool valid = tok < t.ntok;
         const long long qrow = ((long long)(t.q0 + t.row0 + tok) * a.Hq + t.kvh * a.G + hh) * PD;
-        // ---- Q row into this thread's lane of the tensor-memory A tile, two
-        // dims per column (zeros past the new tokens); the previous tile's
-        // products, which read Q, are done (its last PV was waited for)
-        {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.query + qrow);
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t r[32];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint4 v = valid ? __ldg(src + 8 * h + c) : make_uint4(0, 0, 0, 0);
-                    r[4 * c] = v.x;
-                    r[4 * c + 1] = v.y;
-                    r[4 * c + 2] = v.z;
-                    r[4 * c + 3] = v.w;
-                }
-                tmem_st32(trow + TM_Q + 32 * h, r);
-            }
-            tmem_wait_st();
-            tc_fence_before_sync();
-            mbar_arrive(bb.qfull);
-        }
-        const int vis = valid ? t.C + t.row0 + tok : 1;   // positions this row sees
+        // positions of the range this row sees: causally up to its own new
+        // token, or (a shared range) all of them
+        const int vis = !valid ? 1 : MODE == PF_SHARED ? t.L : t.C + t.row0 + tok;
         float mrun = -INFINITY, l = 0.f;
         for (int n = 0; n < t.nkv && ok; ++n) {
             // ---- S row of this KV tile
@@ -566,10 +610,40 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
             ++g;
         }
         if (!ok) break;
-        // ---- epilogue: O / l once the tile's last PV (number g - 1) is done
+        // ---- epilogue: O / l once the tile's last PV (number g - 1) is done;
+        // the next item's Q first
         if (!wait(bb.pvdone[(g - 1) & 1], ((g - 1) >> 1) & 1)) break;
         tc_fence_after_sync();
+        if (item + (int)gridDim.x < total) store_q(pf_item<MODE>(a, item + gridDim.x));
         const bool bad = *pf_bad_slot(smem, OFF_CTRL, pf_local(item)) == pf_local(item) + 1;
+        if constexpr (MODE == PF_SHARED) {
+            // the member's partial row of this shared range: unnormalised O,
+            // and (m, l) -- the decode kernel's partial format -- at the
+            // canonical row part_off[member] + the range's partition index
+            const float qnan = __int_as_float(0x7fc00000);
+            const long long wrow = valid ? ((long long)a.part_off[t.q0 + tok] + t.kv0 / a.pt) * a.Hq +
+                                               t.kvh * a.G + hh
+                                         : 0;
+            float *prow = a.ws_o + wrow * PD;
+#pragma unroll 1
+            for (int c4 = 0; c4 < PD / 32; ++c4) {
+                uint32_t o[32];
+                tmem_ld32(trow + TM_O + c4 * 32, o);
+                tmem_wait_ld();
+                if (valid) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4 *>(prow + c4 * 32 + c) =
+                            bad ? make_float4(qnan, qnan, qnan, qnan)
+                                : make_float4(__uint_as_float(o[c]) * a.v_scale, __uint_as_float(o[c + 1]) * a.v_scale,
+                                              __uint_as_float(o[c + 2]) * a.v_scale,
+                                              __uint_as_float(o[c + 3]) * a.v_scale);
+                }
+            }
+            if (valid) a.ws_ml[wrow] = bad ? make_float2(qnan, qnan) : make_float2(mrun, l);
+            tc_fence_before_sync();
+            continue;
+        }
         const float inv = bad ? __int_as_float(0x7fc00000) : a.v_scale / l;
         uint16_t *orow = a.out + qrow;
 #pragma unroll 1
@@ -597,7 +671,7 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
     }
 }
 
-template <int KV>
+template <int KV, int MODE>
 __global__ void __launch_bounds__(PfL<KV>::THREADS, 1) prefill_kernel(const __grid_constant__ CUtensorMap tmk,
                                                                  const __grid_constant__ CUtensorMap tmv,
                                                                  const PrefillArgs a) {
@@ -648,17 +722,17 @@ __global__ void __launch_bounds__(PfL<KV>::THREADS, 1) prefill_kernel(const __gr
         if constexpr (L::F8)
             pf_convert_fp8(smem, a, bb, abort_flag, total, warp);
         else
-            pf_producer<KV>(smem, warp ? &tmv : &tmk, a, bb, abort_flag, total, warp);
+            pf_producer<KV, MODE>(smem, warp ? &tmv : &tmk, a, bb, abort_flag, total, warp);
     } else if (warp == 2) {
         if ((threadIdx.x & 31) == 0) {
-            pf_mma<KV>(smem, a, bb, tmem, KV == PA_KV_BF16, abort_flag, total);
+            pf_mma<KV, MODE>(smem, a, bb, tmem, KV == PA_KV_BF16, abort_flag, total);
             // every MMA issued has completed before tensor memory is released
             umma_commit(bb.flags);
             mbar_wait_bounded(bb.flags, 0, WAIT_LIMIT);
         }
         __syncwarp();
     } else if (warp < 7) {
-        pf_softmax<KV>(smem, a, bb, tmem, abort_flag, total);
+        pf_softmax<KV, MODE>(smem, a, bb, tmem, abort_flag, total);
     } else if constexpr (L::F8) {   // warp 7: the codes of K and V into the staging rings
         const int off[2] = {L::OFF_K8, L::OFF_V8};
         const BarRing full[2] = {bb.k8full, bb.v8full};
@@ -666,7 +740,7 @@ __global__ void __launch_bounds__(PfL<KV>::THREADS, 1) prefill_kernel(const __gr
         const CUtensorMap *maps[2] = {&tmk, &tmv};
         pf_stream<L::S8, true, 2>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total, [&](int item) {
             const PfTile t = pf_tile(a, item);
-            return PfRange{t.seq, t.kvh, t.nkv, t.L};
+            return PfRange{t.seq, t.kvh, t.nkv, t.L, t.kv0};
         });
     }
     tc_fence_before_sync();
@@ -868,26 +942,35 @@ __device__ void p2_softmax(uint8_t *smem, const PrefillArgs &a, const P2Bars &bb
         }
         return ok;
     };
+    const int tok = m / a.G, hh = m - tok * a.G;
+    // ---- an item's Q row into shared memory in the 128-byte-swizzled K-major
+    // layout (zeros past the tile's new tokens).  Stored for the next item as
+    // soon as this tile's last PV is done (every product that read Q_x is then
+    // done), before the epilogue, so that the next S_x overlaps the epilogue.
+    int q_item = -1;   // the item whose Q_x is in shared memory
+    auto tile_of = [&](int it) {
+        const P2Item p = p2_item(a, it);
+        return x ? p.t[1] : p.t[0];   // (a run-time index would put the pair in local memory)
+    };
+    auto store_q = [&](int it, const PfTile &tq) {
+        const bool v = tok < tq.ntok;
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            a.query + ((long long)(tq.q0 + tq.row0 + tok) * a.Hq + tq.kvh * a.G + hh) * PD);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+            const uint4 q = v ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4 *>(qs + (c >> 3) * (PM * 128) + m * 128 + (((c & 7) ^ (m & 7)) << 4)) = q;
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(bb.qfull[x]);
+        q_item = it;
+    };
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x) {
-        const P2Item p = p2_item(a, item);
-        const PfTile t = x ? p.t[1] : p.t[0];      // (a run-time index would put the pair in local memory)
+        const PfTile t = tile_of(item);
         if (t.nkv == 0) continue;                  // the pair has no tile 1
-        const int tok = m / a.G, hh = m - tok * a.G;
         const bool valid = tok < t.ntok;
         const long long qrow = ((long long)(t.q0 + t.row0 + tok) * a.Hq + t.kvh * a.G + hh) * PD;
-        // ---- Q row into shared memory in the 128-byte-swizzled K-major layout
-        // (zeros past the tile's new tokens); this tile's products of the
-        // previous item, which read Q, are done (its last PV was waited for)
-        {
-            const uint4 *src = reinterpret_cast<const uint4 *>(a.query + qrow);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint4 v = valid ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4 *>(qs + (c >> 3) * (PM * 128) + m * 128 + (((c & 7) ^ (m & 7)) << 4)) = v;
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(bb.qfull[x]);
-        }
+        if (q_item != item) store_q(item, t);
         const int vis = valid ? t.C + t.row0 + tok : 1;   // positions this row sees
         float mrun = -INFINITY, l = 0.f;
         for (int n = 0; n < t.nkv && ok; ++n) {
@@ -990,9 +1073,14 @@ __device__ void p2_softmax(uint8_t *smem, const PrefillArgs &a, const P2Bars &bb
             ++pvc;
         }
         if (!ok) break;
-        // ---- epilogue: O / l once this tile's last PV is done
+        // ---- epilogue: O / l once this tile's last PV is done; the next
+        // item's Q_x first, if it has this tile
         if (!wait(bb.pvdone[x], (pvc - 1) & 1)) break;
         tc_fence_after_sync();
+        if (item + (int)gridDim.x < total) {
+            const PfTile tn = tile_of(item + gridDim.x);
+            if (tn.nkv > 0) store_q(item + gridDim.x, tn);
+        }
         const bool bad = *pf_bad_slot(smem, P2_OFF_CTRL, pf_local(item)) == pf_local(item) + 1;
         const float inv = bad ? __int_as_float(0x7fc00000) : a.v_scale / l;
         uint16_t *orow = a.out + qrow;
@@ -1071,7 +1159,7 @@ __global__ void __launch_bounds__(P2_THREADS, 1) prefill2_kernel(const __grid_co
             // both producers stream the pair's whole range: tile 0's, the longer one
             auto range = [&](int item) {
                 const P2Item p = p2_item(a, item);
-                return PfRange{p.t[0].seq, p.t[0].kvh, p.t[0].nkv, p.t[0].L};
+                return PfRange{p.t[0].seq, p.t[0].kvh, p.t[0].nkv, p.t[0].L, 0};
             };
             if (warp == 0) {
                 const int off[1] = {P2_OFF_K};
@@ -1144,15 +1232,15 @@ int launch_prefill2_kv(const CUtensorMap &tmk, const CUtensorMap &tmv, const Pre
     return cuda_status(cudaGetLastError());
 }
 
-template <int KV>
+template <int KV, int MODE>
 int launch_prefill_kv(const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args, long long max_items,
                       cudaStream_t st) {
     static int grid = 0;
     static cudaError_t init_err = cudaSuccess;
     static std::once_flag once;
     std::call_once(once, [] {   // one CTA per SM
-        init_err =
-            cudaFuncSetAttribute(prefill_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, PfL<KV>::SMEM);
+        init_err = cudaFuncSetAttribute(prefill_kernel<KV, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        PfL<KV>::SMEM);
         int dev = 0, sms = 0;
         if (init_err == cudaSuccess) init_err = cudaGetDevice(&dev);
         if (init_err == cudaSuccess) init_err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1160,7 +1248,7 @@ int launch_prefill_kv(const CUtensorMap &tmk, const CUtensorMap &tmv, const Pref
     });
     if (init_err != cudaSuccess || grid <= 0) return PA_ERR_CUDA;
     const int g = (int)(max_items < grid ? (max_items > 0 ? max_items : 1) : grid);
-    prefill_kernel<KV><<<g, PfL<KV>::THREADS, PfL<KV>::SMEM, st>>>(tmk, tmv, args);
+    prefill_kernel<KV, MODE><<<g, PfL<KV>::THREADS, PfL<KV>::SMEM, st>>>(tmk, tmv, args);
     return cuda_status(cudaGetLastError());
 }
 
@@ -1168,10 +1256,15 @@ int launch_prefill_kv(const CUtensorMap &tmk, const CUtensorMap &tmv, const Pref
 
 int launch_prefill(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
                    long long max_items, cudaStream_t st) {
-    if (kv == PA_KV_BF16) return launch_prefill_kv<PA_KV_BF16>(tmk, tmv, args, max_items, st);
-    if (kv == PA_KV_F16) return launch_prefill_kv<PA_KV_F16>(tmk, tmv, args, max_items, st);
-    if (kv == PA_KV_FP8_E4M3) return launch_prefill_kv<PA_KV_FP8_E4M3>(tmk, tmv, args, max_items, st);
+    if (kv == PA_KV_BF16) return launch_prefill_kv<PA_KV_BF16, PF_CAUSAL>(tmk, tmv, args, max_items, st);
+    if (kv == PA_KV_F16) return launch_prefill_kv<PA_KV_F16, PF_CAUSAL>(tmk, tmv, args, max_items, st);
+    if (kv == PA_KV_FP8_E4M3) return launch_prefill_kv<PA_KV_FP8_E4M3, PF_CAUSAL>(tmk, tmv, args, max_items, st);
     return PA_ERR_UNSUPPORTED;
+}
+
+int launch_shared_ranges(const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
+                         long long max_items, cudaStream_t st) {
+    return launch_prefill_kv<PA_KV_F16, PF_SHARED>(tmk, tmv, args, max_items, st);
 }
 
 bool prefill2_usable(int kv) {

@@ -23,6 +23,12 @@ struct PrefillArgs {
     float scale_log2;                 // softmax scale (times the K scale of an FP8 cache) x log2(e)
     float v_scale;                    // V scale of an FP8 cache (1 otherwise)
     long long wait_limit;
+    // shared-prefix mode: tiles holds {first member, members, t0, t1} (t0 a
+    // multiple of pt), and partial rows go to the decode kernel's workspace
+    const int *part_off;
+    float2 *ws_ml;
+    float *ws_o;
+    int pt;
 };
 
 // Query rows per work tile, and the smallest number of query rows
@@ -41,6 +47,16 @@ constexpr int PF_MIN_ROWS = PA_PF_MIN_ROWS;
 // is a host bound that trims the grid.  tmk / tmv: the caches' tensor maps.
 int launch_prefill(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
                    long long max_items, cudaStream_t st);
+
+// Launch the one-tile kernel in its shared-prefix mode (fp16 cache, head_dim
+// 128): each work item is up to 128 / G members of a shared-prefix group over
+// one partition [t0, t1) of their shared blocks, all members' query rows in one
+// tile, each shared K/V tile read once for all of them.  It writes each
+// member's partial row (m, l, unnormalised O) of that partition; the decode
+// kernel, launched after it on the same stream, merges them with the
+// members' own partitions.  Item count: pf_items in the workspace header.
+int launch_shared_ranges(const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
+                         long long max_items, cudaStream_t st);
 
 // Whether the two-tile kernel can run for this cache type (fp16 or bf16, and
 // built with the register count its register split assumes); checked once.

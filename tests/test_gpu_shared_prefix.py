@@ -121,3 +121,20 @@ def test_member_outside_its_leaders_run_shares_nothing():
     leader[1] = 1
     out = run_shared(d, w, leader, shared)
     compare(out.cpu().numpy(), expect)
+
+
+def test_out_of_range_block_in_a_shared_range():
+    # an id past the pool in the shared blocks of the 12-member group (every
+    # member's table, as sharing requires): that group's rows are NaN, the
+    # other groups' rows are the oracle's
+    sizes = [3, 12, 5]
+    prefix = [900, 2100, 513]
+    w, d, leader, shared, expect = grouped(77, sizes, prefix, 32, 8, 128, 16)
+    bad = d["tables"].clone()
+    g0, g1 = 3, 15                            # members 3 .. 14
+    bad[g0:g1, 70] = w.num_blocks + 3        # positions 1120 .. 1135 of the 2100 shared
+    d["tables"] = bad
+    out = run_shared(d, w, leader, shared).cpu().numpy()
+    assert np.isnan(out[g0:g1]).all()
+    keep = np.r_[0:g0, g1:w.num_seqs]
+    compare(out[keep].astype(np.float64), expect[keep])
