@@ -842,7 +842,7 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     // sequences with many new tokens go to the tensor-core prefill kernel
     // (head_dim 128, G dividing the 128-row tile; FP8 codes become fp16 tiles on chip)
     const bool pf = prefill_enabled() && head_dim == 128 && PF_ROWS % G == 0 &&
-                    (long long)num_query_tokens * G >= PF_MIN_ROWS;
+                    (long long)num_query_tokens * G >= PF_MIN_ROWS && prefill_usable(kv);
     int4 *ptiles = reinterpret_cast<int4 *>(ws + L.ptiles);
     int4 *ppairs = reinterpret_cast<int4 *>(ws + L.ppairs);
     // sequences with several row tiles take them two at a time (16-bit caches)

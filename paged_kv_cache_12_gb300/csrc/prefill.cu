@@ -84,10 +84,14 @@ struct PfL {
     static constexpr int OFF_V8 = OFF_K8 + S8 * F8_BYTES;
     static constexpr int OFF_CTRL = OFF_V8 + S8 * F8_BYTES;
     static constexpr int SMEM = OFF_CTRL + CTRL_BYTES + 1024;   // + alignment slack
-    // K producer, V producer, MMA, 4 softmax warps; an FP8 cache adds the
-    // warp that issues the copies of the codes (warps 0 and 1 convert); 8
-    // warps at most keep two warps per SM sub-partition (registers)
-    static constexpr int THREADS = (F8 ? 8 : 7) * 32;
+    // 16-bit caches: warps 0 / 1 produce K / V, 2 issues the MMAs, 3-6 run
+    // the softmax.  FP8 caches: warp 0 issues the copies of the codes, 2 the
+    // MMAs, 4-7 run the softmax and 8-11 convert (two per cache, one on each
+    // SM sub-partition), with a register split (CONV_REGS / SOFT_REGS).
+    static constexpr int THREADS = (F8 ? 12 : 7) * 32;
+    static constexpr int SOFT_WARP0 = F8 ? 4 : 3;
+    static constexpr int SOFT_REGS = 232, CONV_REGS = 136, LAUNCH_REGS = 168;   // FP8: 65536 / 384 at launch
+    static_assert(!F8 || 128 * SOFT_REGS + 256 * CONV_REGS <= THREADS * LAUNCH_REGS, "register split");
     static_assert(R <= MAXST && S8 <= MAXST, "ring stages");
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
 };
@@ -290,9 +294,10 @@ __device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const Prefill
                     });
 }
 
-// FP8 cache: warp 7 streams the codes of the K and V tiles into 3-stage
-// staging rings (pf_stream, one 128-byte box column per block), and warps 0
-// and 1 turn each staged tile into the 16-bit tile the MMAs read, in the same
+// FP8 cache: warp 0 streams the codes of the K and V tiles into 3-stage
+// staging rings (pf_stream, one 128-byte box column per block), and two warps
+// per cache (each half of the rows) turn each staged tile into the 16-bit
+// tile the MMAs read, in the same
 // swizzled layout a 16-bit TMA copy would have written: code chunk j (dims
 // 16 j .. 16 j + 15) of row r becomes fp16 chunks 2 (j % 4) and 2 (j % 4) + 1
 // of the 64-dim block j / 4.  Every E4M3 value is an fp16 value, so the tile
@@ -300,7 +305,7 @@ __device__ void pf_producer(uint8_t *smem, const CUtensorMap *map, const Prefill
 // converting warp loads no block id and issues no copy, so it never waits on
 // memory latency except for the staged tile itself.
 __device__ void pf_convert_fp8(uint8_t *smem, const PrefillArgs &a, const PfBars &bb, volatile int *abort_flag,
-                               int total, int kv) {
+                               int total, int kv, int half) {
     using L = PfL<PA_KV_FP8_E4M3>;
     constexpr int R = L::R, S8 = L::S8;
     const int lane = threadIdx.x & 31;
@@ -332,7 +337,7 @@ __device__ void pf_convert_fp8(uint8_t *smem, const PrefillArgs &a, const PfBars
             // groups in either store (the halves are 16 KB apart: same banks).
             const int j = lane & 7, h = j >> 2, c0 = 2 * (j & 3);
 #pragma unroll 4
-            for (int i = 0; i < PN / 4; ++i) {   // 4 rows x 8 code chunks per pass
+            for (int i = half * (PN / 8); i < (half + 1) * (PN / 8); ++i) {   // this warp's half of the rows
                 const int r = 4 * i + (lane >> 3);
                 const uint4 x = *reinterpret_cast<const uint4 *>(src + r * 128 + ((j ^ (r & 7)) << 4));
                 const uint32_t a0 = h ? x.z : x.x, a1 = h ? x.w : x.y, b0 = h ? x.x : x.z, b1 = h ? x.y : x.w;
@@ -437,7 +442,7 @@ __device__ void pf_softmax(uint8_t *smem, const PrefillArgs &a, const PfBars &bb
     using L = PfL<KV>;
     constexpr int PST = L::R;
     constexpr int OFF_V = L::OFF_V, OFF_CTRL = L::OFF_CTRL;
-    const int tid = threadIdx.x - 96;             // 0 .. 127
+    const int tid = threadIdx.x - 32 * L::SOFT_WARP0;   // 0 .. 127
     const int lane = threadIdx.x & 31;
     const int quarter = (threadIdx.x >> 5) & 3;    // tensor-memory lanes 32 quarter .. + 31
     const int m = quarter * 32 + lane;             // this thread's query row in the tile
@@ -684,17 +689,18 @@ __global__ void __launch_bounds__(PfL<KV>::THREADS, 1) prefill_kernel(const __gr
     const int total = *reinterpret_cast<volatile int *>(&a.hdr->pf_items);   // written by the prep kernel
     if ((int)blockIdx.x >= total) return;   // no work item for this CTA (the whole CTA leaves)
     if (threadIdx.x == 0) {
+        constexpr uint32_t fill = L::F8 ? 2 : 1;   // FP8: two converting warps per ring
         for (int s = 0; s < L::R; ++s) {
-            mbar_init(bb.kfull[s], 1);
+            mbar_init(bb.kfull[s], fill);
             mbar_init(bb.kempty[s], 1);
-            mbar_init(bb.vfull[s], 1);
+            mbar_init(bb.vfull[s], fill);
             mbar_init(bb.vempty[s], 1);
         }
         for (int s = 0; s < L::S8; ++s) {
             mbar_init(bb.k8full[s], 1);
             mbar_init(bb.v8full[s], 1);
-            mbar_init(bb.k8empty[s], 1);
-            mbar_init(bb.v8empty[s], 1);
+            mbar_init(bb.k8empty[s], 2);
+            mbar_init(bb.v8empty[s], 2);
         }
         mbar_init(bb.sfull[0], 1);
         mbar_init(bb.sfull[1], 1);
@@ -718,12 +724,7 @@ __global__ void __launch_bounds__(PfL<KV>::THREADS, 1) prefill_kernel(const __gr
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + (bb.tmem_slot - smem_u32(smem)));
-    if (warp < 2) {
-        if constexpr (L::F8)
-            pf_convert_fp8(smem, a, bb, abort_flag, total, warp);
-        else
-            pf_producer<KV, MODE>(smem, warp ? &tmv : &tmk, a, bb, abort_flag, total, warp);
-    } else if (warp == 2) {
+    auto mma = [&]() {
         if ((threadIdx.x & 31) == 0) {
             pf_mma<KV, MODE>(smem, a, bb, tmem, KV == PA_KV_BF16, abort_flag, total);
             // every MMA issued has completed before tensor memory is released
@@ -731,17 +732,38 @@ __global__ void __launch_bounds__(PfL<KV>::THREADS, 1) prefill_kernel(const __gr
             mbar_wait_bounded(bb.flags, 0, WAIT_LIMIT);
         }
         __syncwarp();
-    } else if (warp < 7) {
-        pf_softmax<KV, MODE>(smem, a, bb, tmem, abort_flag, total);
-    } else if constexpr (L::F8) {   // warp 7: the codes of K and V into the staging rings
-        const int off[2] = {L::OFF_K8, L::OFF_V8};
-        const BarRing full[2] = {bb.k8full, bb.v8full};
-        const BarRing empty[2] = {bb.k8empty, bb.v8empty};
-        const CUtensorMap *maps[2] = {&tmk, &tmv};
-        pf_stream<L::S8, true, 2>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total, [&](int item) {
-            const PfTile t = pf_tile(a, item);
-            return PfRange{t.seq, t.kvh, t.nkv, t.L, t.kv0};
-        });
+    };
+    if constexpr (L::F8) {
+        // register split: the softmax warpgroup (warps 4-7) gets SOFT_REGS
+        // registers, the others CONV_REGS (the host checks the launch count)
+        if (warp >= 4 && warp < 8) {
+            regs_increase<L::SOFT_REGS>();
+            pf_softmax<KV, MODE>(smem, a, bb, tmem, abort_flag, total);
+        } else {
+            regs_decrease<L::CONV_REGS>();
+            if (warp == 0) {   // the codes of K and V into the staging rings
+                const int off[2] = {L::OFF_K8, L::OFF_V8};
+                const BarRing full[2] = {bb.k8full, bb.v8full};
+                const BarRing empty[2] = {bb.k8empty, bb.v8empty};
+                const CUtensorMap *maps[2] = {&tmk, &tmv};
+                pf_stream<L::S8, true, 2>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total,
+                                          [&](int item) {
+                                              const PfTile t = pf_tile(a, item);
+                                              return PfRange{t.seq, t.kvh, t.nkv, t.L, t.kv0};
+                                          });
+            } else if (warp == 2) {
+                mma();
+            } else if (warp >= 8) {   // 8, 9: K; 10, 11: V; each half of the rows
+                pf_convert_fp8(smem, a, bb, abort_flag, total, (warp - 8) >> 1, warp & 1);
+            }
+        }
+    } else {
+        if (warp < 2)
+            pf_producer<KV, MODE>(smem, warp ? &tmv : &tmk, a, bb, abort_flag, total, warp);
+        else if (warp == 2)
+            mma();
+        else
+            pf_softmax<KV, MODE>(smem, a, bb, tmem, abort_flag, total);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -1232,21 +1254,34 @@ int launch_prefill2_kv(const CUtensorMap &tmk, const CUtensorMap &tmv, const Pre
     return cuda_status(cudaGetLastError());
 }
 
+// One-time set-up of the one-tile kernel: shared memory and grid; for an FP8
+// cache also the check that the kernel launches with the register count its
+// register split assumes (otherwise it is never launched, see prefill_usable).
+template <int KV, int MODE>
+const P2Setup &prefill_setup() {
+    static P2Setup su;
+    static std::once_flag once;
+    std::call_once(once, [] {   // one CTA per SM
+        su.err = cudaFuncSetAttribute(prefill_kernel<KV, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      PfL<KV>::SMEM);
+        int dev = 0, sms = 0;
+        cudaFuncAttributes fa;
+        if (su.err == cudaSuccess) su.err = cudaGetDevice(&dev);
+        if (su.err == cudaSuccess) su.err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (su.err == cudaSuccess) su.err = cudaFuncGetAttributes(&fa, prefill_kernel<KV, MODE>);
+        su.grid = sms;
+        su.usable = su.err == cudaSuccess && sms > 0 && (!PfL<KV>::F8 || fa.numRegs == PfL<KV>::LAUNCH_REGS);
+    });
+    return su;
+}
+
 template <int KV, int MODE>
 int launch_prefill_kv(const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args, long long max_items,
                       cudaStream_t st) {
-    static int grid = 0;
-    static cudaError_t init_err = cudaSuccess;
-    static std::once_flag once;
-    std::call_once(once, [] {   // one CTA per SM
-        init_err = cudaFuncSetAttribute(prefill_kernel<KV, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        PfL<KV>::SMEM);
-        int dev = 0, sms = 0;
-        if (init_err == cudaSuccess) init_err = cudaGetDevice(&dev);
-        if (init_err == cudaSuccess) init_err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        grid = sms;
-    });
-    if (init_err != cudaSuccess || grid <= 0) return PA_ERR_CUDA;
+    const P2Setup &su = prefill_setup<KV, MODE>();
+    if (su.err != cudaSuccess) return PA_ERR_CUDA;
+    if (!su.usable) return PA_ERR_UNSUPPORTED;
+    const int grid = su.grid;
     const int g = (int)(max_items < grid ? (max_items > 0 ? max_items : 1) : grid);
     prefill_kernel<KV, MODE><<<g, PfL<KV>::THREADS, PfL<KV>::SMEM, st>>>(tmk, tmv, args);
     return cuda_status(cudaGetLastError());
@@ -1265,6 +1300,13 @@ int launch_prefill(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const
 int launch_shared_ranges(const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
                          long long max_items, cudaStream_t st) {
     return launch_prefill_kv<PA_KV_F16, PF_SHARED>(tmk, tmv, args, max_items, st);
+}
+
+bool prefill_usable(int kv) {
+    if (kv == PA_KV_BF16) return prefill_setup<PA_KV_BF16, PF_CAUSAL>().usable;
+    if (kv == PA_KV_F16) return prefill_setup<PA_KV_F16, PF_CAUSAL>().usable;
+    if (kv == PA_KV_FP8_E4M3) return prefill_setup<PA_KV_FP8_E4M3, PF_CAUSAL>().usable;
+    return false;
 }
 
 bool prefill2_usable(int kv) {

@@ -58,6 +58,10 @@ int launch_prefill(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const
 int launch_shared_ranges(const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
                          long long max_items, cudaStream_t st);
 
+// Whether the one-tile kernel can run for this cache type (for an FP8 cache:
+// built with the register count its register split assumes); checked once.
+bool prefill_usable(int kv);
+
 // Whether the two-tile kernel can run for this cache type (fp16 or bf16, and
 // built with the register count its register split assumes); checked once.
 bool prefill2_usable(int kv);
