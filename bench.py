@@ -166,6 +166,15 @@ def prefill_launch(w, kv_dtype) -> bool:
             and 128 % G == 0 and w.num_new_tokens * G >= 17)
 
 
+def shared_on_tensor_cores(w, kv_dtype) -> bool:
+    """Whether pa_decode_shared_prefix reduces the shared ranges on the
+    tensor-core kernel (the library's rule: fp16 cache, head_dim 128, G
+    dividing 128; PA_PREFILL=0 or PA_SHARED_TC=0 disable)."""
+    G = w.num_heads // w.num_kv_heads
+    return (kv_dtype == "f16" and w.head_dim == 128 and 128 % G == 0
+            and os.environ.get("PA_PREFILL", "1")[:1] != "0" and os.environ.get("PA_SHARED_TC", "1")[:1] != "0")
+
+
 def kv_write_bytes(w, esz=2) -> int:
     """fp16/bf16 rows read, cache elements written, slots read."""
     T = w.num_new_tokens
@@ -690,8 +699,11 @@ def run_ours(args):
         "decode_ms": {"mean": round(dec_avg_ms, 5), "p10": round(float(np.percentile(dec_ms, 10)), 5),
                       "p90": round(float(np.percentile(dec_ms, 90)), 5)},
         "roofline": {
-            "kernel": ("pa_attention_causal" if multi else "pa_decode") +
-                      " (prep + persistent partition kernel with fused log-sum-exp merge)",
+            "kernel": ("pa_attention_causal (prep, tensor-core kernels for long runs of new tokens, decode "
+                       "pipeline beside them)" if multi else
+                       "pa_decode_shared_prefix (prep, shared ranges on the tensor-core kernel, own ranges and "
+                       "merges on the decode kernel)" if shared_mode else
+                       "pa_decode (prep + persistent partition kernel with fused log-sum-exp merge)"),
             "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "traffic": kernel_traffic() if headline else None,
@@ -711,7 +723,8 @@ def run_ours(args):
         # per layer: KV write, prep, decode pipeline, block copy (if pairs), the
         # tensor-core kernels (one-tile, and two-tile for 16-bit caches)
         "gpu_launches": args.steps * layers * (3 + (1 if has_pairs else 0) +
-                                               ((1 + (kvd != "fp8")) if prefill_launch(w, kvd) else 0)),
+                                               ((1 + (kvd != "fp8")) if prefill_launch(w, kvd) else 0) +
+                                               (1 if shared_mode and shared_on_tensor_cores(w, kvd) else 0)),
         "alloc_us_per_step": round(alloc_us, 1),
         "clocks": clk.summary(),
     }
