@@ -166,6 +166,13 @@ def prefill_launch(w, kv_dtype) -> bool:
             and 128 % G == 0 and w.num_new_tokens * G >= 17)
 
 
+def narrow_launch(w, kv_dtype) -> bool:
+    """Whether a multi-token call that launches the tensor-core kernels also
+    launches the narrow one, for sequences of at most 32 query rows (the
+    library's rule; PA_NARROW=0 disables)."""
+    return prefill_launch(w, kv_dtype) and os.environ.get("PA_NARROW", "1")[:1] != "0"
+
+
 def shared_on_tensor_cores(w, kv_dtype) -> bool:
     """Whether pa_decode_shared_prefix reduces the shared ranges on the
     tensor-core kernel (the library's rule: fp16 cache, head_dim 128, G
@@ -699,8 +706,9 @@ def run_ours(args):
         "decode_ms": {"mean": round(dec_avg_ms, 5), "p10": round(float(np.percentile(dec_ms, 10)), 5),
                       "p90": round(float(np.percentile(dec_ms, 90)), 5)},
         "roofline": {
-            "kernel": ("pa_attention_causal (prep, tensor-core kernels for long runs of new tokens, decode "
-                       "pipeline beside them)" if multi else
+            "kernel": ("pa_attention_causal (prep, tensor-core kernels for sequences of more than 16 query "
+                       "rows -- narrow for up to 32, 128-row tiles beyond -- decode pipeline beside them)"
+                       if multi else
                        "pa_decode_shared_prefix (prep, shared ranges on the tensor-core kernel, own ranges and "
                        "merges on the decode kernel)" if shared_mode else
                        "pa_decode (prep + persistent partition kernel with fused log-sum-exp merge)"),
@@ -721,9 +729,10 @@ def run_ours(args):
             "ms_per_step": round(graph_ms / args.steps, 4),
             "note": "the whole step captured once in a CUDA Graph and replayed"},
         # per layer: KV write, prep, decode pipeline, block copy (if pairs), the
-        # tensor-core kernels (one-tile, and two-tile for 16-bit caches)
+        # tensor-core kernels (narrow, one-tile, and two-tile for 16-bit caches)
         "gpu_launches": args.steps * layers * (3 + (1 if has_pairs else 0) +
-                                               ((1 + (kvd != "fp8")) if prefill_launch(w, kvd) else 0) +
+                                               ((1 + (kvd != "fp8") + narrow_launch(w, kvd))
+                                                if prefill_launch(w, kvd) else 0) +
                                                (1 if shared_mode and shared_on_tensor_cores(w, kvd) else 0)),
         "alloc_us_per_step": round(alloc_us, 1),
         "clocks": clk.summary(),

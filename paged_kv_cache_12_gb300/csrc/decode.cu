@@ -283,12 +283,14 @@ __device__ __forceinline__ int last_le(const int32_t *a, int n, int x) {
 // goes to the tensor-core prefill kernels instead: it gets no items here.  Its
 // ceil(T G / 128) row tiles, last rows first, are listed in ptiles when there
 // is one (or when pairs is 0), otherwise in pptiles as pairs of neighbouring
-// tiles {seq, tile, tile - 1, 0} (an odd one out as {seq, 0, -1, 0}).
+// tiles {seq, tile, tile - 1, 0} (an odd one out as {seq, 0, -1, 0}) -- unless
+// its rows number at most nr_max (0: never), then it is listed in ntiles
+// ({seq, 0, 0, 0}) for the narrow kernel.
 __global__ void __launch_bounds__(PREP_THREADS) causal_prep_kernel(
     const int32_t *__restrict__ context_lens, const int32_t *__restrict__ qs, int B, int NQ, int Hq, int D, int Hkv,
     int max_ctx, long long max_table_tokens, int pt, int ms, WsHeader *hdr, int *part_off, int *vlen, int *gstart,
     ItemRec *items, int *grp, uint16_t *out, uint32_t nan2, int pf_min_rows, int4 *ptiles, int4 *pptiles,
-    int pairs) {
+    int pairs, int nr_max, int4 *ntiles) {
     constexpr int NBK = MAX_PART_TOKENS / CHUNK;
     __shared__ int warp_sums[PREP_THREADS / 32];
     __shared__ int hist[NBK], cursor[NBK];
@@ -342,26 +344,35 @@ __global__ void __launch_bounds__(PREP_THREADS) causal_prep_kernel(
         run_g += tot;
     }
     // pass 2b: row tiles of the prefill kernels
-    int run_t = 0, run_p = 0;
+    int run_t = 0, run_p = 0, run_n = 0;
     for (int base = 0; base < B; base += PREP_THREADS) {
         const int i = base + threadIdx.x;
-        int n = 0, L, T;
-        if (i < B && qs_ok && seq_ok(i, L, T) && prefill(T)) n = (int)(((long long)T * G + 127) / 128);
+        int n = 0, nn = 0, L, T;
+        if (i < B && qs_ok && seq_ok(i, L, T) && prefill(T)) {
+            if ((long long)T * G <= nr_max)
+                nn = 1;
+            else
+                n = (int)(((long long)T * G + 127) / 128);
+        }
         const bool paired = pairs && n >= 2;
         const int ns = paired ? 0 : n, np = paired ? (n + 1) / 2 : 0;
-        int tot, totp;
+        int tot, totp, totn;
         const int e = run_t + block_exclusive_scan(ns, warp_sums, &tot);
         const int ep = run_p + block_exclusive_scan(np, warp_sums, &totp);
+        const int en = run_n + block_exclusive_scan(nn, warp_sums, &totn);
         for (int k = 0; k < ns; ++k) ptiles[e + k] = make_int4(i, n - 1 - k, 0, 0);
         for (int k = 0; k < np; ++k) pptiles[ep + k] = make_int4(i, n - 1 - 2 * k, n - 2 - 2 * k, 0);
+        if (nn) ntiles[en] = make_int4(i, 0, 0, 0);
         run_t += tot;
         run_p += totp;
+        run_n += totn;
     }
     if (threadIdx.x == 0) {
         gstart[B] = run_g;
         part_off[NQ] = run;
         hdr->pf_items = run_t * Hkv;
         hdr->pf2_items = run_p * Hkv;
+        hdr->pfn_items = run_n * Hkv;
     }
     __syncthreads();
     const int NG = run_g;
@@ -523,6 +534,26 @@ bool prefill_pairs_enabled() {
     static const bool on = [] {
         const char *e = std::getenv("PA_PREFILL_PAIRS");
         return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
+// Whether sequences (and shared ranges) of at most NARROW_ROWS query rows go to
+// the narrow tensor-core kernel (unless PA_NARROW=0, read once).
+bool narrow_enabled() {
+    static const bool on = [] {
+        const char *e = std::getenv("PA_NARROW");
+        return !(e && e[0] == '0');
+    }();
+    return on;
+}
+
+// Whether shared ranges of at most NARROW_ROWS rows go to the narrow kernel
+// (only with PA_NARROW_SHARED=1, read once).
+bool narrow_shared_enabled() {
+    static const bool on = [] {
+        const char *e = std::getenv("PA_NARROW_SHARED");
+        return e && e[0] == '1' && narrow_enabled();
     }();
     return on;
 }
@@ -690,7 +721,12 @@ int decode_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     // item; the decode kernel then reduces each member's own partitions only.
     const bool tc = grouped && kv == PA_KV_F16 && head_dim == 128 && PF_ROWS % G == 0 && prefill_enabled() &&
                     shared_tc_enabled();
-    const int mt = tc ? PF_ROWS / G : 0;
+    // up to NARROW_ROWS / G members on the narrow kernel when that is at least 4
+    // (only with PA_NARROW_SHARED=1: on the parallel-sampling workload the
+    // 128-row kernel is faster)
+    const bool tcn = tc && narrow_shared_enabled() && NARROW_ROWS % G == 0 && NARROW_ROWS / G >= 4 &&
+                     narrow_usable(PA_KV_F16);
+    const int mt = tcn ? NARROW_ROWS / G : tc ? PF_ROWS / G : 0;
     // query rows per decode item: one sequence's G heads, or, for a shared
     // range on this kernel, as many members' G heads as two head tiles hold
     const int NT = (G > 8 || (grouped && !tc)) ? 2 : 1;
@@ -738,7 +774,8 @@ int decode_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
         pa_.ws_ml = ws_ml;
         pa_.ws_o = ws_o;
         pa_.pt = L.pt;
-        const int rc = launch_shared_ranges(tmk, tmv, pa_, L.ptile_cap * num_kv_heads, st);
+        const int rc = tcn ? launch_narrow_shared(tmk, tmv, pa_, L.ptile_cap * num_kv_heads, st)
+                           : launch_shared_ranges(tmk, tmv, pa_, L.ptile_cap * num_kv_heads, st);
         if (rc != PA_OK) return rc;
     }
 
@@ -847,11 +884,15 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     int4 *ppairs = reinterpret_cast<int4 *>(ws + L.ppairs);
     // sequences with several row tiles take them two at a time (16-bit caches)
     const bool pairs = pf && kv != PA_KV_FP8_E4M3 && prefill_pairs_enabled() && prefill2_usable(kv);
+    // sequences of at most NARROW_ROWS rows go to the narrow kernel
+    const bool narrow = pf && narrow_enabled() && narrow_usable(kv);
+    int4 *ntiles = reinterpret_cast<int4 *>(ws + L.ntiles);
     causal_prep_kernel<<<1, PREP_THREADS, 0, st>>>(context_lens, query_start, num_seqs, num_query_tokens, num_heads,
                                                    head_dim, num_kv_heads, max_context_len,
                                                    (long long)max_blocks_per_seq * block_size, L.pt, ms, hdr,
                                                    part_off, vlen, gstart, items, grp, hout, nan_pair(kv),
-                                                   pf ? PF_MIN_ROWS : 0, ptiles, ppairs, pairs ? 1 : 0);
+                                                   pf ? PF_MIN_ROWS : 0, ptiles, ppairs, pairs ? 1 : 0,
+                                                   narrow ? NARROW_ROWS : 0, ntiles);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
 
     DecodeArgs args;
@@ -879,7 +920,7 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     args.ws_o = reinterpret_cast<float *>(ws + L.o);
     const long long max_items = L.item_cap * num_kv_heads;
     if (!pf) return launch_kv_any(kv, head_dim, PA_CAUSAL_NT, true, tmk, tmv, args, max_items, st);
-    PrefillArgs pa_;
+    PrefillArgs pa_{};
     pa_.out = hout;
     pa_.query = query;
     pa_.block_tables = block_tables;
@@ -897,9 +938,15 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     pa_.scale_log2 = args.scale_log2;   // with the K scale of an FP8 cache
     pa_.v_scale = args.v_scale;
     pa_.wait_limit = wait_limit_cycles();
-    // the tensor-core kernels on `on`: pairs first (the long chunks), then the
-    // sequences of one row tile
+    // the tensor-core kernels on `on`: the narrow items, pairs (the long
+    // chunks), then the sequences of one row tile
     auto tensor_core = [&](cudaStream_t on) {
+        if (narrow) {
+            PrefillArgs na = pa_;
+            na.tiles = ntiles;
+            const int rcn = launch_narrow(kv, tmk, tmv, na, (long long)num_seqs * num_kv_heads, on);
+            if (rcn != PA_OK) return rcn;
+        }
         if (pairs) {
             const int rc2 = launch_prefill2(kv, tmk, tmv, pa_, (L.ptile_cap + 1) / 2 * num_kv_heads, on);
             if (rc2 != PA_OK) return rc2;

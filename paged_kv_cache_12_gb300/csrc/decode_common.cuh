@@ -81,12 +81,13 @@ struct WsHeader {
     int counter;
     int pf_items;    // multi-token form: work items of the one-tile tensor-core kernel
     int pf2_items;   // multi-token form: work items of the two-tile tensor-core kernel
-    int pad[59];
+    int pfn_items;   // multi-token form: work items of the narrow tensor-core kernel
+    int pad[58];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
 struct WsLayout {
-    size_t part_off, gsize, gshared, items, grp, ml, o, ptiles, ppairs, total;
+    size_t part_off, gsize, gshared, items, grp, ml, o, ptiles, ppairs, ntiles, total;
     int pmax, pt;
     long long item_cap, ptile_cap;
 };
@@ -161,6 +162,9 @@ inline WsLayout ws_layout_causal(int B, int NQ, int Hq, int Hkv, int D, int max_
     off += up256(sizeof(int4) * (size_t)w.ptile_cap);
     w.ppairs = off;
     off += up256(sizeof(int4) * (size_t)w.ptile_cap);
+    // narrow tensor-core kernel: sequences whose new tokens fill at most 32 rows
+    w.ntiles = off;
+    off += up256(sizeof(int4) * (size_t)B);
     w.total = off;
     return w;
 }

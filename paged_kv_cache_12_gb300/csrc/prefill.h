@@ -58,6 +58,21 @@ int launch_prefill(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const
 int launch_shared_ranges(const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
                          long long max_items, cudaStream_t st);
 
+// The narrow kernel (narrow.cu): work items of at most NARROW_ROWS query rows
+// (new tokens x G of one sequence, or members x G of a shared range), with the
+// KV tokens on the MMAs' M side.  launch_narrow: the causal rows of the
+// sequences listed in args.tiles ({sequence, 0, 0, 0}; pfn_items in the
+// header), any cache type; launch_narrow_shared: the shared-prefix mode of
+// launch_shared_ranges (fp16 cache), item count pf_items.
+constexpr int NARROW_ROWS = 32;
+int launch_narrow(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
+                  long long max_items, cudaStream_t st);
+int launch_narrow_shared(const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
+                         long long max_items, cudaStream_t st);
+// Whether the narrow kernel can run for this cache type (for an FP8 cache:
+// built with the register count its register split assumes); checked once.
+bool narrow_usable(int kv);
+
 // Whether the one-tile kernel can run for this cache type (for an FP8 cache:
 // built with the register count its register split assumes); checked once.
 bool prefill_usable(int kv);

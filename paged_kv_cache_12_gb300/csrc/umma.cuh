@@ -118,6 +118,12 @@ __host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool bf16, bool b
            | ((uint32_t)(M >> 4) << 24);              // M / 16
 }
 
+// The same with A MN-major too (A stored with M contiguous, as a tile of
+// K rows of M elements): used where the A operand is a transposed tile.
+__host__ __device__ constexpr uint32_t idesc_f16_at(int M, int N, bool bf16, bool b_mn_major) {
+    return idesc_f16(M, N, bf16, b_mn_major) | (1u << 15);   // A major-ness
+}
+
 // D[tmem] (+)= A[smem] * B[smem]; issued by one thread.
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
