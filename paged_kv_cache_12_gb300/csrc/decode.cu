@@ -774,6 +774,7 @@ int decode_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
         pa_.ws_ml = ws_ml;
         pa_.ws_o = ws_o;
         pa_.pt = L.pt;
+        pa_.scratch = ws + L.nscr;
         const int rc = tcn ? launch_narrow_shared(tmk, tmv, pa_, L.ptile_cap * num_kv_heads, st)
                            : launch_shared_ranges(tmk, tmv, pa_, L.ptile_cap * num_kv_heads, st);
         if (rc != PA_OK) return rc;
@@ -944,6 +945,7 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
         if (narrow) {
             PrefillArgs na = pa_;
             na.tiles = ntiles;
+            na.scratch = ws + L.nscr;
             const int rcn = launch_narrow(kv, tmk, tmv, na, (long long)num_seqs * num_kv_heads, on);
             if (rcn != PA_OK) return rcn;
         }

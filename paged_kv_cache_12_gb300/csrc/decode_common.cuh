@@ -86,8 +86,15 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
+// The narrow tensor-core kernel merges the four partial results of a work
+// item's rows through a scratch area of the workspace: per CTA (at most
+// NW_MAX_CTAS of them) and item parity, 4 x 128 dims x 32 rows of fp32 O and
+// 4 x 32 (m, l) pairs.
+constexpr int NW_MAX_CTAS = 160;
+constexpr size_t NW_SCRATCH_PER_CTA = 2 * (4 * 128 * 32 * 4 + 4 * 32 * 8);
+
 struct WsLayout {
-    size_t part_off, gsize, gshared, items, grp, ml, o, ptiles, ppairs, ntiles, total;
+    size_t part_off, gsize, gshared, items, grp, ml, o, ptiles, ppairs, ntiles, nscr, total;
     int pmax, pt;
     long long item_cap, ptile_cap;
 };
@@ -124,6 +131,10 @@ inline WsLayout ws_layout(int B, int Hq, int Hkv, int D, int max_ctx, bool group
     w.ptiles = off;
     off += up256(sizeof(int4) * (size_t)w.ptile_cap);
     w.ppairs = off;
+    w.ntiles = off;
+    // the narrow kernel's merge scratch (shared ranges of up to 32 rows)
+    w.nscr = off;
+    if (grouped && D == 128 && 32 % (Hq / Hkv) == 0 && 32 / (Hq / Hkv) >= 4) off += NW_MAX_CTAS * NW_SCRATCH_PER_CTA;
     w.total = off;
     return w;
 }
@@ -162,9 +173,12 @@ inline WsLayout ws_layout_causal(int B, int NQ, int Hq, int Hkv, int D, int max_
     off += up256(sizeof(int4) * (size_t)w.ptile_cap);
     w.ppairs = off;
     off += up256(sizeof(int4) * (size_t)w.ptile_cap);
-    // narrow tensor-core kernel: sequences whose new tokens fill at most 32 rows
+    // narrow tensor-core kernel: sequences whose new tokens fill at most 32
+    // rows, and its merge scratch
     w.ntiles = off;
     off += up256(sizeof(int4) * (size_t)B);
+    w.nscr = off;
+    if (D == 128 && 128 % G == 0) off += NW_MAX_CTAS * NW_SCRATCH_PER_CTA;
     w.total = off;
     return w;
 }

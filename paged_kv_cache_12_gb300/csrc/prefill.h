@@ -29,6 +29,8 @@ struct PrefillArgs {
     float2 *ws_ml;
     float *ws_o;
     int pt;
+    // narrow kernel: merge scratch, NW_SCRATCH_PER_CTA bytes per CTA
+    uint8_t *scratch;
 };
 
 // Query rows per work tile, and the smallest number of query rows

@@ -134,11 +134,12 @@ __device__ void pf_stream(uint8_t *smem, const int *off_ring, int off_ctrl, cons
                 if (cnt > s)
                     mbar_wait_bounded(full[r][s], (uint32_t)(((s + (cnt - 1 - s) / PST * PST) / PST) & 1), WAIT_LIMIT);
     };
-    // The warp walks this CTA's tiles, item by item, with a cursor two steps
+    // The warp walks this CTA's tiles, item by item, with a cursor LA steps
     // ahead of the tile it issues: each lane's block-table entry (and at an
     // item's start the item's range) is loaded there, so that the load's round
-    // trip through L2 overlaps two tiles' copies instead of preceding each.
+    // trip through L2 overlaps tiles' copies instead of preceding each.
     // Lane j owns box j of a tile (tokens t0 + j box_rows ..).
+    constexpr int LA = 2;
     struct Cur {
         int item, n;
         PfRange t;
@@ -167,17 +168,19 @@ __device__ void pf_stream(uint8_t *smem, const int *off_ring, int off_ctrl, cons
         }
         fetch(c);
     };
-    Cur c0;
-    c0.item = blockIdx.x;
-    c0.n = 0;
-    c0.t = PfRange{0, 0, 0, 0, 0};
-    next_item(c0);
-    fetch(c0);
-    Cur c1 = c0;
-    step(c1);
-    Cur c2 = c1;
-    step(c2);
-    while (c0.item < total) {
+    Cur cs[LA + 1];
+    cs[0].item = blockIdx.x;
+    cs[0].n = 0;
+    cs[0].t = PfRange{0, 0, 0, 0, 0};
+    next_item(cs[0]);
+    fetch(cs[0]);
+#pragma unroll
+    for (int i = 1; i <= LA; ++i) {
+        cs[i] = cs[i - 1];
+        step(cs[i]);
+    }
+    while (cs[0].item < total) {
+        const Cur &c0 = cs[0];
         const int item = c0.item;
         const PfRange &t = c0.t;
         const int tok = c0.n * PN + lane * box_rows;
@@ -215,9 +218,9 @@ __device__ void pf_stream(uint8_t *smem, const int *off_ring, int off_ctrl, cons
         }
         __syncwarp();
         ++cnt;
-        c0 = c1;
-        c1 = c2;
-        step(c2);
+#pragma unroll
+        for (int i = 0; i < LA; ++i) cs[i] = cs[i + 1];
+        step(cs[LA]);
     }
     drain();
 }

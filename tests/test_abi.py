@@ -53,9 +53,12 @@ def test_workspace_size_is_a_host_bound():
     g1 = pa.pa_decode_workspace_size(64, 32, 32, 128, 2048)
     assert 64 * 8 * 32 * 128 * 4 <= g1 < 64 * 9 * 32 * 128 * 4
     assert pa.lib().pa_decode_workspace_size(1, 8, 0, 128, 10) == 0
-    # multi-token form: a partial row per query row and partition (400 rows x 8 partitions of 1024)
+    # multi-token form: a partial row per query row and partition (400 rows x 8
+    # partitions of 1024), and the narrow kernel's merge scratch (160 CTAs x two
+    # item parities x four quarters' 128 x 32 fp32 O and 32 (m, l) pairs)
     spec = pa.pa_attention_causal_workspace_size(100, 400, 64, 8, 128, 8192)
-    assert 400 * 8 * 64 * 128 * 4 <= spec < 400 * 9 * 64 * 128 * 4
+    scratch = 160 * 2 * 4 * (128 * 32 * 4 + 32 * 8)
+    assert 400 * 8 * 64 * 128 * 4 + scratch <= spec < 400 * 9 * 64 * 128 * 4 + scratch
     assert pa.lib().pa_attention_causal_workspace_size(1, 4, 6, 4, 128, 10) == 0
 
 
