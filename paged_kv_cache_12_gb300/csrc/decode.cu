@@ -285,12 +285,15 @@ __device__ __forceinline__ int last_le(const int32_t *a, int n, int x) {
 // is one (or when pairs is 0), otherwise in pptiles as pairs of neighbouring
 // tiles {seq, tile, tile - 1, 0} (an odd one out as {seq, 0, -1, 0}) -- unless
 // its rows number at most nr_max (0: never), then it is listed in ntiles
-// ({seq, 0, 0, 0}) for the narrow kernel.
+// ({seq, 0, 0, 0}) for the narrow kernel.  Its N = (listed sequences x Hkv)
+// items run on nw_grid CTAs; when the last round is partial (R = N mod
+// nw_grid items), those R items are split into k = nw_grid / R pieces of their
+// KV ranges (at least two KV tiles each), which the kernel merges.
 __global__ void __launch_bounds__(PREP_THREADS) causal_prep_kernel(
     const int32_t *__restrict__ context_lens, const int32_t *__restrict__ qs, int B, int NQ, int Hq, int D, int Hkv,
     int max_ctx, long long max_table_tokens, int pt, int ms, WsHeader *hdr, int *part_off, int *vlen, int *gstart,
     ItemRec *items, int *grp, uint16_t *out, uint32_t nan2, int pf_min_rows, int4 *ptiles, int4 *pptiles,
-    int pairs, int nr_max, int4 *ntiles) {
+    int pairs, int nr_max, int4 *ntiles, int nw_grid, int *ntickets) {
     constexpr int NBK = MAX_PART_TOKENS / CHUNK;
     __shared__ int warp_sums[PREP_THREADS / 32];
     __shared__ int hist[NBK], cursor[NBK];
@@ -375,6 +378,24 @@ __global__ void __launch_bounds__(PREP_THREADS) causal_prep_kernel(
         hdr->pfn_items = run_n * Hkv;
     }
     __syncthreads();
+    if (threadIdx.x == 0 && nw_grid > 0) {
+        const int N = run_n * Hkv;
+        int whole = N, k = 1;
+        const int F = N / nw_grid, R = N - F * nw_grid;
+        if (R > 0) {
+            int kk = nw_grid / R;
+            // every piece at least two KV tiles: capped by the shortest split item
+            for (int x = N - R; x < N && kk >= 2; x += Hkv - (x % Hkv)) {
+                const int nkv = (context_lens[ntiles[x / Hkv].x] + 127) / 128;
+                kk = min(kk, nkv / 2);
+            }
+            if (kk >= 2) whole = F * nw_grid, k = kk;
+        }
+        hdr->pfn_whole = whole;
+        hdr->pfn_split = k;
+        hdr->pfn_items = whole + (N - whole) * k;
+        for (int j = 0; j < NW_MAX_CTAS; ++j) ntickets[j] = 0;
+    }
     const int NG = run_g;
     // group g: rows [r0 + jl, r0 + jh) of sequence i; C = L - T + 1 positions
     // seen by its first new token; the last member sees vis positions
@@ -893,7 +914,8 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
                                                    (long long)max_blocks_per_seq * block_size, L.pt, ms, hdr,
                                                    part_off, vlen, gstart, items, grp, hout, nan_pair(kv),
                                                    pf ? PF_MIN_ROWS : 0, ptiles, ppairs, pairs ? 1 : 0,
-                                                   narrow ? NARROW_ROWS : 0, ntiles);
+                                                   narrow ? NARROW_ROWS : 0, ntiles, narrow ? narrow_grid() : 0,
+                                                   narrow ? nw_split_area(ws + L.nscr).tickets : nullptr);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
 
     DecodeArgs args;
@@ -946,7 +968,7 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
             PrefillArgs na = pa_;
             na.tiles = ntiles;
             na.scratch = ws + L.nscr;
-            const int rcn = launch_narrow(kv, tmk, tmv, na, (long long)num_seqs * num_kv_heads, on);
+            const int rcn = launch_narrow(kv, tmk, tmv, na, narrow_grid(), on);
             if (rcn != PA_OK) return rcn;
         }
         if (pairs) {

@@ -82,7 +82,9 @@ struct WsHeader {
     int pf_items;    // multi-token form: work items of the one-tile tensor-core kernel
     int pf2_items;   // multi-token form: work items of the two-tile tensor-core kernel
     int pfn_items;   // multi-token form: work items of the narrow tensor-core kernel
-    int pad[58];
+    int pfn_whole;   // ... of which the first pfn_whole are whole (sequence, kv head) items,
+    int pfn_split;   // the others pfn_split pieces each of the last items' KV ranges
+    int pad[56];
 };
 static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 
@@ -92,6 +94,27 @@ static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
 // 4 x 32 (m, l) pairs.
 constexpr int NW_MAX_CTAS = 160;
 constexpr size_t NW_SCRATCH_PER_CTA = 2 * (4 * 128 * 32 * 4 + 4 * 32 * 8);
+// ... and, after the CTAs' areas, the pieces of split items (at most
+// NW_MAX_CTAS of them): 32 rows of fp32 O (128 dims) and (m, l) each, and a
+// ticket per split item.
+constexpr size_t NW_SPLIT_BYTES = (size_t)NW_MAX_CTAS * 32 * (128 * 4 + 8) + NW_MAX_CTAS * 4;
+
+struct NwSplitArea {
+    float *o;       // [piece][row][128]
+    float2 *ml;     // [piece][row]
+    int *tickets;   // [split item]
+};
+
+__host__ __device__ inline NwSplitArea nw_split_area(uint8_t *nscr) {
+    uint8_t *p = nscr + (size_t)NW_MAX_CTAS * NW_SCRATCH_PER_CTA;
+    NwSplitArea s;
+    s.o = reinterpret_cast<float *>(p);
+    p += (size_t)NW_MAX_CTAS * 32 * 128 * 4;
+    s.ml = reinterpret_cast<float2 *>(p);
+    p += (size_t)NW_MAX_CTAS * 32 * 8;
+    s.tickets = reinterpret_cast<int *>(p);
+    return s;
+}
 
 struct WsLayout {
     size_t part_off, gsize, gshared, items, grp, ml, o, ptiles, ppairs, ntiles, nscr, total;
@@ -178,7 +201,7 @@ inline WsLayout ws_layout_causal(int B, int NQ, int Hq, int Hkv, int D, int max_
     w.ntiles = off;
     off += up256(sizeof(int4) * (size_t)B);
     w.nscr = off;
-    if (D == 128 && 128 % G == 0) off += NW_MAX_CTAS * NW_SCRATCH_PER_CTA;
+    if (D == 128 && 128 % G == 0) off += NW_MAX_CTAS * NW_SCRATCH_PER_CTA + up256(NW_SPLIT_BYTES);
     w.total = off;
     return w;
 }

@@ -20,15 +20,16 @@
 // workspace (m = max of the four, O and l scaled by 2^(m_q - m) and summed).
 //
 // Products (M 128, N 128, K 16 per instruction):
-//   S = Q' K^T   A = Q' (the four copies of Q, shared memory), B = K tile;
+//   S = Q' K^T   A = Q' (the four copies of Q, tensor memory), B = K tile;
 //   O += P V     A = P (tensor memory, written by the softmax), B = V tile.
-// Tensor memory: S in two buffers of 128 columns, P (two fp16/bf16 per
-// column) in two buffers of 64, O in 128: all 512 columns, one CTA per SM.
+// Tensor memory: S in two buffers of 128 columns, P and Q' (two fp16/bf16
+// per column) 64 each, O 128: all 512 columns, one CTA per SM; shared memory
+// holds only the K/V rings (and an FP8 cache's staging rings).
 //
 // One CTA per SM, persistent over the item list; warps:
 //   0, 1   producers: K and V tiles of 128 tokens by TMA through the block
-//          table (16-bit caches: 3-stage rings; FP8: the codes, 2-stage
-//          staging rings);
+//          table (16-bit caches: 3-stage rings; FP8: the codes, 3-stage
+//          staging rings before 2-stage 16-bit rings);
 //   2, 3   MMA issuers (one thread each): warp 2 the S products, warp 3 the
 //          PV products -- one thread takes about 100 cycles per tcgen05.mma,
 //          two streams halve the time the products hold the pipeline;
@@ -46,10 +47,10 @@ namespace pa {
 namespace {
 
 constexpr int NR = NARROW_ROWS;           // query rows of an item (padded): one per lane of a quarter
-constexpr int NQ_BYTES = PM * PD * 2;     // Q': 128 rows x 128 dims, 16-bit, 128-byte swizzled K-major
 constexpr int NW_SOFT0 = 4;               // first softmax warp
-// tensor memory: S 0, S 1 (PN fp32 columns each), P 0, P 1 (PN / 2), O (PD)
-constexpr int NW_S = 0, NW_P = 2 * PN, NW_O = 2 * PN + PN;
+// tensor memory: S 0, S 1 (PN fp32 columns each), P (PN / 2: two 16-bit
+// values per column), Q' (PD / 2), O (PD)
+constexpr int NW_S = 0, NW_P = 2 * PN, NW_Q = NW_P + PN / 2, NW_O = NW_Q + PD / 2;
 constexpr int NW_TMEM_COLS = 512;
 static_assert(NR == 32 && PM == 4 * NR, "four copies of the item's rows fill the tile");
 static_assert(PN == 128, "a quarter of a KV tile per softmax warp: 32 tokens");
@@ -62,12 +63,12 @@ static_assert(NW_O + PD <= NW_TMEM_COLS, "tensor-memory columns");
 #define PA_NW_R8 2
 #endif
 #ifndef PA_NW_S8
-#define PA_NW_S8 2
+#define PA_NW_S8 3
 #endif
 
 // Shared memory per cache type: K and V rings of R 16-bit stages (the TMA
 // fills them, or for an FP8 cache the converting warps from staging rings of
-// S8 stages of codes), then Q'.
+// S8 stages of codes).
 template <int KV>
 struct NwL {
     static constexpr bool F8 = KV == PA_KV_FP8_E4M3;
@@ -77,15 +78,14 @@ struct NwL {
     static constexpr int OFF_V = R * KV_BYTES;
     static constexpr int OFF_K8 = 2 * R * KV_BYTES;
     static constexpr int OFF_V8 = OFF_K8 + S8 * F8_BYTES;
-    static constexpr int OFF_Q = OFF_V8 + S8 * F8_BYTES;
-    static constexpr int OFF_CTRL = OFF_Q + NQ_BYTES;
+    static constexpr int OFF_CTRL = OFF_V8 + S8 * F8_BYTES;
     static constexpr int SMEM = OFF_CTRL + CTRL_BYTES + 1024;   // + alignment slack
     // 16-bit caches: warps 0 / 1 produce K / V, 2 / 3 issue the MMAs, 4-7 run
     // the softmax.  FP8 caches: warps 0 / 1 stage the codes and 8-11 / 12-15
     // convert K / V, a quarter of the rows each (two per SM sub-partition).
     static constexpr int THREADS = (F8 ? 16 : 8) * 32;
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
-    static_assert(OFF_Q % 1024 == 0 && OFF_K8 % 1024 == 0, "swizzled tiles 1024-byte aligned");
+    static_assert(OFF_K8 % 1024 == 0, "swizzled tiles 1024-byte aligned");
     static_assert(R <= MAXST && S8 <= MAXST, "ring stages");
 };
 
@@ -123,10 +123,48 @@ __device__ __forceinline__ int nw_total(const PrefillArgs &a) {
 
 __device__ __forceinline__ void prefetch_l2(const void *p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
+// The causal item list: items below `whole` are whole (sequence, kv head)
+// items; each later one is one of k pieces of the KV range of one of the last
+// items (the prep kernel splits the last, partial round of items so that it
+// fills the grid).  Shared ranges are never split.
+struct NwSplit {
+    int whole, k;
+};
+
+template <int MODE>
+__device__ __forceinline__ NwSplit nw_split(const PrefillArgs &a, int total) {
+    if constexpr (MODE == PF_SHARED)
+        return NwSplit{total, 1};
+    else
+        return NwSplit{*reinterpret_cast<volatile int *>(&a.hdr->pfn_whole),
+                       *reinterpret_cast<volatile int *>(&a.hdr->pfn_split)};
+}
+
+template <int MODE>
+__device__ __forceinline__ PfTile nw_item(const PrefillArgs &a, const NwSplit &sp, int item) {
+    if constexpr (MODE == PF_SHARED) {
+        return pf_shared_item(a, item);
+    } else {
+        if (item < sp.whole) return pf_tile(a, item);
+        const int j = item - sp.whole, sid = j / sp.k, piece = j - sid * sp.k;
+        PfTile t = pf_tile(a, sp.whole + sid);
+        // KV tiles [n0, n1) of the item's range; positions relative to the piece
+        const int n0 = piece * t.nkv / sp.k, n1 = (piece + 1) * t.nkv / sp.k;
+        t.kv0 = n0 * PN;
+        t.L = min(n1 * PN, t.L) - t.kv0;
+        t.C -= t.kv0;
+        t.nkv = n1 - n0;
+        t.piece = piece;
+        t.np = sp.k;
+        t.sid = sid;
+        return t;
+    }
+}
+
 // ----------------------------------------------------------- MMA issuers
 
 template <int KV, int MODE>
-__device__ void nw_mma(uint8_t *smem, const PrefillArgs &a, const NwBars &bb, uint32_t tmem,
+__device__ void nw_mma(uint8_t *smem, const PrefillArgs &a, const NwSplit &sp, const NwBars &bb, uint32_t tmem,
                        volatile int *abort_flag, int total, bool pv_role) {
     using L = NwL<KV>;
     constexpr int R = L::R;
@@ -145,15 +183,15 @@ __device__ void nw_mma(uint8_t *smem, const PrefillArgs &a, const NwBars &bb, ui
     int it = 0;
     if (!pv_role) {
         const uint32_t id_s = idesc_f16(PM, PN, BF, false);
-        // Q' (A) and K (B), both K-major: 128-byte rows of 64 dims, one per
-        // row / token; the next 64 dims 128 rows further.  K-step k (16 dims):
-        // byte 32 (k % 4) of the 64-dim block k / 4.
-        const uint64_t dq = sw128_desc(base + L::OFF_Q, 16, 1024);
+        // Q' (A) in tensor memory, two dims per column; K (B) K-major: 128-byte
+        // rows of 64 dims, one per token, the next 64 dims PN rows further.
+        // K-step k (16 dims): columns 8 k .. 8 k + 7 of Q', byte 32 (k % 4)
+        // of K's 64-dim block k / 4.
         const uint64_t dk0 = sw128_desc(base + L::OFF_K, 16, 1024);
         int kc = 0, sc = 0;
         for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++it) {
-            const PfTile t = pf_item<MODE>(a, item);
-            if (!wait(bb.qfull, it & 1)) break;   // this item's Q' is in shared memory
+            const PfTile t = nw_item<MODE>(a, sp, item);
+            if (!wait(bb.qfull, it & 1)) break;   // this item's Q' is in tensor memory
             for (int n = 0; n < t.nkv && ok; ++n) {   // S(n) into tensor-memory buffer sc & 1
                 const int ks = kc % R, b = sc & 1;
                 if (!wait(bb.kfull[ks], (kc / R) & 1)) break;
@@ -161,10 +199,9 @@ __device__ void nw_mma(uint8_t *smem, const PrefillArgs &a, const NwBars &bb, ui
                 tc_fence_after_sync();
                 const uint64_t dk = dk0 + (uint64_t)(ks * (KV_BYTES >> 4));
 #pragma unroll
-                for (int k = 0; k < PD / 16; ++k) {
-                    const uint64_t step = (uint64_t)((((k >> 2) * (128 * 128)) + (k & 3) * 32) >> 4);
-                    umma_f16(tmem + NW_S + b * PN, dq + step, dk + step, id_s, k > 0 ? 1u : 0u);
-                }
+                for (int k = 0; k < PD / 16; ++k)
+                    umma_f16_ts(tmem + NW_S + b * PN, tmem + NW_Q + 8 * k,
+                                dk + (uint64_t)((((k >> 2) * (PN * 128)) + (k & 3) * 32) >> 4), id_s, k > 0 ? 1u : 0u);
                 umma_commit(bb.sfull[b]);
                 umma_commit(bb.kempty[ks]);
                 ++kc;
@@ -179,9 +216,9 @@ __device__ void nw_mma(uint8_t *smem, const PrefillArgs &a, const NwBars &bb, ui
         const uint64_t dv0 = sw128_desc(base + L::OFF_V, PN * 128, 1024);
         int vc = 0, pc = 0;
         for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++it) {
-            const PfTile t = pf_item<MODE>(a, item);
+            const PfTile t = nw_item<MODE>(a, sp, item);
             for (int n = 0; n < t.nkv && ok; ++n) {
-                const int pb = pc & 1;
+                const int pb = pc & 1;   // barrier parity of PV number pc (one P buffer)
                 if (!wait(bb.pfull[pb], (pc >> 1) & 1)) break;
                 ++pc;
                 const int vs = vc % R;
@@ -190,7 +227,7 @@ __device__ void nw_mma(uint8_t *smem, const PrefillArgs &a, const NwBars &bb, ui
                 const uint64_t dv = dv0 + (uint64_t)(vs * (KV_BYTES >> 4));
 #pragma unroll
                 for (int k = 0; k < PN / 16; ++k)
-                    umma_f16_ts(tmem + NW_O, tmem + NW_P + pb * (PN / 2) + 8 * k,
+                    umma_f16_ts(tmem + NW_O, tmem + NW_P + 8 * k,
                                 dv + (uint64_t)((k * 16 * 128) >> 4), id_o, (n > 0 || k > 0) ? 1u : 0u);
                 umma_commit(bb.pvdone[pb]);
                 umma_commit(bb.vempty[vs]);
@@ -203,7 +240,7 @@ __device__ void nw_mma(uint8_t *smem, const PrefillArgs &a, const NwBars &bb, ui
 // ------------------------------------------------------------- softmax
 
 template <int KV, int MODE>
-__device__ void nw_softmax(uint8_t *smem, const PrefillArgs &a, const NwBars &bb, uint32_t tmem,
+__device__ void nw_softmax(uint8_t *smem, const PrefillArgs &a, const NwSplit &sp, const NwBars &bb, uint32_t tmem,
                            volatile int *abort_flag, int total) {
     using L = NwL<KV>;
     constexpr int R = L::R;
@@ -212,11 +249,10 @@ __device__ void nw_softmax(uint8_t *smem, const PrefillArgs &a, const NwBars &bb
     const int tl = quarter * 32 + lane;           // this thread's tensor-memory lane
     const uint32_t trow = tmem + ((uint32_t)(quarter * 32) << 16);
     const float sl2 = a.scale_log2;
-    uint8_t *qt = smem + L::OFF_Q;
     // this CTA's merge scratch: per item parity, O as [quarter][dim][row] and
     // (m, l) as [quarter][row]
     float *scr = reinterpret_cast<float *>(a.scratch + (size_t)blockIdx.x * NW_SCRATCH_PER_CTA);
-    int sc = 0, g = 0, vcount = 0, it = 0;
+    int sc = 0, g = 0, vcount = 0, it = 0, mph = 0;   // mph: phases of `merged` used
     bool ok = true;
     // every thread of a warp takes the same decision, so warp-collective
     // instructions are never reached by part of a warp
@@ -230,52 +266,53 @@ __device__ void nw_softmax(uint8_t *smem, const PrefillArgs &a, const NwBars &bb
         }
         return ok;
     };
-    // Q': thread tl copies 16-byte chunk tl % 16 of item rows tl / 16 + 8 j
-    // (j < 4) into all four quarters; zeros past the item's rows
-    const int qc = tl & 15;
-    auto q_src = [&](const PfTile &tq, int r) -> const uint4 * {
-        const int tok = r / a.G, hh = r - tok * a.G;
+    // Q': this thread's lane holds row `lane` of the item (every quarter a
+    // copy), 128 dims two per column; zeros past the item's rows
+    auto q_src = [&](const PfTile &tq) -> const uint4 * {
+        const int tok = lane / a.G, hh = lane - tok * a.G;
         if (tok >= tq.ntok) return nullptr;
         return reinterpret_cast<const uint4 *>(a.query +
-                                               ((long long)(tq.q0 + tq.row0 + tok) * a.Hq + tq.kvh * a.G + hh) * PD) +
-               qc;
+                                               ((long long)(tq.q0 + tq.row0 + tok) * a.Hq + tq.kvh * a.G + hh) * PD);
     };
     auto store_q = [&](const PfTile &tq) {
+        const uint4 *src = q_src(tq);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int r = (tl >> 4) + 8 * j;
-            const uint4 *src = q_src(tq, r);
-            const uint4 x = src ? __ldg(src) : make_uint4(0, 0, 0, 0);
+        for (int h = 0; h < 2; ++h) {
+            uint32_t r[32];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int m = 32 * q + r;   // tile row; m % 8 == r % 8
-                *reinterpret_cast<uint4 *>(qt + (qc >> 3) * (128 * 128) + m * 128 + (((qc & 7) ^ (r & 7)) << 4)) = x;
+            for (int c = 0; c < 8; ++c) {
+                const uint4 x = src ? __ldg(src + 8 * h + c) : make_uint4(0, 0, 0, 0);
+                r[4 * c] = x.x;
+                r[4 * c + 1] = x.y;
+                r[4 * c + 2] = x.z;
+                r[4 * c + 3] = x.w;
             }
+            tmem_st32(trow + NW_Q + 32 * h, r);
         }
-        fence_proxy_async_smem();   // for the tensor cores
+        tmem_wait_st();
+        tc_fence_before_sync();
         mbar_arrive(bb.qfull);
     };
     // P columns of the other quarters' tokens stay zero: each thread writes
-    // only its quarter's 16 columns of either buffer
+    // only its quarter's 16 columns
     {
         uint32_t z[32];
 #pragma unroll
         for (int c = 0; c < 32; ++c) z[c] = 0;
         tmem_st32(trow + NW_P, z);
         tmem_st32(trow + NW_P + 32, z);
-        tmem_st32(trow + NW_P + 64, z);
-        tmem_st32(trow + NW_P + 96, z);
         tmem_wait_st();
     }
-    if ((int)blockIdx.x < total) store_q(pf_item<MODE>(a, blockIdx.x));
+    if ((int)blockIdx.x < total) store_q(nw_item<MODE>(a, sp, blockIdx.x));
     for (int item = blockIdx.x; item < total && ok; item += gridDim.x, ++it) {
-        const PfTile t = pf_item<MODE>(a, item);
+        const PfTile t = nw_item<MODE>(a, sp, item);
         const bool has_next = item + (int)gridDim.x < total;
-        const PfTile tn = pf_item<MODE>(a, has_next ? item + (int)gridDim.x : item);
+        const PfTile tn = nw_item<MODE>(a, sp, has_next ? item + (int)gridDim.x : item);
         if (has_next) {
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (const uint4 *src = q_src(tn, (tl >> 4) + 8 * j)) prefetch_l2(src);
+            if (const uint4 *src = q_src(tn)) {
+                prefetch_l2(src);
+                prefetch_l2(src + 8);
+            }
         }
         // positions this row sees: up to its own new token (causal), or the
         // whole range (shared); the first row's bound decides whether a tile
@@ -362,9 +399,8 @@ __device__ void nw_softmax(uint8_t *smem, const PrefillArgs &a, const NwBars &bb
                 }
             }
             // ---- p = 2^(s scale log2(e) - m) for this quarter's tokens, into
-            // this thread's 16 columns of P buffer g & 1 (PV number g - 2 read it
-            // before); while no token of the quarter has been seen (maximum
-            // -inf) p is 0
+            // this thread's 16 columns of P (PV number g - 1 read it before);
+            // while no token of the quarter has been seen (maximum -inf) p is 0
             const float msub = mrun == -INFINITY ? 0.f : mrun;
             uint32_t pw[16];
             float lp[4] = {0.f, 0.f, 0.f, 0.f};
@@ -376,8 +412,8 @@ __device__ void nw_softmax(uint8_t *smem, const PrefillArgs &a, const NwBars &bb
                 pw[c] = pack_p<KV>(p0, p1);
             }
             l += (lp[0] + lp[1]) + (lp[2] + lp[3]);
-            if (g >= 2 && !wait(bb.pvdone[g & 1], ((g - 2) >> 1) & 1)) break;
-            tmem_st16(trow + NW_P + (g & 1) * (PN / 2) + 16 * quarter, pw);
+            if (g >= 1 && !wait(bb.pvdone[(g - 1) & 1], ((g - 1) >> 1) & 1)) break;
+            tmem_st16(trow + NW_P + 16 * quarter, pw);
             tmem_wait_st();
             if (zero_v) fence_proxy_async_smem();   // the zeroed V rows, for the tensor cores
             tc_fence_before_sync();
@@ -403,7 +439,8 @@ __device__ void nw_softmax(uint8_t *smem, const PrefillArgs &a, const NwBars &bb
         tc_fence_before_sync();
         __threadfence_block();
         mbar_arrive(bb.merged);
-        if (!wait(bb.merged, it & 1)) break;
+        if (!wait(bb.merged, mph & 1)) break;
+        ++mph;
         // row `lane`: its maximum over all positions, each quarter's weight,
         // its sum; this thread then writes dims 32 quarter .. 32 quarter + 31
         float2 mlq[4];
@@ -428,6 +465,67 @@ __device__ void nw_softmax(uint8_t *smem, const PrefillArgs &a, const NwBars &bb
 #pragma unroll
             for (int q = 0; q < 4; ++q) x = fmaf(wq[q], __ldcg(so + (q * PD + d) * 32 + lane), x);
             ov[c] = x;
+        }
+        if constexpr (MODE == PF_CAUSAL) {
+            if (t.np > 1) {
+                // A piece of a split item: its partial rows (unnormalised O and
+                // (m, l)) into the split area; the CTA that completes the item's
+                // last piece (its ticket) merges the pieces into the output.
+                const NwSplitArea sa = nw_split_area(a.scratch);
+                const int slot = t.sid * t.np + t.piece;
+                float *po = sa.o + ((size_t)slot * 32 + lane) * PD + 32 * quarter;
+#pragma unroll
+                for (int c = 0; c < 32; c += 4)
+                    *reinterpret_cast<float4 *>(po + c) =
+                        bad ? make_float4(qnan, qnan, qnan, qnan) : make_float4(ov[c], ov[c + 1], ov[c + 2], ov[c + 3]);
+                if (quarter == 0) sa.ml[slot * 32 + lane] = bad ? make_float2(qnan, qnan) : make_float2(mall, lall);
+                __threadfence();
+                mbar_arrive(bb.merged);
+                if (!wait(bb.merged, mph & 1)) break;
+                ++mph;
+                volatile int *last = reinterpret_cast<volatile int *>(smem + L::OFF_CTRL + CTRL_ABORT + 4);
+                if (tl == 0) *last = atomicAdd(sa.tickets + t.sid, 1) == t.np - 1;
+                mbar_arrive(bb.merged);
+                if (!wait(bb.merged, mph & 1)) break;
+                ++mph;
+                if (!*last) continue;
+                __threadfence();
+                const int s0 = t.sid * t.np;
+                float mp = -INFINITY;
+                for (int p = 0; p < t.np; ++p) mp = fmaxf(mp, __ldcg(sa.ml + (s0 + p) * 32 + lane).x);
+                float lp = 0.f, acc[32];
+#pragma unroll
+                for (int c = 0; c < 32; ++c) acc[c] = 0.f;
+                for (int p = 0; p < t.np; ++p) {
+                    const float2 ml = __ldcg(sa.ml + (s0 + p) * 32 + lane);
+                    const float w = fast_exp2(ml.x - mp);   // NaN from a piece that met a bad block id
+                    lp += w * ml.y;
+                    const float *pp = sa.o + ((size_t)(s0 + p) * 32 + lane) * PD + 32 * quarter;
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(pp + c));
+                        acc[c] = fmaf(w, x.x, acc[c]);
+                        acc[c + 1] = fmaf(w, x.y, acc[c + 1]);
+                        acc[c + 2] = fmaf(w, x.z, acc[c + 2]);
+                        acc[c + 3] = fmaf(w, x.w, acc[c + 3]);
+                    }
+                }
+                if (valid) {
+                    const float inv = a.v_scale / lp;
+                    uint16_t *orow =
+                        a.out + ((long long)(t.q0 + t.row0 + tok) * a.Hq + t.kvh * a.G + hh) * PD + 32 * quarter;
+#pragma unroll
+                    for (int c = 0; c < 32; c += 8) {
+                        uint4 v;
+                        v.x = (uint32_t)out_bits<KV>(acc[c] * inv) | ((uint32_t)out_bits<KV>(acc[c + 1] * inv) << 16);
+                        v.y = (uint32_t)out_bits<KV>(acc[c + 2] * inv) | ((uint32_t)out_bits<KV>(acc[c + 3] * inv) << 16);
+                        v.z = (uint32_t)out_bits<KV>(acc[c + 4] * inv) | ((uint32_t)out_bits<KV>(acc[c + 5] * inv) << 16);
+                        v.w = (uint32_t)out_bits<KV>(acc[c + 6] * inv) | ((uint32_t)out_bits<KV>(acc[c + 7] * inv) << 16);
+                        *reinterpret_cast<uint4 *>(orow + c) = v;
+                    }
+                }
+                continue;
+            }
         }
         if constexpr (MODE == PF_SHARED) {
             // the member's partial row of this shared range: unnormalised O
@@ -472,6 +570,7 @@ __global__ void __launch_bounds__(NwL<KV>::THREADS, 1) narrow_kernel(const __gri
     const int warp = threadIdx.x >> 5;
     const int total = nw_total<MODE>(a);   // written by the prep kernel
     if ((int)blockIdx.x >= total) return;  // no work item for this CTA (the whole CTA leaves)
+    const NwSplit sp = nw_split<MODE>(a, total);
     if (threadIdx.x == 0) {
         constexpr uint32_t fill = L::F8 ? 4 : 1;   // FP8: four converting warps per ring
         for (int s = 0; s < L::R; ++s) {
@@ -508,12 +607,12 @@ __global__ void __launch_bounds__(NwL<KV>::THREADS, 1) narrow_kernel(const __gri
     tc_fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + (bb.tmem_slot - smem_u32(smem)));
     auto range = [&](int item) {
-        const PfTile t = pf_item<MODE>(a, item);
+        const PfTile t = nw_item<MODE>(a, sp, item);
         return PfRange{t.seq, t.kvh, t.nkv, t.L, t.kv0};
     };
     if (warp == 2 || warp == 3) {
         if ((threadIdx.x & 31) == 0) {
-            nw_mma<KV, MODE>(smem, a, bb, tmem, abort_flag, total, warp == 3);
+            nw_mma<KV, MODE>(smem, a, sp, bb, tmem, abort_flag, total, warp == 3);
             // every MMA issued (by both threads) has completed before tensor
             // memory is released
             umma_commit(bb.flags);
@@ -521,7 +620,7 @@ __global__ void __launch_bounds__(NwL<KV>::THREADS, 1) narrow_kernel(const __gri
         }
         __syncwarp();
     } else if (warp >= NW_SOFT0 && warp < NW_SOFT0 + 4) {
-        nw_softmax<KV, MODE>(smem, a, bb, tmem, abort_flag, total);
+        nw_softmax<KV, MODE>(smem, a, sp, bb, tmem, abort_flag, total);
     } else if (warp < 2) {
         if constexpr (L::F8) {   // the codes of K (warp 0) and V (warp 1) into their staging rings
             const int off[1] = {warp ? L::OFF_V8 : L::OFF_K8};
@@ -542,7 +641,7 @@ __global__ void __launch_bounds__(NwL<KV>::THREADS, 1) narrow_kernel(const __gri
             pf_convert_ring<L::R, L::S8, 4>(smem + (kv ? L::OFF_V8 : L::OFF_K8), smem + (kv ? L::OFF_V : L::OFF_K),
                                             kv ? bb.v8full : bb.k8full, kv ? bb.v8empty : bb.k8empty,
                                             kv ? bb.vfull : bb.kfull, kv ? bb.vempty : bb.kempty, a, abort_flag,
-                                            total, warp & 3, [&](int item) { return pf_item<MODE>(a, item).nkv; });
+                                            total, warp & 3, [&](int item) { return nw_item<MODE>(a, sp, item).nkv; });
         }
     }
     tc_fence_before_sync();
@@ -600,6 +699,8 @@ int launch_narrow_shared(const CUtensorMap &tmk, const CUtensorMap &tmv, const P
                          long long max_items, cudaStream_t st) {
     return launch_narrow_kv<PA_KV_F16, PF_SHARED>(tmk, tmv, args, max_items, st);
 }
+
+int narrow_grid() { return narrow_setup<PA_KV_F16, PF_CAUSAL>().grid; }
 
 bool narrow_usable(int kv) {
     if (kv == PA_KV_BF16) return narrow_setup<PA_KV_BF16, PF_CAUSAL>().err == cudaSuccess;

@@ -71,9 +71,13 @@ int launch_narrow(int kv, const CUtensorMap &tmk, const CUtensorMap &tmv, const 
                   long long max_items, cudaStream_t st);
 int launch_narrow_shared(const CUtensorMap &tmk, const CUtensorMap &tmv, const PrefillArgs &args,
                          long long max_items, cudaStream_t st);
-// Whether the narrow kernel can run for this cache type (for an FP8 cache:
-// built with the register count its register split assumes); checked once.
+// Whether the narrow kernel can run for this cache type; checked once.
 bool narrow_usable(int kv);
+
+// CTAs the narrow kernel launches (one per SM, at most NW_MAX_CTAS); the
+// causal prep kernel splits the items of the last, partial round into pieces
+// for this many CTAs.
+int narrow_grid();
 
 // Whether the one-tile kernel can run for this cache type (for an FP8 cache:
 // built with the register count its register split assumes); checked once.

@@ -40,8 +40,12 @@ constexpr int PF_CAUSAL = 0, PF_SHARED = 1;
 // seq: the block-table row; tokens kv0 .. kv0 + L - 1 of it are the KV range,
 // nkv tiles of PN tokens; rows: ntok query tokens (or members) from query row
 // q0 + row0, G heads each; C: positions the first new token sees (causal).
+// piece / np / sid: a work item may be one of np pieces of a sequence's KV
+// range (the narrow kernel's split of its last round of items); sid indexes
+// the split items (-1: a whole item).
 struct PfTile {
     int seq, kvh, row0, ntok, C, nkv, L, q0, kv0;
+    int piece, np, sid;
 };
 
 // Row tile `rt` (128 / G consecutive new tokens) of sequence `seq`, kv head kvh.
@@ -58,6 +62,9 @@ __device__ __forceinline__ PfTile pf_row_tile(const PrefillArgs &a, int seq, int
     t.C = t.L - T + 1;                      // positions the first new token sees
     t.nkv = (t.C + t.row0 + t.ntok - 1 + PN - 1) / PN;
     t.kv0 = 0;
+    t.piece = 0;
+    t.np = 1;
+    t.sid = -1;
     return t;
 }
 
@@ -83,6 +90,9 @@ __device__ __forceinline__ PfTile pf_shared_item(const PrefillArgs &a, int item)
     t.L = rec.w - rec.z; // tokens of the range
     t.C = t.L;
     t.nkv = (t.L + PN - 1) / PN;
+    t.piece = 0;
+    t.np = 1;
+    t.sid = -1;
     return t;
 }
 
