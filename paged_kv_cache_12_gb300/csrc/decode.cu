@@ -961,19 +961,22 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     pa_.scale_log2 = args.scale_log2;   // with the K scale of an FP8 cache
     pa_.v_scale = args.v_scale;
     pa_.wait_limit = wait_limit_cycles();
-    // the tensor-core kernels on `on`: the narrow items, pairs (the long
-    // chunks), then the sequences of one row tile
+    // the tensor-core kernels on `on`: pairs (the long chunks) first, then
+    // the narrow items and the sequences of one row tile.  The host does not
+    // know which lists are empty; a kernel with none still claims a whole SM
+    // per CTA while it starts, so an empty one must not stand between the
+    // decode pipeline on the side stream and the long chunks.
     auto tensor_core = [&](cudaStream_t on) {
+        if (pairs) {
+            const int rc2 = launch_prefill2(kv, tmk, tmv, pa_, (L.ptile_cap + 1) / 2 * num_kv_heads, on);
+            if (rc2 != PA_OK) return rc2;
+        }
         if (narrow) {
             PrefillArgs na = pa_;
             na.tiles = ntiles;
             na.scratch = ws + L.nscr;
             const int rcn = launch_narrow(kv, tmk, tmv, na, narrow_grid(), on);
             if (rcn != PA_OK) return rcn;
-        }
-        if (pairs) {
-            const int rc2 = launch_prefill2(kv, tmk, tmv, pa_, (L.ptile_cap + 1) / 2 * num_kv_heads, on);
-            if (rc2 != PA_OK) return rc2;
         }
         return launch_prefill(kv, tmk, tmv, pa_, L.ptile_cap * num_kv_heads, on);
     };

@@ -28,8 +28,8 @@
 //
 // One CTA per SM, persistent over the item list; warps:
 //   0, 1   producers: K and V tiles of 128 tokens by TMA through the block
-//          table (16-bit caches: 3-stage rings; FP8: the codes, 3-stage
-//          staging rings before 2-stage 16-bit rings);
+//          table (16-bit caches: 4-stage K and 3-stage V rings; FP8: the
+//          codes, 3-stage staging rings before 2-stage 16-bit rings);
 //   2, 3   MMA issuers (one thread each): warp 2 the S products, warp 3 the
 //          PV products -- one thread takes about 100 cycles per tcgen05.mma,
 //          two streams halve the time the products hold the pipeline;
@@ -56,8 +56,13 @@ static_assert(NR == 32 && PM == 4 * NR, "four copies of the item's rows fill the
 static_assert(PN == 128, "a quarter of a KV tile per softmax warp: 32 tokens");
 static_assert(NW_O + PD <= NW_TMEM_COLS, "tensor-memory columns");
 
-#ifndef PA_NW_R16
-#define PA_NW_R16 3
+constexpr int NW_MAXST = 4;   // barrier slots per ring
+
+#ifndef PA_NW_RK16
+#define PA_NW_RK16 4
+#endif
+#ifndef PA_NW_RV16
+#define PA_NW_RV16 3
 #endif
 #ifndef PA_NW_R8
 #define PA_NW_R8 2
@@ -72,11 +77,12 @@ static_assert(NW_O + PD <= NW_TMEM_COLS, "tensor-memory columns");
 template <int KV>
 struct NwL {
     static constexpr bool F8 = KV == PA_KV_FP8_E4M3;
-    static constexpr int R = F8 ? PA_NW_R8 : PA_NW_R16;   // 16-bit ring stages
-    static constexpr int S8 = F8 ? PA_NW_S8 : 0;          // FP8 staging stages
+    static constexpr int RK = F8 ? PA_NW_R8 : PA_NW_RK16;   // 16-bit K ring stages
+    static constexpr int RV = F8 ? PA_NW_R8 : PA_NW_RV16;   // 16-bit V ring stages
+    static constexpr int S8 = F8 ? PA_NW_S8 : 0;            // FP8 staging stages
     static constexpr int OFF_K = 0;
-    static constexpr int OFF_V = R * KV_BYTES;
-    static constexpr int OFF_K8 = 2 * R * KV_BYTES;
+    static constexpr int OFF_V = RK * KV_BYTES;
+    static constexpr int OFF_K8 = (RK + RV) * KV_BYTES;
     static constexpr int OFF_V8 = OFF_K8 + S8 * F8_BYTES;
     static constexpr int OFF_CTRL = OFF_V8 + S8 * F8_BYTES;
     static constexpr int SMEM = OFF_CTRL + CTRL_BYTES + 1024;   // + alignment slack
@@ -86,22 +92,23 @@ struct NwL {
     static constexpr int THREADS = (F8 ? 16 : 8) * 32;
     static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
     static_assert(OFF_K8 % 1024 == 0, "swizzled tiles 1024-byte aligned");
-    static_assert(R <= MAXST && S8 <= MAXST, "ring stages");
+    static_assert(RK <= NW_MAXST && RV <= NW_MAXST && S8 <= NW_MAXST, "ring stages");
+    static_assert(!F8 || RK == RV, "the converting warps fill K and V rings of one depth");
 };
 
 struct NwBars {
     // sfull / sfree: S buffers; pfull / pvdone: P buffers (by PV-number parity)
-    BarRing kfull, kempty, vfull, vempty, k8full, v8full, k8empty, v8empty;   // MAXST each
+    BarRing kfull, kempty, vfull, vempty, k8full, v8full, k8empty, v8empty;   // NW_MAXST each
     BarRing sfull, sfree, pfull, pvdone;                                      // 2 each
     uint32_t qfull, merged, tmem_slot, flags;                                 // shared addresses
 };
-static_assert(8 * (8 * MAXST + 8 + 4) <= CTRL_BAD, "control block layout");
+static_assert(8 * (8 * NW_MAXST + 8 + 4) <= CTRL_BAD, "control block layout");
 
 __device__ __forceinline__ NwBars nw_bars(uint8_t *smem, int off_ctrl) {
     uint32_t a = smem_u32(smem + off_ctrl);
     NwBars b;
     BarRing *rings[8] = {&b.kfull, &b.kempty, &b.vfull, &b.vempty, &b.k8full, &b.v8full, &b.k8empty, &b.v8empty};
-    for (int r = 0; r < 8; ++r) rings[r]->base = a, a += 8 * MAXST;
+    for (int r = 0; r < 8; ++r) rings[r]->base = a, a += 8 * NW_MAXST;
     BarRing *pairs[4] = {&b.sfull, &b.sfree, &b.pfull, &b.pvdone};
     for (int r = 0; r < 4; ++r) pairs[r]->base = a, a += 16;
     b.qfull = a, a += 8;
@@ -167,7 +174,7 @@ template <int KV, int MODE>
 __device__ void nw_mma(uint8_t *smem, const PrefillArgs &a, const NwSplit &sp, const NwBars &bb, uint32_t tmem,
                        volatile int *abort_flag, int total, bool pv_role) {
     using L = NwL<KV>;
-    constexpr int R = L::R;
+    constexpr int RK = L::RK, RV = L::RV;
     constexpr bool BF = KV == PA_KV_BF16;
     const uint32_t base = smem_u32(smem);
     bool ok = true;
@@ -193,8 +200,8 @@ __device__ void nw_mma(uint8_t *smem, const PrefillArgs &a, const NwSplit &sp, c
             const PfTile t = nw_item<MODE>(a, sp, item);
             if (!wait(bb.qfull, it & 1)) break;   // this item's Q' is in tensor memory
             for (int n = 0; n < t.nkv && ok; ++n) {   // S(n) into tensor-memory buffer sc & 1
-                const int ks = kc % R, b = sc & 1;
-                if (!wait(bb.kfull[ks], (kc / R) & 1)) break;
+                const int ks = kc % RK, b = sc & 1;
+                if (!wait(bb.kfull[ks], (kc / RK) & 1)) break;
                 if (sc >= 2 && !wait(bb.sfree[b], ((sc >> 1) - 1) & 1)) break;
                 tc_fence_after_sync();
                 const uint64_t dk = dk0 + (uint64_t)(ks * (KV_BYTES >> 4));
@@ -221,8 +228,8 @@ __device__ void nw_mma(uint8_t *smem, const PrefillArgs &a, const NwSplit &sp, c
                 const int pb = pc & 1;   // barrier parity of PV number pc (one P buffer)
                 if (!wait(bb.pfull[pb], (pc >> 1) & 1)) break;
                 ++pc;
-                const int vs = vc % R;
-                if (!wait(bb.vfull[vs], (vc / R) & 1)) break;
+                const int vs = vc % RV;
+                if (!wait(bb.vfull[vs], (vc / RV) & 1)) break;
                 tc_fence_after_sync();
                 const uint64_t dv = dv0 + (uint64_t)(vs * (KV_BYTES >> 4));
 #pragma unroll
@@ -243,7 +250,7 @@ template <int KV, int MODE>
 __device__ void nw_softmax(uint8_t *smem, const PrefillArgs &a, const NwSplit &sp, const NwBars &bb, uint32_t tmem,
                            volatile int *abort_flag, int total) {
     using L = NwL<KV>;
-    constexpr int R = L::R;
+    constexpr int RV = L::RV;
     const int lane = threadIdx.x & 31;            // the row r of the item
     const int quarter = (threadIdx.x >> 5) & 3;   // tensor-memory lanes 32 quarter .. + 31; tokens 32 quarter ..
     const int tl = quarter * 32 + lane;           // this thread's tensor-memory lane
@@ -384,8 +391,8 @@ __device__ void nw_softmax(uint8_t *smem, const PrefillArgs &a, const NwSplit &s
             }
             // ---- the last KV tile: V rows past the range are zeroed (P is 0
             // there, but the rows hold stale bits)
-            const int vs = vcount % R;
-            const int vphase = (vcount / R) & 1;
+            const int vs = vcount % RV;
+            const int vphase = (vcount / RV) & 1;
             ++vcount;
             const bool zero_v = t0 + PN > t.L;
             if (zero_v) {
@@ -573,9 +580,11 @@ __global__ void __launch_bounds__(NwL<KV>::THREADS, 1) narrow_kernel(const __gri
     const NwSplit sp = nw_split<MODE>(a, total);
     if (threadIdx.x == 0) {
         constexpr uint32_t fill = L::F8 ? 4 : 1;   // FP8: four converting warps per ring
-        for (int s = 0; s < L::R; ++s) {
+        for (int s = 0; s < L::RK; ++s) {
             mbar_init(bb.kfull[s], fill);
             mbar_init(bb.kempty[s], 1);
+        }
+        for (int s = 0; s < L::RV; ++s) {
             mbar_init(bb.vfull[s], fill);
             mbar_init(bb.vempty[s], 1);
         }
@@ -633,12 +642,15 @@ __global__ void __launch_bounds__(NwL<KV>::THREADS, 1) narrow_kernel(const __gri
             const BarRing full[1] = {warp ? bb.vfull : bb.kfull};
             const BarRing empty[1] = {warp ? bb.vempty : bb.kempty};
             const CUtensorMap *maps[1] = {warp ? &tmv : &tmk};
-            pf_stream<L::R, false, 1>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total, range);
+            if (warp)
+                pf_stream<L::RV, false, 1>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total, range);
+            else
+                pf_stream<L::RK, false, 1>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total, range);
         }
     } else if constexpr (L::F8) {
         if (warp >= 8) {   // 8-11: K; 12-15: V; a quarter of the rows each
             const int kv = (warp - 8) >> 2;
-            pf_convert_ring<L::R, L::S8, 4>(smem + (kv ? L::OFF_V8 : L::OFF_K8), smem + (kv ? L::OFF_V : L::OFF_K),
+            pf_convert_ring<L::RK, L::S8, 4>(smem + (kv ? L::OFF_V8 : L::OFF_K8), smem + (kv ? L::OFF_V : L::OFF_K),
                                             kv ? bb.v8full : bb.k8full, kv ? bb.v8empty : bb.k8empty,
                                             kv ? bb.vfull : bb.kfull, kv ? bb.vempty : bb.kempty, a, abort_flag,
                                             total, warp & 3, [&](int item) { return nw_item<MODE>(a, sp, item).nkv; });
