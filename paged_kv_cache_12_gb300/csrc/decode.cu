@@ -99,7 +99,7 @@ __device__ __forceinline__ int block_exclusive_scan(int x, int *warp_sums, int *
 __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
     const int32_t *__restrict__ context_lens, const int32_t *__restrict__ lead,
     const int32_t *__restrict__ shared_len, int B, int Hq, int D, int Hkv, int bs, int max_ctx,
-    long long max_table_tokens, int pt, int ms, WsHeader *hdr, int *part_off, int *gsize, int *gshared,
+    long long max_table_tokens, int pt, int pts, int ms, WsHeader *hdr, int *part_off, int *gsize, int *gshared,
     ItemRec *items, int *grp, uint16_t *out, uint32_t nan2, int mt, int4 *sitems) {
     constexpr int NBK = MAX_PART_TOKENS / CHUNK;     // length buckets of the short items
     __shared__ int warp_sums[PREP_THREADS / 32];
@@ -151,13 +151,13 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
             else if (L == 0)
                 code = 1;
             else
-                P = partitions_of(L, S, pt);
+                P = partitions_of(L, S, pt, pts);
             if (P > 0) {
                 nfull = (L - S + pt - 1) / pt - 1;   // own partitions but the last
                 if (ld == i && S > 0) {
                     Ms = gsize[i];
-                    Ps = (S + pt - 1) / pt;
-                    if (!mt) nfull += (S / pt) * ((Ms + ms - 1) / ms);
+                    Ps = (S + pts - 1) / pts;
+                    if (!mt) nfull += (S / pts) * ((Ms + ms - 1) / ms);
                 }
             }
         }
@@ -171,20 +171,20 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
         if (i < B) {
             part_off[i] = ep;
             if (P > 0) {
-                const int ps_i = (S + pt - 1) / pt;
+                const int ps_i = (S + pts - 1) / pts;
                 if (Ps > 0 && mt) {   // leader: its shared ranges, for the tensor-core kernel
                     for (int p = 0; p < Ps; ++p)
                         for (int k = 0; k < Ms; k += mt)
-                            sitems[es++] = make_int4(i + k, min(mt, Ms - k), p * pt, min((p + 1) * pt, S));
-                } else if (Ps > 0) {   // leader: full shared items
-                    for (int p = 0; p < S / pt; ++p)
+                            sitems[es++] = make_int4(i + k, min(mt, Ms - k), p * pts, min((p + 1) * pts, S));
+                } else if (Ps > 0) {   // leader: full shared items (pts == pt here)
+                    for (int p = 0; p < S / pts; ++p)
                         for (int k = 0; k < Ms; k += ms) {
                             ItemRec r;
-                            r.a = make_int4(i + k, min(ms, Ms - k), p * pt, (p + 1) * pt);
+                            r.a = make_int4(i + k, min(ms, Ms - k), p * pts, (p + 1) * pts);
                             r.b = make_int4(p, S, L, -1);
                             items[ef++] = r;
                         }
-                    if (S % pt) atomicAdd(&hist[(pt - S % pt) / CHUNK], (Ms + ms - 1) / ms);
+                    if (S % pts) atomicAdd(&hist[(pts - S % pts) / CHUNK], (Ms + ms - 1) / ms);
                 }
                 const int pp = (L - S + pt - 1) / pt;      // own partitions
                 for (int p = 0; p + 1 < pp; ++p) {         // all full but the last
@@ -222,14 +222,14 @@ __global__ void __launch_bounds__(PREP_THREADS) decode_prep_kernel(
         if (L <= 0 || !valid_len(L)) continue;
         int ld;
         const int S = shared_of(i, ld);
-        const int ps_i = (S + pt - 1) / pt;
-        if (!mt && ld == i && S > 0 && S % pt) {
+        const int ps_i = (S + pts - 1) / pts;
+        if (!mt && ld == i && S > 0 && S % pts) {
             const int Ms = gsize[i];
             for (int k = 0; k < Ms; k += ms) {
                 ItemRec r;
-                r.a = make_int4(i + k, min(ms, Ms - k), S / pt * pt, S);
+                r.a = make_int4(i + k, min(ms, Ms - k), S / pts * pts, S);
                 r.b = make_int4(ps_i - 1, S, L, -1);
-                items[atomicAdd(&cursor[(pt - S % pt) / CHUNK], 1)] = r;
+                items[atomicAdd(&cursor[(pts - S % pts) / CHUNK], 1)] = r;
             }
         }
         const int pp = (L - S + pt - 1) / pt;
@@ -569,6 +569,18 @@ bool narrow_enabled() {
     return on;
 }
 
+// Shared-range pieces on the tensor cores span this many decode partitions
+// (PA_SHARED_PIECE, read once; default 4: on the parallel-sampling workload a
+// whole 2048-token prompt per piece, 1 % faster than pieces of one partition).
+int shared_piece_factor() {
+    static const int f = [] {
+        const char *e = std::getenv("PA_SHARED_PIECE");
+        const int v = e ? std::atoi(e) : 4;
+        return v >= 1 && v <= 64 ? v : 4;
+    }();
+    return f;
+}
+
 // Whether shared ranges of at most NARROW_ROWS rows go to the narrow kernel
 // (only with PA_NARROW_SHARED=1, read once).
 bool narrow_shared_enabled() {
@@ -766,9 +778,13 @@ int decode_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     uint16_t *hout = out;
 
     int4 *sitems = reinterpret_cast<int4 *>(ws + L.ptiles);
+    // shared ranges on the tensor cores are cut into longer pieces than the
+    // decode partitions: each piece is a tensor-core item with its start-up and
+    // epilogue, and each member merges one partial per piece
+    const int pts = tc ? L.pt * shared_piece_factor() : L.pt;
     decode_prep_kernel<<<1, PREP_THREADS, 0, st>>>(context_lens, lead, shared_len, num_seqs, num_heads, head_dim,
                                                    num_kv_heads, block_size, max_context_len,
-                                                   (long long)max_blocks_per_seq * block_size, L.pt, ms, hdr,
+                                                   (long long)max_blocks_per_seq * block_size, L.pt, pts, ms, hdr,
                                                    part_off, gsize, gshared, items, grp, hout, nan_pair(kv), mt,
                                                    sitems);
     if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
@@ -794,7 +810,7 @@ int decode_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
         pa_.part_off = part_off;
         pa_.ws_ml = ws_ml;
         pa_.ws_o = ws_o;
-        pa_.pt = L.pt;
+        pa_.pt = pts;
         pa_.scratch = ws + L.nscr;
         const int rc = tcn ? launch_narrow_shared(tmk, tmv, pa_, L.ptile_cap * num_kv_heads, st)
                            : launch_shared_ranges(tmk, tmv, pa_, L.ptile_cap * num_kv_heads, st);
@@ -812,6 +828,7 @@ int decode_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     args.bs = block_size;
     args.mbps = max_blocks_per_seq;
     args.pt = L.pt;
+    args.pts = pts;
     args.ms = ms;
     args.num_blocks = num_blocks;
     args.wait_limit = wait_limit_cycles();
@@ -929,6 +946,7 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     args.bs = block_size;
     args.mbps = max_blocks_per_seq;
     args.pt = L.pt;
+    args.pts = L.pt;
     args.ms = ms;
     args.num_blocks = num_blocks;
     args.wait_limit = wait_limit_cycles();

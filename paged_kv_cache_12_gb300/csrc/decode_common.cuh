@@ -223,6 +223,7 @@ struct DecodeArgs {
     const int32_t *block_tables;
     const int32_t *context_lens;
     int Hq, Hkv, G, bs, mbps, pt, ms;
+    int pts;                 // partition length of shared ranges (pt, or longer when the tensor cores take them)
     long long num_blocks;
     long long wait_limit;   // bound of every pipeline wait, clock cycles
     float scale_log2;        // softmax scale (times the K scale of an fp8 cache) * log2(e)
@@ -301,8 +302,10 @@ __host__ __device__ constexpr int swz(int row, int col) {
 // Partitions of one sequence: its shared prefix [0, S) and its own range
 // [S, L), each cut into pieces of pt tokens (S = 0 for a sequence that
 // shares nothing).
-__device__ __forceinline__ int partitions_of(int L, int S, int pt) {
-    return (S + pt - 1) / pt + (L - S + pt - 1) / pt;
+// Partitions of a sequence of L positions whose first S are shared: the shared
+// range in pieces of pts, the rest in pieces of pt.
+__device__ __forceinline__ int partitions_of(int L, int S, int pt, int pts) {
+    return (S + pts - 1) / pts + (L - S + pt - 1) / pt;
 }
 
 namespace {
@@ -459,7 +462,7 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
                         d.nmem = n_rec.a.y;
                         d.pidx = n_rec.b.x;
                         d.shared = n_rec.b.y;
-                        d.P0 = CAUSAL ? 0 : partitions_of(n_rec.b.z, n_rec.b.y, a.pt);
+                        d.P0 = CAUSAL ? 0 : partitions_of(n_rec.b.z, n_rec.b.y, a.pt, a.pts);
                         d.canon0 = n_rec.b.w;
                         d.nchunks = nch[c];
                         d.ntok_last = t1[c] - (t0[c] + (nch[c] - 1) * CHUNK);
@@ -993,7 +996,7 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
                     const int seq = dsc.seq0 + mbr;
                     int P = dsc.P0, canon = dsc.canon0;
                     if (dsc.canon0 < 0) {   // a shared-prefix item: every member has its own P and row
-                        P = partitions_of(__ldg(&a.context_lens[seq]), dsc.shared, a.pt);
+                        P = partitions_of(__ldg(&a.context_lens[seq]), dsc.shared, a.pt, a.pts);
                         canon = __ldg(&a.part_off[seq]) + dsc.pidx;
                     }
                     const int h = dsc.kvh * a.G + g;
@@ -1030,7 +1033,7 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
             owe_seq = dsc.seq0 + lane;
             owe_kvh = dsc.kvh;
             const int Lm = __ldg(&a.context_lens[owe_seq]);
-            owe_P = dsc.canon0 < 0 ? partitions_of(Lm, dsc.shared, a.pt) : dsc.P0;
+            owe_P = dsc.canon0 < 0 ? partitions_of(Lm, dsc.shared, a.pt, a.pts) : dsc.P0;
             owe_T = a.tc_shared ? (Lm - dsc.shared + a.pt - 1) / a.pt : owe_P;
         }
         owe = __any_sync(0xffffffffu, owe_P > 1);
