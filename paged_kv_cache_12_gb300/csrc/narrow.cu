@@ -57,11 +57,6 @@ static_assert(PN == 128, "a quarter of a KV tile per softmax warp: 32 tokens");
 static_assert(NW_O + PD <= NW_TMEM_COLS, "tensor-memory columns");
 
 constexpr int NW_MAXST = 4;   // barrier slots per ring
-#ifndef PA_NW_ONCE
-#define PA_NW_ONCE 1
-#endif
-// every K/V tile of a narrow item is read by one CTA once: L2 evict-first
-constexpr bool NW_ONCE = PA_NW_ONCE != 0;
 
 #ifndef PA_NW_RK16
 #define PA_NW_RK16 4
@@ -641,19 +636,16 @@ __global__ void __launch_bounds__(NwL<KV>::THREADS, 1) narrow_kernel(const __gri
             const BarRing full[1] = {warp ? bb.v8full : bb.k8full};
             const BarRing empty[1] = {warp ? bb.v8empty : bb.k8empty};
             const CUtensorMap *maps[1] = {warp ? &tmv : &tmk};
-            pf_stream<L::S8, true, 1, decltype(range), NW_ONCE>(smem, off, L::OFF_CTRL, full, empty, maps, a,
-                                                                abort_flag, total, range);
+            pf_stream<L::S8, true, 1>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total, range);
         } else {
             const int off[1] = {warp ? L::OFF_V : L::OFF_K};
             const BarRing full[1] = {warp ? bb.vfull : bb.kfull};
             const BarRing empty[1] = {warp ? bb.vempty : bb.kempty};
             const CUtensorMap *maps[1] = {warp ? &tmv : &tmk};
             if (warp)
-                pf_stream<L::RV, false, 1, decltype(range), NW_ONCE>(smem, off, L::OFF_CTRL, full, empty, maps, a,
-                                                                     abort_flag, total, range);
+                pf_stream<L::RV, false, 1>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total, range);
             else
-                pf_stream<L::RK, false, 1, decltype(range), NW_ONCE>(smem, off, L::OFF_CTRL, full, empty, maps, a,
-                                                                     abort_flag, total, range);
+                pf_stream<L::RK, false, 1>(smem, off, L::OFF_CTRL, full, empty, maps, a, abort_flag, total, range);
         }
     } else if constexpr (L::F8) {
         if (warp >= 8) {   // 8-11: K; 12-15: V; a quarter of the rows each
