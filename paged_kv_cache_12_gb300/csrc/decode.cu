@@ -982,21 +982,31 @@ int causal_impl(uint16_t *out, const uint16_t *query, const void *k_cache, const
     // the tensor-core kernels on `on`: pairs (the long chunks) first, then
     // the narrow items and the sequences of one row tile.  The host does not
     // know which lists are empty; a kernel with none still claims a whole SM
-    // per CTA while it starts, so an empty one must not stand between the
-    // decode pipeline on the side stream and the long chunks.
+    // per CTA while it starts, so an empty one launched ahead of a busy one
+    // waits for the decode pipeline's CTAs on the side stream to leave the SMs
+    // and the busy one with it.  Of the narrow and one-tile lists, the one more
+    // likely to be empty goes last: the narrow kernel first when sequences
+    // average at most NARROW_ROWS query rows, otherwise after the one-tile
+    // kernel (ahead of it, empty, it cost the chunked-prefill step 4 %).
+    const bool narrow_first = (long long)num_query_tokens * G <= (long long)NARROW_ROWS * num_seqs;
     auto tensor_core = [&](cudaStream_t on) {
         if (pairs) {
             const int rc2 = launch_prefill2(kv, tmk, tmv, pa_, (L.ptile_cap + 1) / 2 * num_kv_heads, on);
             if (rc2 != PA_OK) return rc2;
         }
-        if (narrow) {
+        auto narrow_launch = [&]() {
             PrefillArgs na = pa_;
             na.tiles = ntiles;
             na.scratch = ws + L.nscr;
-            const int rcn = launch_narrow(kv, tmk, tmv, na, narrow_grid(), on);
+            return launch_narrow(kv, tmk, tmv, na, narrow_grid(), on);
+        };
+        if (narrow && narrow_first) {
+            const int rcn = narrow_launch();
             if (rcn != PA_OK) return rcn;
         }
-        return launch_prefill(kv, tmk, tmv, pa_, L.ptile_cap * num_kv_heads, on);
+        const int rc1 = launch_prefill(kv, tmk, tmv, pa_, L.ptile_cap * num_kv_heads, on);
+        if (rc1 != PA_OK || !narrow || narrow_first) return rc1;
+        return narrow_launch();
     };
     int dev = -1;
     Side *side = cudaGetDevice(&dev) == cudaSuccess ? side_of(dev) : nullptr;
