@@ -36,6 +36,9 @@
 #ifndef PA_DECODE_MINB
 #define PA_DECODE_MINB 8
 #endif
+#ifndef PA_DECODE_SPLIT_FP8
+#define PA_DECODE_SPLIT_FP8 1
+#endif
 #ifndef PA_CAUSAL_L2
 #define PA_CAUSAL_L2 0
 #endif
@@ -261,7 +264,25 @@ struct Cfg {
     static constexpr int DATA = DEPTH * STAGE + 2 * QSLOT; // per consumer, a multiple of 1024
     static constexpr int CTRL_USED = (2 * DEPTH + 2) * 8 + 16 + 2 * 64;
     static constexpr int CTRL = (CTRL_USED + 255) / 256 * 256;   // per consumer: barriers and descriptors
-    static constexpr int SMEM = NC * (DATA + CTRL) + 1024;
+    // CTA shape.  In general one producer warp feeds NC consumer warps and
+    // the CTA's warps all hold what the consumer needs (the register count
+    // bounds the CTAs per SM).  FP8 single-token decode (SPLIT) is bound by
+    // the latency of its consumers, so it puts more of them on an SM: four
+    // producer warps (one warpgroup, each feeding one consumer) lower their
+    // registers to PROD_REGS and hand them to the four consumer warps (the
+    // other warpgroup, CONS_REGS), two CTAs per SM: 8 consumers per SM instead
+    // of 6.  The split must fit the pool the CTA is launched with (threads x
+    // LAUNCH_REGS); the host checks the compiled count before the first launch.
+    static constexpr bool SPLIT = FP8 && NT == 1 && PA_DECODE_SPLIT_FP8 != 0;
+    static constexpr int NCON = SPLIT ? 4 : NC;             // consumer warps per CTA
+    static constexpr int PER = SPLIT ? 1 : NC;              // consumers per producer warp
+    static constexpr int WARPS = SPLIT ? 8 : NWARPS;
+    static constexpr int MINB = SPLIT ? 2 : NT == 1 ? (FP8 ? PA_DECODE_MINB_FP8 : PA_DECODE_MINB) : PA_DECODE_MINB_WIDE;
+    static constexpr int LAUNCH_REGS = 65536 / (WARPS * 32 * MINB);
+    static constexpr int PROD_REGS = 80, CONS_REGS = 176;
+    static_assert(!SPLIT || (WARPS == 8 && 128 * PROD_REGS + 128 * CONS_REGS <= WARPS * 32 * LAUNCH_REGS),
+                  "register split");
+    static constexpr int SMEM = NCON * (DATA + CTRL) + 1024;
     static_assert(BOXES >= 1, "a tile row is at least one 128-byte box");
     static_assert(DATA % 1024 == 0, "stages must stay 1024-byte aligned for the 128-byte swizzle");
 };
@@ -324,7 +345,7 @@ template <int D, int NT, int KV>
 __device__ __forceinline__ ConsumerSmem consumer_smem(uint8_t *smem, int c) {
     using C = Cfg<D, NT, KV>;
     constexpr int DEPTH = C::DEPTH;
-    uint8_t *ctrl = smem + NC * C::DATA + c * C::CTRL;
+    uint8_t *ctrl = smem + C::NCON * C::DATA + c * C::CTRL;
     ConsumerSmem s;
     s.data = smem_u32(smem + c * C::DATA);
     s.full = reinterpret_cast<uint64_t *>(ctrl);
@@ -334,11 +355,13 @@ __device__ __forceinline__ ConsumerSmem consumer_smem(uint8_t *smem, int c) {
     return s;
 }
 
-// Producer warp: hands items to the consumers round-robin and keeps their
-// rings full.  All lanes run the loop; lane 0 issues the copies.
+// Producer warp: hands items to its consumers (C::PER of them from consumer
+// c0 on) round-robin and keeps their rings full.  All lanes run the loop;
+// lane 0 issues the copies.
 template <int D, int NT, bool CAUSAL, int KV>
-__device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMap *tmv, const DecodeArgs &a) {
+__device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMap *tmv, const DecodeArgs &a, int c0) {
     using C = Cfg<D, NT, KV>;
+    constexpr int NC = C::PER;   // this warp's consumers
     constexpr int DEPTH = C::DEPTH;
     const int lane = threadIdx.x & 31;
     const int total = a.hdr->total_items;
@@ -394,7 +417,7 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
     auto drain = [&]() {
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
-            const ConsumerSmem cs = consumer_smem<D, NT, KV>(smem, c);
+            const ConsumerSmem cs = consumer_smem<D, NT, KV>(smem, c0 + c);
             for (int slot = 0; slot < DEPTH; ++slot)
                 if (sc[c] > slot) {
                     const int k = slot + (sc[c] - 1 - slot) / DEPTH * DEPTH;
@@ -410,7 +433,7 @@ __device__ void producer(uint8_t *smem, const CUtensorMap *tmk, const CUtensorMa
 #pragma unroll
         for (int c = 0; c < NC; ++c) {
             if (done[c]) continue;
-            const ConsumerSmem cs = consumer_smem<D, NT, KV>(smem, c);
+            const ConsumerSmem cs = consumer_smem<D, NT, KV>(smem, c0 + c);
             const int s = sc[c] % DEPTH;
             const uint32_t full = smem_u32(&cs.full[s]);
             // every lane waits; the warp goes on only if all of them saw the
@@ -1041,15 +1064,14 @@ __device__ void consumer(uint8_t *smem, int c, const DecodeArgs &a) {
 }
 
 template <int D, int NT, bool CAUSAL, int KV>
-__global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? (KV == PA_KV_FP8_E4M3 ? PA_DECODE_MINB_FP8 : PA_DECODE_MINB)
-                                                       : PA_DECODE_MINB_WIDE) decode_kernel(const __grid_constant__ CUtensorMap tmk,
-                                                             const __grid_constant__ CUtensorMap tmv,
-                                                             const DecodeArgs a) {
+__global__ void __launch_bounds__(Cfg<D, NT, KV>::WARPS * 32, Cfg<D, NT, KV>::MINB)
+    decode_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, const DecodeArgs a) {
+    using C = Cfg<D, NT, KV>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int c = 0; c < NC; ++c) {
+        for (int c = 0; c < C::NCON; ++c) {
             const ConsumerSmem cs = consumer_smem<D, NT, KV>(smem, c);
             for (int s = 0; s < Cfg<D, NT, KV>::DEPTH; ++s) {
                 mbar_init(smem_u32(&cs.full[s]), 1);
@@ -1061,10 +1083,20 @@ __global__ void __launch_bounds__(NWARPS * 32, NT == 1 ? (KV == PA_KV_FP8_E4M3 ?
         fence_mbar_init();
     }
     __syncthreads();
-    if (warp == 0)
-        producer<D, NT, CAUSAL, KV>(smem, &tmk, &tmv, a);
-    else
-        consumer<D, NT, CAUSAL, KV>(smem, warp - 1, a);
+    if constexpr (C::SPLIT) {   // warpgroup 0: producers, warpgroup 1: their consumers
+        if (warp < 4) {
+            regs_decrease<C::PROD_REGS>();
+            producer<D, NT, CAUSAL, KV>(smem, &tmk, &tmv, a, warp);
+        } else {
+            regs_increase<C::CONS_REGS>();
+            consumer<D, NT, CAUSAL, KV>(smem, warp - 4, a);
+        }
+    } else {
+        if (warp == 0)
+            producer<D, NT, CAUSAL, KV>(smem, &tmk, &tmv, a, 0);
+        else
+            consumer<D, NT, CAUSAL, KV>(smem, warp - 1, a);
+    }
 }
 
 template <int D, int NT, bool CAUSAL, int KV>
@@ -1072,6 +1104,7 @@ int launch_decode(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeAr
                   cudaStream_t st) {
     using C = Cfg<D, NT, KV>;
     static int grid = 0;
+    static bool usable = false;
     static std::once_flag once;
     static cudaError_t init_err = cudaSuccess;
     std::call_once(once, [] {
@@ -1079,18 +1112,25 @@ int launch_decode(const CUtensorMap &tmk, const CUtensorMap &tmv, const DecodeAr
             cudaFuncSetAttribute(decode_kernel<D, NT, CAUSAL, KV>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
         if (init_err != cudaSuccess) return;
         int dev = 0, sms = 0, per_sm = 0;
+        cudaFuncAttributes fa;
         init_err = cudaGetDevice(&dev);
         if (init_err == cudaSuccess) init_err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (init_err == cudaSuccess)
             init_err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_kernel<D, NT, CAUSAL, KV>,
-                                                                     NWARPS * 32, C::SMEM);
+                                                                     C::WARPS * 32, C::SMEM);
+        if (init_err == cudaSuccess) init_err = cudaFuncGetAttributes(&fa, decode_kernel<D, NT, CAUSAL, KV>);
         if (init_err == cudaSuccess) grid = sms * (per_sm > 0 ? per_sm : 1);
+        // a register split is only run with the launch count it was sized for
+        // (a larger split than the pool would make the consumers' increase
+        // wait forever)
+        usable = init_err == cudaSuccess && (!C::SPLIT || fa.numRegs == C::LAUNCH_REGS);
     });
     if (init_err != cudaSuccess || grid <= 0) return PA_ERR_CUDA;
+    if (!usable) return PA_ERR_UNSUPPORTED;
     // no more CTAs than there can be items for their consumers
-    const long long need = (max_items + NC - 1) / NC;
+    const long long need = (max_items + C::NCON - 1) / C::NCON;
     const int g = (int)(need < grid ? (need > 0 ? need : 1) : grid);
-    decode_kernel<D, NT, CAUSAL, KV><<<g, NWARPS * 32, C::SMEM, st>>>(tmk, tmv, args);
+    decode_kernel<D, NT, CAUSAL, KV><<<g, C::WARPS * 32, C::SMEM, st>>>(tmk, tmv, args);
     return cuda_status(cudaGetLastError());
 }
 

@@ -78,19 +78,6 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 
 // ------------------------------------------------------- register split
 
-// Raise / lower this warpgroup's per-thread register count to N (a multiple of
-// 8 in 24 .. 256).  Every thread of the warpgroup executes it; the registers
-// come from the pool the CTA was launched with (threads x registers at
-// launch), so the shares of all warpgroups must add up to no more than that.
-template <uint32_t N>
-__device__ __forceinline__ void regs_increase() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void regs_decrease() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
-
 // ------------------------------------------------------------------ MMA
 
 // Shared-memory matrix descriptor for a 128-byte-swizzled operand tile (the
