@@ -36,8 +36,8 @@
 #ifndef PA_DECODE_MINB
 #define PA_DECODE_MINB 8
 #endif
-#ifndef PA_DECODE_SPLIT_FP8
-#define PA_DECODE_SPLIT_FP8 1
+#ifndef PA_DECODE_SPLIT
+#define PA_DECODE_SPLIT 1
 #endif
 #ifndef PA_CAUSAL_L2
 #define PA_CAUSAL_L2 0
@@ -266,14 +266,16 @@ struct Cfg {
     static constexpr int CTRL = (CTRL_USED + 255) / 256 * 256;   // per consumer: barriers and descriptors
     // CTA shape.  In general one producer warp feeds NC consumer warps and
     // the CTA's warps all hold what the consumer needs (the register count
-    // bounds the CTAs per SM).  FP8 single-token decode (SPLIT) is bound by
-    // the latency of its consumers, so it puts more of them on an SM: four
-    // producer warps (one warpgroup, each feeding one consumer) lower their
-    // registers to PROD_REGS and hand them to the four consumer warps (the
-    // other warpgroup, CONS_REGS), two CTAs per SM: 8 consumers per SM instead
-    // of 6.  The split must fit the pool the CTA is launched with (threads x
+    // bounds the CTAs per SM).  Single-token decode at head_dim 128 (SPLIT)
+    // is bound by its consumers' latency, so it gives them the registers the
+    // producers do not need: four producer warps (one warpgroup, each feeding
+    // one consumer) lower their registers to PROD_REGS and hand them to the
+    // four consumer warps (the other warpgroup, CONS_REGS), two CTAs per SM.
+    // FP8 (167 registers a consumer) gets 8 consumer warps per SM instead of
+    // 6; fp16/bf16 keep 8 but without the spills of a 128-register bound.  The
+    // split must fit the pool the CTA is launched with (threads x
     // LAUNCH_REGS); the host checks the compiled count before the first launch.
-    static constexpr bool SPLIT = FP8 && NT == 1 && PA_DECODE_SPLIT_FP8 != 0;
+    static constexpr bool SPLIT = NT == 1 && D == 128 && PA_DECODE_SPLIT != 0;
     static constexpr int NCON = SPLIT ? 4 : NC;             // consumer warps per CTA
     static constexpr int PER = SPLIT ? 1 : NC;              // consumers per producer warp
     static constexpr int WARPS = SPLIT ? 8 : NWARPS;
