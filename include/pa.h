@@ -62,7 +62,11 @@ enum {
     PA_ERR_STATE = -3,         /* allocator bookkeeping found an inconsistency */
     PA_ERR_WORKSPACE = -4,     /* workspace missing, misaligned or too small */
     PA_ERR_CUDA = -5,          /* a CUDA runtime call or launch failed */
-    PA_ERR_UNSUPPORTED = -6,   /* valid but not built: head_dim, block_size or group size */
+    PA_ERR_UNSUPPORTED = -6,   /* valid but not built: head_dim, block_size or group size;
+                                * also a decode kernel whose compiled register count
+                                * is not the one its register split was sized for
+                                * (a build of other sources or another compiler; it
+                                * is never launched then) */
     PA_ERR_TIMEOUT = -7        /* a kernel gave up waiting on its own copies (see pa_workspace_status) */
 };
 
