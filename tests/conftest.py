@@ -18,3 +18,14 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def golden_dir():
     return GOLDEN
+
+
+@pytest.fixture(scope="session", autouse=True)
+def built_library():
+    """Build libpa.so in-tree before the first test when the checkout has none
+    (build outputs are not under version control).  The library itself never
+    builds on demand: outside the tests a missing build still fails loudly."""
+    if not os.path.exists(os.path.join(ROOT, "paged_kv_cache_12_gb300", "libpa.so")):
+        from paged_kv_cache_12_gb300 import build
+
+        build.build()
